@@ -1,0 +1,230 @@
+"""CPU oracle (ctypes wrapper around ``tsi_oracle.c``).
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import this
+package.  The product library never loads it and shares no code with it.
+
+Every function computes in double precision from the stored bit patterns of its
+inputs; see the C file's header for the passages each function follows.
+"""
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "tsi_oracle.c")
+_LIB = os.path.join(_HERE, "libtsi_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+DTYPE_CODE = {"f32": 0, "bf16": 1, "e4m3": 2}
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (plain C11, no machine-specific flags)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-shared", "-fPIC", "-pthread",
+                               "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            vp, i32, i64, dbl = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_double
+            lib.tsio_decode.argtypes = [vp, i64, i32]
+            lib.tsio_decode.restype = dbl
+            lib.tsio_indexer_topk.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32,
+                                              vp, i64, vp, vp, vp, vp, i32]
+            lib.tsio_indexer_topk.restype = i32
+            lib.tsio_indexer_scores.argtypes = [vp, vp, vp, i32, i32, i32, i32, i64, vp]
+            lib.tsio_indexer_scores.restype = i64
+            lib.tsio_sparse_attn.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32,
+                                             dbl, vp, i32, vp, i64, vp, vp, vp, i32]
+            lib.tsio_sparse_attn.restype = i32
+            _lib = lib
+    return _lib
+
+
+def _as_bytes_array(x):
+    """Return (numpy array with the tensor's raw storage, dtype name)."""
+    import torch
+
+    if isinstance(x, np.ndarray):
+        if x.dtype == np.float32:
+            return np.ascontiguousarray(x), "f32"
+        raise TypeError("numpy inputs must be float32; pass torch tensors for bf16/e4m3")
+    x = x.detach().to("cpu").contiguous()
+    if x.dtype == torch.float32:
+        return x.numpy(), "f32"
+    if x.dtype == torch.bfloat16:
+        return x.view(torch.int16).numpy(), "bf16"
+    if x.dtype == torch.float8_e4m3fn:
+        return x.view(torch.uint8).numpy(), "e4m3"
+    raise TypeError(f"unsupported dtype {x.dtype}")
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def n_threads_default() -> int:
+    return max(1, os.cpu_count() or 1)
+
+
+def decode(x) -> np.ndarray:
+    """Decode every stored element of ``x`` to float64 (oracle's own decoder)."""
+    arr, dt = _as_bytes_array(x)
+    lib = _load()
+    flat = arr.reshape(-1)
+    return np.array([lib.tsio_decode(_ptr(flat), i, DTYPE_CODE[dt]) for i in range(flat.size)],
+                    dtype=np.float64).reshape(arr.shape)
+
+
+def _rows_arrays(B, T, rows):
+    if rows is None:
+        rb = np.repeat(np.arange(B, dtype=np.int32), T)
+        rt = np.tile(np.arange(T, dtype=np.int32), B)
+    else:
+        rows = np.asarray(rows, dtype=np.int64).reshape(-1)
+        rb = (rows // max(T, 1)).astype(np.int32)
+        rt = (rows % max(T, 1)).astype(np.int32)
+    return np.ascontiguousarray(rb), np.ascontiguousarray(rt)
+
+
+def indexer_topk(qI, kI, w, topk, kv_len=None, rows=None, n_threads=None):
+    """Top-k of I[t,s] = sum_j w[t,j] ReLU(qI[t,j].kI[s]) over s <= p_t.
+
+    qI [B,T,H_I,d_I], kI [B,S,d_I], w [B,T,H_I]; ``rows`` lists flattened query
+    rows b*T+t (default: all).  Returns (idx int32 [n,topk], score float64
+    [n,topk]) in rank order (score desc, index asc), padded with -1 / -inf.
+    """
+    B, T, H_I, d_I = qI.shape
+    rb, rt = _rows_arrays(B, T, rows)
+    flat = rb.astype(np.int64) * T + rt
+    q_rows = qI.reshape(B * T, H_I, d_I)
+    w_rows = w.reshape(B * T, H_I)
+    if rows is not None:
+        import torch
+
+        sel = torch.as_tensor(flat)
+        q_rows = q_rows[sel.to(q_rows.device)]
+        w_rows = w_rows[sel.to(w_rows.device)]
+    return indexer_topk_rows(q_rows, kI, w_rows, topk, T, flat, kv_len, n_threads)
+
+
+def indexer_topk_rows(q_rows, kI, w_rows, topk, T, rows, kv_len=None, n_threads=None):
+    """Like ``indexer_topk`` with query-side tensors already compacted to ``rows``."""
+    import torch
+
+    B, S, d_I = kI.shape
+    n, H_I = q_rows.shape[0], q_rows.shape[1]
+    rb, rt = _rows_arrays(B, T, rows)
+    assert rb.size == n
+    q_arr, qdt = _as_bytes_array(q_rows)
+    k_arr, kdt = _as_bytes_array(kI)
+    w_arr, wdt = _as_bytes_array(w_rows)
+    assert qdt == kdt
+    kv = None if kv_len is None else np.ascontiguousarray(
+        torch.as_tensor(kv_len).to("cpu", torch.int32).numpy())
+    idx = np.empty((n, topk), dtype=np.int32)
+    sc = np.empty((n, topk), dtype=np.float64)
+    rc = _load().tsio_indexer_topk(_ptr(q_arr), _ptr(k_arr), _ptr(w_arr), DTYPE_CODE[qdt],
+                                   DTYPE_CODE[wdt], B, T, S, H_I, d_I, topk, _ptr(kv), n,
+                                   _ptr(rb), _ptr(rt), _ptr(idx), _ptr(sc),
+                                   n_threads or n_threads_default())
+    if rc != 0:
+        raise RuntimeError(f"oracle indexer_topk failed ({rc})")
+    return idx, sc
+
+
+def indexer_scores(q_row, k_seq, w_row, p):
+    """All scores I[s], s = 0..p, of one query row (q_row [H_I,d_I], k_seq [S,d_I])."""
+    H_I, d_I = q_row.shape
+    q_arr, qdt = _as_bytes_array(q_row)
+    k_arr, kdt = _as_bytes_array(k_seq)
+    w_arr, wdt = _as_bytes_array(w_row)
+    assert qdt == kdt
+    out = np.empty(max(int(p) + 1, 1), dtype=np.float64)
+    n = _load().tsio_indexer_scores(_ptr(q_arr), _ptr(k_arr), _ptr(w_arr), DTYPE_CODE[qdt],
+                                    DTYPE_CODE[wdt], H_I, d_I, int(p), _ptr(out))
+    if n < 0:
+        raise RuntimeError("oracle indexer_scores failed")
+    return out[:n]
+
+
+def sparse_attn(q_rows, k, v, idx_rows, scale, T, rows, Dv=None, kv_len=None, n_threads=None):
+    """O[r,h,:] = softmax over row r's selected keys of scale*Q.K, applied to V.
+
+    q_rows [n,H,Dqk] (compacted to ``rows``, flattened b*T+t), k [B,S,Hkv,Dqk],
+    v [B,S,Hkv,Dv] or None (then the value is the first ``Dv`` dims of k),
+    idx_rows [n,topk] (entries outside [0, kv_len[b]) are not keys).
+    Returns float64 [n,H,Dv].
+    """
+    import torch
+
+    B, S, Hkv, Dqk = k.shape
+    n, H, Dqk2 = q_rows.shape
+    assert Dqk2 == Dqk
+    if v is not None:
+        Dv = v.shape[-1]
+    if Dv is None:
+        raise ValueError("Dv required when v is None")
+    rb, rt = _rows_arrays(B, T, rows)
+    assert rb.size == n
+    q_arr, qdt = _as_bytes_array(q_rows)
+    k_arr, kdt = _as_bytes_array(k)
+    v_arr = None
+    if v is not None:
+        v_arr, vdt = _as_bytes_array(v)
+        assert vdt == kdt
+    assert qdt == kdt
+    idx = np.ascontiguousarray(torch.as_tensor(idx_rows).to("cpu", torch.int32).numpy())
+    topk = idx.shape[-1]
+    assert idx.shape[0] == n
+    kv = None if kv_len is None else np.ascontiguousarray(
+        torch.as_tensor(kv_len).to("cpu", torch.int32).numpy())
+    out = np.empty((n, H, Dv), dtype=np.float64)
+    rc = _load().tsio_sparse_attn(_ptr(q_arr), _ptr(k_arr), _ptr(v_arr), DTYPE_CODE[qdt], B, T, S,
+                                  H, Hkv, Dqk, Dv, float(scale), _ptr(idx), topk, _ptr(kv), n,
+                                  _ptr(rb), _ptr(rt), _ptr(out), n_threads or n_threads_default())
+    if rc != 0:
+        raise RuntimeError(f"oracle sparse_attn failed ({rc})")
+    return out
+
+
+def dsa_group(indexer_inputs, layers, topk, scale, Dv=None, kv_len=None, share=True,
+              n_threads=None):
+    """One IndexShare group (1 Full + Shared layers) or, with share=False, per-layer DSA.
+
+    indexer_inputs: list of (qI, kI, w); with share=True only element 0 (the Full
+    layer's indexer) is used and its index rows serve every layer ("GLM-5.2
+    技术报告速览" §IndexShare: Shared layers inherit the nearest Full layer's index
+    set; each layer still attends with its own Q/K/V).  With share=False layer l
+    selects with indexer_inputs[l] (plain DSA).  layers: list of (Q, K, V) with
+    Q [B,T,H,Dqk].  Returns (list of idx [B*T,topk], list of O float64 [B*T,H,Dv]).
+    """
+    idxs, outs = [], []
+    full_idx = None
+    for l, (Q, K, V) in enumerate(layers):
+        if share:
+            if full_idx is None:
+                qI, kI, w = indexer_inputs[0]
+                full_idx, _ = indexer_topk(qI, kI, w, topk, kv_len, n_threads=n_threads)
+            idx = full_idx
+        else:
+            qI, kI, w = indexer_inputs[l]
+            idx, _ = indexer_topk(qI, kI, w, topk, kv_len, n_threads=n_threads)
+        B, T, H, Dqk = Q.shape
+        rows = np.arange(B * T)
+        outs.append(sparse_attn(Q.reshape(B * T, H, Dqk), K, V, idx, scale, T, rows, Dv=Dv,
+                                kv_len=kv_len, n_threads=n_threads))
+        idxs.append(idx)
+    return idxs, outs
