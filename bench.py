@@ -1,0 +1,444 @@
+"""Benchmark of the DSA indexer + top-k + IndexShare sparse-attention path on GB300.
+
+One step = the whole hot path over the L = 131072 prefill workload: 16 layers in
+4 IndexShare groups; per group one indexer + top-k call (the Full layer) and
+sparse attention for its 4 layers over the shared index rows.  Inputs are
+synthetic (seeded Gaussians, distinct per layer) and resident in HBM before the
+timed region; they are larger than L2, so L2 is not flushed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--config C]
+
+Prints one JSON line (rank 0).  With --impl reference the CPU oracle is timed on
+the host cores on a bounded row sample of the same workload.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "indexer+top-k query rows/s and group prefill tok/s @L=128K; % TC peak / HBM BW"
+UNIT = "tok/s"
+FP8_PER_BF16 = 2.0  # nominal dense FP8 : BF16 tensor ratio (4.5 : 2.25 PFLOP/s)
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def _kernel_sources_sha(names):
+    h = hashlib.sha256()
+    for n in names:
+        p = os.path.join(ROOT, "top_selection_indexer_gb300", "csrc", n)
+        if os.path.exists(p):
+            h.update(open(p, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def _profiled_traffic(kernel, src_files):
+    """DRAM bytes per launch from profiles/traffic.txt, if taken on the current source."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    sha = _kernel_sources_sha(src_files)
+    for line in open(path):
+        kv = dict(x.split("=", 1) for x in line.split() if "=" in x)
+        if kv.get("kernel") == kernel and kv.get("src_sha") == sha:
+            return float(kv["bytes_per_launch"])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower() in ("active", "1", "yes"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def run_gpu(args, rank, world):
+    import torch
+    import torch.distributed as dist
+
+    import top_selection_indexer_gb300 as tsi
+    from top_selection_indexer_gb300 import accounting
+    from workloads import get_config, make_attn_inputs, make_indexer_inputs
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    tsi.load()
+    cfg = get_config(args.config)
+    G, L = cfg.n_groups, cfg.T
+    stream = torch.cuda.current_stream()
+
+    # --- resident inputs (every layer distinct) --------------------------------------
+    t0 = time.time()
+    ind = [make_indexer_inputs(cfg, g, dev) for g in range(G)]
+    lay = [make_attn_inputs(cfg, l, dev) for l in range(cfg.n_layers)]
+    idx = torch.empty((cfg.B, cfg.T, cfg.topk), dtype=torch.int32, device=dev)
+    outs = [torch.empty((cfg.B, cfg.T, cfg.H, cfg.Dv), dtype=torch.bfloat16, device=dev)
+            for _ in range(cfg.group)]
+    ws_i = tsi.indexer_topk_workspace(cfg.B, cfg.T, cfg.S, cfg.H_I, cfg.d_I, cfg.topk,
+                                      tsi.E4M3 if cfg.qk_dtype == "e4m3" else tsi.BF16)
+    ws_a = tsi.sparse_attn_workspace(cfg.B, cfg.T, cfg.S, cfg.H, cfg.Hkv, cfg.Dqk, cfg.Dv,
+                                     cfg.topk)
+    ws = torch.empty(max(ws_i, ws_a, 16), dtype=torch.uint8, device=dev)
+    torch.cuda.synchronize()
+    setup_s = time.time() - t0
+
+    ev = {"idx": [], "attn": []}
+
+    def step(record):
+        for g in range(G):
+            qI, kI, w = ind[g]
+            if record:
+                a = torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+            tsi.indexer_topk(qI, kI, w, cfg.topk, idx=idx, workspace=ws, stream=stream)
+            if record:
+                b = torch.cuda.Event(enable_timing=True)
+                b.record(stream)
+                ev["idx"].append((a, b))
+            for l0 in range(cfg.group):
+                Q, K, V = lay[g * cfg.group + l0]
+                if record:
+                    a = torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                tsi.sparse_attn_group([Q], [K], None if V is None else [V], idx, cfg.scale,
+                                      outs=[outs[l0]], workspace=ws, stream=stream, Dv=cfg.Dv)
+                if record:
+                    b = torch.cuda.Event(enable_timing=True)
+                    b.record(stream)
+                    ev["attn"].append((a, b))
+
+    for _ in range(args.warmup):
+        step(False)
+    tsi.device_status(stream)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    launches0 = tsi.launch_count()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clocks:
+        t_start.record(stream)
+        for _ in range(args.steps):
+            step(True)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    launches = tsi.launch_count() - launches0
+    tsi.device_status(stream)
+    ms_total = t_start.elapsed_time(t_end)
+    if world > 1:
+        tt = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_total = float(tt.item())
+        dist.barrier()
+    ms_step = ms_total / args.steps
+    ms_idx = statistics.mean(a.elapsed_time(b) for a, b in ev["idx"])
+    ms_attn = statistics.mean(a.elapsed_time(b) for a, b in ev["attn"])
+
+    # --- rates and roofline ------------------------------------------------------------
+    rows = cfg.B * cfg.T
+    pairs = accounting.causal_pairs(cfg.B, cfg.T, cfg.S)
+    valid_k = accounting.selected_pairs(cfg.B, cfg.T, cfg.S, cfg.topk)
+    tok_per_group = cfg.B * cfg.T
+    value = world * G * tok_per_group / (ms_step / 1e3)  # group prefill tok/s, all ranks
+    peaks = _peaks()
+    qk_bytes = 1 if cfg.qk_dtype == "e4m3" else 2
+    idx_flops = accounting.indexer_flops(pairs, cfg.H_I, cfg.d_I)
+    tc_peak = peaks["bf16_tflops_sustained"] * (FP8_PER_BF16 if cfg.qk_dtype == "e4m3" else 1.0)
+    idx_achieved = idx_flops / (ms_idx / 1e3) / 1e12
+    attn_bytes = accounting.attn_bytes(valid_k, rows, cfg.H, cfg.Hkv, cfg.Dqk, cfg.Dv,
+                                       cfg.topk, cfg.v_from_k)
+    attn_achieved = attn_bytes / (ms_attn / 1e3) / 1e9
+    attn_tc = accounting.attn_flops(valid_k, cfg.H, cfg.Dqk, cfg.Dv) / (ms_attn / 1e3) / 1e12
+    attn_kernel = "tsi_attn_tc_kernel" if cfg.Dqk == 576 and cfg.Hkv == 1 else "attn_generic_kernel"
+    idx_kernel = "tsi_indexer_tc_kernel" if cfg.d_I == 128 and cfg.H_I == 64 else \
+        "indexer_generic_kernel"
+    roof_attn = {"kernel": attn_kernel, "bound": "hbm", "achieved": round(attn_achieved, 1),
+                 "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                 "frac": round(attn_achieved / peaks["hbm_gbs"], 4),
+                 "traffic": _profiled_traffic(attn_kernel, ["attn_tc.cu", "attn_generic.cu"]),
+                 "algorithmic_bytes_per_launch": attn_bytes, "ms_per_launch": round(ms_attn, 4),
+                 "tc_tflops": round(attn_tc, 1),
+                 "peak_source": f"{peaks['source']} hbm_gbs"}
+    roof_idx = {"kernel": idx_kernel, "bound": "tensor", "achieved": round(idx_achieved, 1),
+                "peak": round(tc_peak, 1), "unit": "TFLOP/s",
+                "frac": round(idx_achieved / tc_peak, 4),
+                "traffic": _profiled_traffic(idx_kernel, ["indexer_tc.cu", "indexer_generic.cu",
+                                                          "topk_select.cuh"]),
+                "algorithmic_flops_per_launch": idx_flops, "ms_per_launch": round(ms_idx, 4),
+                "peak_source": f"{peaks['source']} bf16 sustained x {FP8_PER_BF16:g} (fp8)"
+                               if cfg.qk_dtype == "e4m3" else f"{peaks['source']} bf16 sustained"}
+    dominant = roof_attn if ms_attn * cfg.n_layers >= ms_idx * G else roof_idx
+
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": f"{cfg.qk_dtype}+bf16", "data": "synthetic",
+        "config": {"workload": f"prefill L={L}, {cfg.n_layers} layers = {G} IndexShare groups "
+                               f"(1 Full + {cfg.group - 1} Shared), indexer H_I={cfg.H_I} "
+                               f"d_I={cfg.d_I} {cfg.qk_dtype}, k={cfg.topk}, MQA {cfg.H} heads "
+                               f"over a {cfg.Dqk}-d bf16 latent (value = first {cfg.Dv})",
+                   "config_id": cfg.id, "L": L, "layers": cfg.n_layers, "topk": cfg.topk,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2 (not flushed)"},
+        "indexer_topk_rows_per_s": round(world * rows / (ms_idx / 1e3), 1),
+        "tok_s_all_layers": round(world * tok_per_group / (ms_step / 1e3), 2),
+        "stage_ms": {"indexer_topk": round(ms_idx, 4), "sparse_attn_layer": round(ms_attn, 4)},
+        "roofline": dominant,
+        "roofline_indexer": roof_idx,
+        "roofline_attention": roof_attn,
+        "gpu_launches": int(launches),
+        "setup_s": round(setup_s, 1),
+    }
+    result["clocks"] = clocks.summary()
+
+    # --- end to end through the C ABI with host buffers ---------------------------------
+    if not args.no_e2e:
+        result["e2e"] = run_e2e(args, cfg, ind, lay, idx, outs, ws, stream, world)
+    return result
+
+
+def run_e2e(args, cfg, ind, lay, idx, outs, ws, stream, world):
+    """Same step with inputs copied host->device and results device->host inside the
+    timed region (pinned host buffers, one cudaMemcpyAsync per tensor)."""
+    import torch
+
+    import top_selection_indexer_gb300 as tsi
+
+    G = cfg.n_groups
+    pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)  # noqa: E731
+    h_ind = [tuple(pin(x) for x in ind[0])]
+    for hx, dx in zip(h_ind[0], ind[0]):
+        hx.copy_(dx)
+    Q0, K0, _ = lay[0]
+    h_Q, h_K = pin(Q0), pin(K0)
+    h_Q.copy_(Q0)
+    h_K.copy_(K0)
+    h_O = pin(outs[0])
+    h_idx = pin(idx)
+    h2d = d2h = 0
+    steps = max(1, min(args.steps, 2))
+
+    def step():
+        nonlocal h2d, d2h
+        for g in range(G):
+            qI, kI, w = ind[g]
+            for hx, dx in zip(h_ind[0], (qI, kI, w)):
+                dx.copy_(hx, non_blocking=True)
+                h2d += hx.numel() * hx.element_size()
+            tsi.indexer_topk(qI, kI, w, cfg.topk, idx=idx, workspace=ws, stream=stream)
+            h_idx.copy_(idx, non_blocking=True)
+            d2h += idx.numel() * idx.element_size()
+            for l0 in range(cfg.group):
+                Q, K, V = lay[g * cfg.group + l0]
+                Q.copy_(h_Q, non_blocking=True)
+                K.copy_(h_K, non_blocking=True)
+                h2d += h_Q.numel() * 2 + h_K.numel() * 2
+                tsi.sparse_attn_group([Q], [K], None, idx, cfg.scale, outs=[outs[l0]],
+                                      workspace=ws, stream=stream, Dv=cfg.Dv)
+                h_O.copy_(outs[l0], non_blocking=True)
+                d2h += h_O.numel() * 2
+
+    step()  # warm the copy path
+    torch.cuda.synchronize()
+    h2d = d2h = 0
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    return {"value": round(world * G * cfg.B * cfg.T / (ms / 1e3), 2), "unit": UNIT,
+            "h2d_bytes_per_step": h2d // steps, "d2h_bytes_per_step": d2h // steps,
+            "ms_per_step": round(ms, 2), "steps": steps,
+            "note": "every layer uploads Q and the latent from one pinned host buffer"}
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+def run_cpu_oracle(cfg_id, budget_s, on_device=None):
+    """Time the CPU oracle on a bounded, stratified row sample of one IndexShare group of
+    the workload and scale it to the metric (group prefill tok/s)."""
+    import torch
+
+    import oracle
+    from top_selection_indexer_gb300 import accounting
+    from workloads import get_config
+    from workloads.gen import draw
+
+    cfg = get_config(cfg_id)
+    cores = oracle.n_threads_default()
+    T, S = cfg.T, cfg.S
+    n_idx_rows = max(cores, 2 * cores)
+    rows = np.unique(np.linspace(T - 1, 0, n_idx_rows).astype(np.int64))
+    # inputs of the sampled rows only (same distributions as the workload)
+    kI = draw((cfg.B, S, cfg.d_I), cfg.qk_dist, cfg.qk_dtype, 1, "cpu", cfg.d_I)
+    q_rows = draw((len(rows), cfg.H_I, cfg.d_I), cfg.qk_dist, cfg.qk_dtype, 2, "cpu", cfg.d_I)
+    w_rows = draw((len(rows), cfg.H_I), cfg.w_dist, cfg.w_dtype, 3, "cpu")
+    t0 = time.perf_counter()
+    idx_rows, _ = oracle.indexer_topk_rows(q_rows, kI, w_rows, cfg.topk, T, rows)
+    t_idx = time.perf_counter() - t0
+    work_idx = sum(int(r) + 1 for r in rows)
+    t_idx_full = t_idx * accounting.causal_pairs(cfg.B, T, S) / work_idx
+    # attention: 4 layers on a subset of those rows
+    n_att = max(cores, 16)
+    arows = rows[:n_att]
+    K = draw((cfg.B, S, cfg.Hkv, cfg.Dqk), "normal", "bf16", 4, "cpu")
+    Qr = draw((len(arows), cfg.H, cfg.Dqk), "normal", "bf16", 5, "cpu")
+    t0 = time.perf_counter()
+    for _ in range(cfg.group):
+        oracle.sparse_attn(Qr, K, None, idx_rows[:len(arows)], cfg.scale, T, arows, Dv=cfg.Dv)
+    t_att = time.perf_counter() - t0
+    work_att = cfg.group * sum(min(cfg.topk, int(r) + 1) for r in arows)
+    t_att_full = t_att * cfg.group * accounting.selected_pairs(cfg.B, T, S, cfg.topk) / work_att
+    t_group = t_idx_full + t_att_full
+    return {"value": round(cfg.B * T / t_group, 4), "unit": UNIT, "cores": cores,
+            "kind": "oracle",
+            "sample": f"{len(rows)} stratified query rows (indexer + top-k, fp64) and "
+                      f"{len(arows)} of them x {cfg.group} layers (sparse attention, fp64) of "
+                      f"one L={T} IndexShare group; scaled by causal pairs / selected keys",
+            "sample_seconds": round(t_idx + t_att, 2)}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    vals = []
+    info = None
+    for _ in range(args.warmup + args.steps):
+        info = run_cpu_oracle(args.config, budget_s=20)
+        vals.append(info["value"])
+    v = statistics.mean(vals[args.warmup:]) if args.steps else vals[-1]
+    from workloads import get_config
+
+    cfg = get_config(args.config)
+    ms_step = cfg.n_groups * cfg.B * cfg.T / v * 1e3
+    return {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms_step, 1), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"prefill L={cfg.T}, {cfg.n_layers} layers = {cfg.n_groups} "
+                                   "IndexShare groups (CPU oracle on a row sample)",
+                       "config_id": cfg.id, "L": cfg.T, "layers": cfg.n_layers},
+            "cpu_baseline": {k: info[k] for k in ("kind", "cores", "sample")} | {"value": round(v, 4),
+                                                                                "unit": UNIT},
+            "e2e": {"value": round(v, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+# ----------------------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--config", type=int, default=4)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+
+    import torch
+    import torch.distributed as dist
+
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device(
+            "cuda", int(os.environ.get("LOCAL_RANK", 0))))
+    res = run_gpu(args, rank, world)
+    if rank == 0:
+        if not args.no_cpu:
+            res["cpu_baseline"] = run_cpu_oracle(args.config, budget_s=20)
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,140 @@
+/*
+ * tsi.h -- C ABI of the GB300 (sm_103a) DSA lightning-indexer + top-k + IndexShare
+ * sparse-attention library (libtsi.so).
+ *
+ * The library computes, on the GPU:
+ *   1. the lightning-indexer score I[t,s] = sum_j w[t,j] * ReLU(qI[t,j] . kI[s]) for
+ *      every causal pair s <= p_t ("GLM-5.2 技术报告速览", §IndexShare, the score
+ *      equation; one index key per position shared by all H_I heads);
+ *   2. the top-k keys of every query row, ties going to the lower key index
+ *      (same section: k = 2048 << L; "GLM-5: from Vibe Coding to Agentic Engineering"
+ *      (Chinese translation) §3.2 "DSA RL 要点" asks for a deterministic top-k);
+ *   3. sparse attention over those keys for every layer of an IndexShare group: the
+ *      Full layer's index rows are reused by the Shared layers, each layer with its
+ *      own Q/K/V ("GLM-5.2 技术报告速览" §IndexShare; "GLM 5.2: Built for Long Horizon
+ *      Tasks" §5.2 and discussion §3).
+ *
+ * Conventions shared by every entry point
+ *   - All tensor arguments are DEVICE pointers to dense row-major arrays owned by the
+ *     caller; the library never allocates, frees or retains them.  Arrays of pointers
+ *     (the per-layer q/k/v/out lists) are HOST arrays of device pointers.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every call only
+ *     enqueues work on `stream` and returns; results are ready when the stream is.
+ *   - Arguments are checked on the host before anything is launched.  A non-OK status
+ *     means nothing was launched (except TSI_ERR_CUDA, which reports a failed launch);
+ *     tsi_last_error() then describes the problem.
+ *   - Query row t of sequence b sits at position p = kv_len[b] - T + t (kv_len NULL:
+ *     kv_len[b] = S).  Prefill (T == S) gives p = t; decode (T == 1) gives
+ *     p = kv_len[b] - 1.  Device-side kv_len values are clamped to [0, S].
+ *   - Device-side waits are bounded; a wait that runs out, or a failed device check,
+ *     sets a device error word instead of trapping.  tsi_device_status() reads it.
+ */
+#ifndef TSI_H
+#define TSI_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    TSI_OK = 0,
+    TSI_ERR_INVALID_ARG = 1,   /* bad shape, NULL pointer, misaligned pointer */
+    TSI_ERR_UNSUPPORTED = 2,   /* valid request this build does not implement */
+    TSI_ERR_WORKSPACE = 3,     /* workspace NULL or smaller than the query says */
+    TSI_ERR_CUDA = 4,          /* a CUDA runtime call or kernel launch failed */
+    TSI_ERR_TIMEOUT = 5,       /* a bounded device-side wait ran out */
+    TSI_ERR_DEVICE_ASSERT = 6  /* a device-side consistency check failed */
+} tsi_status;
+
+/* Element types.  E4M3 is the FP8 "fn" format (bias 7, no infinities); stored bytes
+ * are the values (no scale factors). */
+typedef enum { TSI_F32 = 0, TSI_BF16 = 1, TSI_E4M3 = 2 } tsi_dtype;
+
+#define TSI_MAX_TOPK 2048
+
+/*
+ * Workspace bytes needed by tsi_indexer_topk for these sizes (0 when none is needed).
+ * The workspace holds per-split candidate lists when rows are few and key ranges are
+ * split across thread blocks (decode).
+ */
+size_t tsi_indexer_topk_workspace(int B, int T, int S, int H_I, int d_I, int topk,
+                                  int qk_dtype);
+
+/*
+ * Lightning-indexer score + causal top-k ("GLM-5.2 技术报告速览", §IndexShare).
+ *
+ *   qI     [B, T, H_I, d_I]  qk_dtype (F32, BF16 or E4M3)   index queries
+ *   kI     [B, S, d_I]       qk_dtype                        index-key cache
+ *   w      [B, T, H_I]       w_dtype (F32 or BF16)            per-head gate weights
+ *   kv_len [B] int32 or NULL                                  cached length per sequence
+ *   idx    [B, T, topk] int32 (out)  key positions in rank order: higher score first,
+ *          equal scores by lower position; rows with fewer than topk causal keys are
+ *          padded with -1 after their p+1 keys.
+ *   score  [B, T, topk] float (out, may be NULL)  the fp32 score of each idx entry,
+ *          -inf for padding.
+ *
+ * Scores are accumulated in fp32 (tensor cores for BF16/E4M3 with H_I = 64,
+ * d_I = 128; CUDA cores otherwise).  1 <= topk <= TSI_MAX_TOPK, d_I <= 256,
+ * H_I <= 128.  Pointers must be 16-byte aligned.  Requires
+ * workspace_bytes >= tsi_indexer_topk_workspace(...).
+ */
+tsi_status tsi_indexer_topk(const void* qI, const void* kI, const void* w, int qk_dtype,
+                            int w_dtype, int B, int T, int S, int H_I, int d_I, int topk,
+                            const int32_t* kv_len, int32_t* idx, float* score, void* workspace,
+                            size_t workspace_bytes, void* stream);
+
+/* Workspace bytes needed by tsi_sparse_attn_group for these sizes (0 when none). */
+size_t tsi_sparse_attn_workspace(int B, int T, int S, int H, int Hkv, int Dqk, int Dv,
+                                 int topk);
+
+/*
+ * Sparse attention for the n_layers layers of one IndexShare group over ONE shared
+ * index buffer ("GLM-5.2 技术报告速览" §IndexShare; "GLM 5.2: Built for Long Horizon
+ * Tasks" §5.2): for every layer l, query row (b,t) and head h,
+ *
+ *   O_l[b,t,h,:] = sum_{s in S} softmax_s(scale * Q_l[b,t,h,:] . K_l[b,s,g,:]) V_l[b,s,g,:]
+ *
+ * with g = h / (H / Hkv) and S the entries of idx[b,t,:] inside [0, kv_len[b]) (the -1
+ * padding is not a key).  A row with no key gets O = 0.
+ *
+ *   q[l]   [B, T, H, Dqk]   bf16
+ *   k[l]   [B, S, Hkv, Dqk] bf16
+ *   v[l]   [B, S, Hkv, Dv]  bf16, or v == NULL / v[l] == NULL: the value is the first
+ *          Dv dims of the key row (MLA latent: 576 = 512 + 64, value = first 512)
+ *   idx    [B, T, topk] int32, shared by all layers (the Full layer's selection)
+ *   out[l] [B, T, H, Dv]    bf16 (out)
+ *
+ * Softmax and accumulation run in fp32.  H % Hkv == 0, Dqk <= 576, Dv <= 512,
+ * 1 <= topk <= TSI_MAX_TOPK.  Pointers must be 16-byte aligned.  Layers run one after
+ * another on `stream`.
+ */
+tsi_status tsi_sparse_attn_group(int n_layers, const void* const* q, const void* const* k,
+                                 const void* const* v, int B, int T, int S, int H, int Hkv,
+                                 int Dqk, int Dv, float scale, const int32_t* idx, int topk,
+                                 const int32_t* kv_len, void* const* out, void* workspace,
+                                 size_t workspace_bytes, void* stream);
+
+/*
+ * Waits for `stream`, then reads and clears the device error word of the current
+ * device.  Returns TSI_OK, TSI_ERR_TIMEOUT (a bounded wait ran out),
+ * TSI_ERR_DEVICE_ASSERT (a device check failed) or TSI_ERR_CUDA.
+ */
+tsi_status tsi_device_status(void* stream);
+
+/* Message for the last non-OK status returned on this host thread ("" if none). */
+const char* tsi_last_error(void);
+
+/* Number of kernels this library has launched in this process (all threads). */
+uint64_t tsi_launch_count(void);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int tsi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TSI_H */

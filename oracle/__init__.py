@@ -99,6 +99,16 @@ def _rows_arrays(B, T, rows):
     return np.ascontiguousarray(rb), np.ascontiguousarray(rt)
 
 
+def _take_rows(x, sel):
+    """x[sel] on the CPU, also for float8 (gathered through a same-size integer view)."""
+    import torch
+
+    x = x.detach().to("cpu")
+    if x.dtype == torch.float8_e4m3fn:
+        return x.view(torch.uint8)[sel].view(torch.float8_e4m3fn)
+    return x[sel]
+
+
 def indexer_topk(qI, kI, w, topk, kv_len=None, rows=None, n_threads=None):
     """Top-k of I[t,s] = sum_j w[t,j] ReLU(qI[t,j].kI[s]) over s <= p_t.
 
@@ -106,17 +116,19 @@ def indexer_topk(qI, kI, w, topk, kv_len=None, rows=None, n_threads=None):
     rows b*T+t (default: all).  Returns (idx int32 [n,topk], score float64
     [n,topk]) in rank order (score desc, index asc), padded with -1 / -inf.
     """
+    import torch
+
     B, T, H_I, d_I = qI.shape
     rb, rt = _rows_arrays(B, T, rows)
     flat = rb.astype(np.int64) * T + rt
     q_rows = qI.reshape(B * T, H_I, d_I)
     w_rows = w.reshape(B * T, H_I)
     if rows is not None:
-        import torch
-
         sel = torch.as_tensor(flat)
-        q_rows = q_rows[sel.to(q_rows.device)]
-        w_rows = w_rows[sel.to(w_rows.device)]
+        if int(sel.min()) < 0 or int(sel.max()) >= B * T:
+            raise IndexError("rows out of range")
+        q_rows = _take_rows(q_rows, sel)
+        w_rows = _take_rows(w_rows, sel)
     return indexer_topk_rows(q_rows, kI, w_rows, topk, T, flat, kv_len, n_threads)
 
 

@@ -1,0 +1,118 @@
+"""The C ABI: the library loads, exports every declared symbol, and rejects bad
+arguments on the host before launching anything (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import top_selection_indexer_gb300 as tsi
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "tsi.h")
+
+FAKE = 0x10000  # aligned, never dereferenced: every call below fails validation first
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(tsi_[a-z_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from top_selection_indexer_gb300 import _build
+
+    _build.build()
+    return tsi.load()
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for n in ("tsi_indexer_topk", "tsi_sparse_attn_group", "tsi_indexer_topk_workspace",
+              "tsi_sparse_attn_workspace", "tsi_last_error", "tsi_device_status"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+    assert set(_declared()) <= set(tsi.EXPORTS)
+    assert lib.tsi_version() >= 100
+
+
+def _idx(lib, **kw):
+    a = dict(qI=FAKE, kI=FAKE, w=FAKE, qk=tsi.E4M3, wdt=tsi.BF16, B=1, T=8, S=8, H_I=64,
+             d_I=128, topk=4, kv=None, idx=FAKE, score=None, ws=None, wsb=0, stream=None)
+    a.update(kw)
+    return lib.tsi_indexer_topk(a["qI"], a["kI"], a["w"], a["qk"], a["wdt"], a["B"], a["T"],
+                                a["S"], a["H_I"], a["d_I"], a["topk"], a["kv"], a["idx"],
+                                a["score"], a["ws"], a["wsb"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(topk=0), tsi.ERR_UNSUPPORTED),
+    (dict(topk=2049), tsi.ERR_UNSUPPORTED),
+    (dict(B=-1), tsi.ERR_INVALID_ARG),
+    (dict(qk=7), tsi.ERR_INVALID_ARG),
+    (dict(wdt=tsi.E4M3), tsi.ERR_INVALID_ARG),
+    (dict(H_I=0), tsi.ERR_INVALID_ARG),
+    (dict(H_I=100, d_I=200), tsi.ERR_UNSUPPORTED),
+    (dict(idx=None), tsi.ERR_INVALID_ARG),
+    (dict(qI=FAKE + 4), tsi.ERR_INVALID_ARG),
+    (dict(B=8, T=1, S=131072, topk=2048, ws=None, wsb=0), tsi.ERR_WORKSPACE),
+])
+def test_indexer_rejects_bad_arguments(lib, kw, status):
+    st = _idx(lib, **kw)
+    assert st == status, lib.tsi_last_error()
+    assert lib.tsi_last_error()
+
+
+def test_indexer_empty_batch_is_a_noop(lib):
+    assert _idx(lib, B=0, qI=None, kI=None, w=None, idx=None) == tsi.OK
+    assert _idx(lib, T=0, qI=None, kI=None, w=None, idx=None) == tsi.OK
+
+
+def test_decode_needs_workspace(lib):
+    need = lib.tsi_indexer_topk_workspace(8, 1, 131072, 64, 128, 2048, tsi.E4M3)
+    assert need > 0
+    st = _idx(lib, B=8, T=1, S=131072, topk=2048, ws=FAKE, wsb=need - 1)
+    assert st == tsi.ERR_WORKSPACE
+
+
+def _attn(lib, n=1, **kw):
+    P = ctypes.c_void_p * n
+    a = dict(q=P(*[FAKE] * n), k=P(*[FAKE] * n), v=None, B=1, T=4, S=4, H=64, Hkv=1,
+             Dqk=576, Dv=512, scale=1 / 24, idx=FAKE, topk=4, kv=None, out=P(*[FAKE] * n),
+             ws=None, wsb=0, stream=None)
+    a.update(kw)
+    return lib.tsi_sparse_attn_group(n, a["q"], a["k"], a["v"], a["B"], a["T"], a["S"], a["H"],
+                                     a["Hkv"], a["Dqk"], a["Dv"], a["scale"], a["idx"],
+                                     a["topk"], a["kv"], a["out"], a["ws"], a["wsb"],
+                                     a["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(topk=0), tsi.ERR_UNSUPPORTED),
+    (dict(topk=4096), tsi.ERR_UNSUPPORTED),
+    (dict(H=6, Hkv=4), tsi.ERR_INVALID_ARG),
+    (dict(Dqk=1024), tsi.ERR_UNSUPPORTED),
+    (dict(Dqk=256, Dv=512), tsi.ERR_UNSUPPORTED),  # value from key needs Dv <= Dqk
+    (dict(scale=float("inf")), tsi.ERR_INVALID_ARG),
+    (dict(idx=None), tsi.ERR_INVALID_ARG),
+    (dict(idx=FAKE + 8), tsi.ERR_INVALID_ARG),
+    (dict(B=-2), tsi.ERR_INVALID_ARG),
+])
+def test_attn_rejects_bad_arguments(lib, kw, status):
+    st = _attn(lib, **kw)
+    assert st == status, lib.tsi_last_error()
+
+
+def test_attn_null_layer_pointer(lib):
+    P = ctypes.c_void_p * 2
+    assert _attn(lib, n=2, q=P(FAKE, None)) == tsi.ERR_INVALID_ARG
+
+
+def test_attn_zero_layers_is_a_noop(lib):
+    assert _attn(lib, n=1, B=0) == tsi.OK

@@ -1,1 +1,189 @@
-"""GB300-native DSA lightning indexer + top-k + IndexShare sparse attention."""
+"""GB300-native DSA lightning indexer + top-k + IndexShare sparse attention.
+
+Thin ctypes binding over ``libtsi.so`` (see ``include/tsi.h``): it checks that
+tensors are CUDA and contiguous, allocates outputs / workspace with torch when
+the caller passes none, and forwards device pointers and sizes.  Every step of
+the computation runs in the library's CUDA kernels; there is no fallback.
+"""
+import ctypes
+import os
+import threading
+
+from . import accounting  # noqa: F401
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libtsi.so")
+_lib = None
+_lock = threading.Lock()
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT, ERR_DEVICE_ASSERT = \
+    range(7)
+F32, BF16, E4M3 = 0, 1, 2
+MAX_TOPK = 2048
+
+EXPORTS = ("tsi_indexer_topk_workspace", "tsi_indexer_topk", "tsi_sparse_attn_workspace",
+           "tsi_sparse_attn_group", "tsi_device_status", "tsi_last_error", "tsi_version",
+           "tsi_launch_count")
+
+
+class TSIError(RuntimeError):
+    def __init__(self, status, msg):
+        super().__init__(f"status {status}: {msg}")
+        self.status = status
+
+
+def load():
+    """Load libtsi.so; raises if it has not been built (no silent fallback)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                                   "`python -c 'import __graft_entry__ as g; g.build()'`")
+            lib = ctypes.CDLL(LIB_PATH)
+            vp, i32, sz, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_float
+            lib.tsi_indexer_topk_workspace.argtypes = [i32] * 7
+            lib.tsi_indexer_topk_workspace.restype = sz
+            lib.tsi_indexer_topk.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32,
+                                             vp, vp, vp, vp, sz, vp]
+            lib.tsi_indexer_topk.restype = i32
+            lib.tsi_sparse_attn_workspace.argtypes = [i32] * 8
+            lib.tsi_sparse_attn_workspace.restype = sz
+            lib.tsi_sparse_attn_group.argtypes = [i32, vp, vp, vp, i32, i32, i32, i32, i32, i32,
+                                                  i32, f32, vp, i32, vp, vp, vp, sz, vp]
+            lib.tsi_sparse_attn_group.restype = i32
+            lib.tsi_device_status.argtypes = [vp]
+            lib.tsi_device_status.restype = i32
+            lib.tsi_last_error.argtypes = []
+            lib.tsi_last_error.restype = ctypes.c_char_p
+            lib.tsi_version.argtypes = []
+            lib.tsi_version.restype = i32
+            lib.tsi_launch_count.argtypes = []
+            lib.tsi_launch_count.restype = ctypes.c_uint64
+            _lib = lib
+    return _lib
+
+
+def launch_count() -> int:
+    """Kernels the library has launched in this process so far."""
+    return int(load().tsi_launch_count())
+
+
+def last_error() -> str:
+    return load().tsi_last_error().decode()
+
+
+def _check(st):
+    if st != OK:
+        raise TSIError(st, last_error())
+
+
+def _dtype_code(t):
+    import torch
+
+    code = {torch.float32: F32, torch.bfloat16: BF16, torch.float8_e4m3fn: E4M3}.get(t.dtype)
+    if code is None:
+        raise TypeError(f"unsupported dtype {t.dtype}")
+    return code
+
+
+def _dev(t, name):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _stream_handle(stream):
+    import torch
+
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def indexer_topk_workspace(B, T, S, H_I, d_I, topk, qk_dtype) -> int:
+    return load().tsi_indexer_topk_workspace(B, T, S, H_I, d_I, topk, qk_dtype)
+
+
+def indexer_topk(qI, kI, w, topk, kv_len=None, idx=None, score=None, workspace=None,
+                 stream=None, want_score=False):
+    """Top-k key positions of the lightning-indexer score (``tsi_indexer_topk``).
+
+    qI [B,T,H_I,d_I], kI [B,S,d_I] (f32/bf16/e4m3), w [B,T,H_I] (f32/bf16),
+    kv_len [B] int32 or None.  Returns idx [B,T,topk] int32 (and score float32
+    when ``want_score`` or ``score`` is given).
+    """
+    import torch
+
+    B, T, H_I, d_I = qI.shape
+    S = kI.shape[1]
+    if idx is None:
+        idx = torch.empty((B, T, topk), dtype=torch.int32, device=qI.device)
+    if score is None and want_score:
+        score = torch.empty((B, T, topk), dtype=torch.float32, device=qI.device)
+    code = _dtype_code(qI)
+    if _dtype_code(kI) != code:
+        raise TypeError("qI and kI must share a dtype")
+    need = indexer_topk_workspace(B, T, S, H_I, d_I, topk, code)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=qI.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().tsi_indexer_topk(
+        _dev(qI, "qI"), _dev(kI, "kI"), _dev(w, "w"), code, _dtype_code(w), B, T, S, H_I, d_I,
+        topk, _dev(kv_len, "kv_len"), _dev(idx, "idx"), _dev(score, "score"),
+        _dev(workspace, "workspace"), ws_bytes, _stream_handle(stream)))
+    return (idx, score) if score is not None else idx
+
+
+def sparse_attn_workspace(B, T, S, H, Hkv, Dqk, Dv, topk) -> int:
+    return load().tsi_sparse_attn_workspace(B, T, S, H, Hkv, Dqk, Dv, topk)
+
+
+def sparse_attn_group(qs, ks, vs, idx, scale, kv_len=None, outs=None, workspace=None,
+                      stream=None, Dv=None):
+    """Sparse attention of every layer of one IndexShare group over the shared ``idx``.
+
+    qs: list of Q [B,T,H,Dqk] bf16; ks: list of K [B,S,Hkv,Dqk] bf16; vs: list of
+    V [B,S,Hkv,Dv] bf16, or None (value = first ``Dv`` dims of K).  Returns the
+    list of O [B,T,H,Dv] bf16.
+    """
+    import torch
+
+    n = len(qs)
+    B, T, H, Dqk = qs[0].shape
+    S, Hkv = ks[0].shape[1], ks[0].shape[2]
+    if vs is not None:
+        Dv = vs[0].shape[-1]
+    if Dv is None:
+        raise ValueError("Dv is required when the value comes from the key")
+    topk = idx.shape[-1]
+    if outs is None:
+        outs = [torch.empty((B, T, H, Dv), dtype=torch.bfloat16, device=qs[0].device)
+                for _ in range(n)]
+    need = sparse_attn_workspace(B, T, S, H, Hkv, Dqk, Dv, topk)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=qs[0].device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    for name, lst in (("q", qs), ("k", ks), ("out", outs)) + ((("v", vs),) if vs else ()):
+        for t in lst:
+            if t.dtype != torch.bfloat16:
+                raise TypeError(f"{name} tensors must be bfloat16")
+    P = ctypes.c_void_p * n
+    qp = P(*[_dev(t, "q") for t in qs])
+    kp = P(*[_dev(t, "k") for t in ks])
+    vp = P(*[_dev(t, "v") for t in vs]) if vs is not None else None
+    op = P(*[_dev(t, "out") for t in outs])
+    _check(load().tsi_sparse_attn_group(
+        n, qp, kp, vp, B, T, S, H, Hkv, Dqk, Dv, float(scale), _dev(idx, "idx"), topk,
+        _dev(kv_len, "kv_len"), op, _dev(workspace, "workspace"), ws_bytes,
+        _stream_handle(stream)))
+    return outs
+
+
+def device_status(stream=None):
+    """Synchronize and read / clear the device error word (raises on a set flag)."""
+    _check(load().tsi_device_status(_stream_handle(stream)))

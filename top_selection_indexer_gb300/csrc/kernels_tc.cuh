@@ -1,0 +1,22 @@
+// Host-side interface of the tensor-core (tcgen05 / TMEM / TMA) kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "attn_generic.cuh"
+#include "indexer_generic.cuh"
+
+namespace tsi {
+
+// Indexer + top-k with tcgen05 MMAs (BF16 or E4M3 inputs, H_I = 64, d_I = 128).
+bool tc_indexer_supported(int qk_dtype, int H_I, int d_I);
+size_t tc_indexer_workspace_bytes(int B, int T, int S, int topk);
+cudaError_t launch_indexer_tc(const IndexerArgs& a, void* workspace, cudaStream_t st);
+
+// Sparse MQA attention over a 576-d latent (value = first 512 dims), H = 64.
+bool tc_attn_supported(int H, int Hkv, int Dqk, int Dv, bool v_from_k);
+size_t tc_attn_workspace_bytes(int B, int T, int H, int Dv, int topk);
+cudaError_t launch_attn_tc(const AttnArgs& a, void* workspace, cudaStream_t st);
+
+}  // namespace tsi

@@ -1,0 +1,278 @@
+// Streaming exact top-k selection in shared memory.
+//
+// Every candidate is a 64-bit key  (order(score) << 32) | (0xFFFFFFFF - s):  the upper
+// word orders fp32 scores as unsigned integers (-0.0 folded onto +0.0), the lower word
+// makes a lower key position compare higher.  Keys are therefore unique and their
+// unsigned order is exactly the rank order "higher score first, equal scores by lower
+// position" (the deterministic top-k that "GLM-5: from Vibe Coding to Agentic
+// Engineering" (Chinese translation) §3.2 asks for, with the lower-index tie rule).
+//
+// A group of NT threads owns one selector: a buffer of CAP keys, an admission
+// threshold `thr` and a 256-bin histogram.  Keys >= thr are appended; when the buffer
+// is nearly full a radix select over the key bits finds the bound T with exactly k
+// keys >= T, drops the rest and raises thr to T.  Invariant: every dropped key is
+// smaller than k kept keys, so the buffer always holds the top k of all offered keys.
+#pragma once
+
+#include "tsi_common.cuh"
+
+namespace tsi {
+
+__device__ __forceinline__ uint32_t score_order_bits(float x) {
+    uint32_t u = __float_as_uint(x);
+    if (u == 0x80000000u) u = 0u;  // -0.0 ranks as +0.0
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float order_bits_score(uint32_t o) {
+    uint32_t u = (o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o;
+    return __uint_as_float(u);
+}
+
+__device__ __forceinline__ uint64_t make_key(float score, uint32_t s) {
+    return (static_cast<uint64_t>(score_order_bits(score)) << 32) |
+           static_cast<uint64_t>(0xFFFFFFFFu - s);
+}
+
+__device__ __forceinline__ int32_t key_position(uint64_t key) {
+    return static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(key));
+}
+
+__device__ __forceinline__ float key_score(uint64_t key) {
+    return order_bits_score(static_cast<uint32_t>(key >> 32));
+}
+
+// Shared-memory footprint of one selector (bytes), excluding alignment slack.
+template <int CAP>
+constexpr int selector_smem_bytes() {
+    return CAP * 8 + 256 * 4 + 8 * 4 + 8;
+}
+
+template <int NT, int CAP>
+struct TopKSelector {
+    static_assert(NT % 32 == 0, "whole warps");
+    static_assert(CAP % NT == 0, "CAP must be a multiple of NT");
+    static_assert(CAP >= 2 * TSI_MAX_TOPK, "room for k keys plus one round");
+
+    uint64_t* buf;   // [CAP]
+    unsigned* hist;  // [256]
+    int* ctl;        // [8]: 0 count, 1 digit, 2 above, 3 in-bin, 4 write cursor
+    uint64_t* thr;   // admission threshold
+    int tid;         // 0..NT-1 within the group
+    int bar_id;      // named barrier of the group
+    unsigned* err;   // device error word: consistency checks record kErrAssert here
+
+    // Carve the selector out of `smem` (8-byte aligned); returns the bytes used.
+    __device__ int bind(uint8_t* smem, int tid_, int bar_id_, unsigned* err_) {
+        err = err_;
+        buf = reinterpret_cast<uint64_t*>(smem);
+        hist = reinterpret_cast<unsigned*>(smem + CAP * 8);
+        ctl = reinterpret_cast<int*>(smem + CAP * 8 + 256 * 4);
+        thr = reinterpret_cast<uint64_t*>(smem + CAP * 8 + 256 * 4 + 8 * 4);
+        tid = tid_;
+        bar_id = bar_id_;
+        return selector_smem_bytes<CAP>();
+    }
+
+    __device__ __forceinline__ void sync() const { named_bar(bar_id, NT); }
+
+    __device__ __forceinline__ int count() const {
+        return *reinterpret_cast<volatile int*>(&ctl[0]);
+    }
+
+    __device__ void reset() {
+        sync();
+        if (tid == 0) {
+            ctl[0] = 0;
+            *thr = 0ull;
+        }
+        sync();
+    }
+
+    // Collective over the NT threads: each thread may carry one key.  The caller has
+    // made room (count() + NT <= CAP) with make_room().
+    __device__ __forceinline__ void offer(bool has, uint64_t key) {
+        const int lane = threadIdx.x & 31;
+        const bool take = has && key >= *thr;
+        const unsigned m = __ballot_sync(kFull, take);
+        if (m) {
+            const int leader = __ffs(m) - 1;
+            int base = 0;
+            if (lane == leader) base = atomicAdd(&ctl[0], __popc(m));
+            base = __shfl_sync(kFull, base, leader);
+            const int pos = base + __popc(m & ((1u << lane) - 1u));
+            if (take) {
+                if (pos < CAP)
+                    buf[pos] = key;
+                else
+                    atomicOr(err, kErrAssert);
+            }
+        }
+    }
+
+    // Collective: the held count, read by every thread of the group.  The second barrier
+    // keeps any thread from offering (and bumping the count) before all have read it, so
+    // every thread takes the same branch on the value.
+    __device__ __forceinline__ int settled_count() {
+        sync();
+        const int n = count();
+        sync();
+        return n;
+    }
+
+    // Collective: ensure room for one more round of NT offers.
+    __device__ __forceinline__ void make_room(int k) {
+        const int n = settled_count();
+        if (n > CAP - NT) compact(k, n);
+    }
+
+    // Collective: keep exactly the k largest of the n held keys (no-op when n <= k).
+    // `n` must be a settled_count() result (the same value in every thread).
+    __device__ void compact(int k, int n) {
+        if (n <= k) return;
+        uint64_t prefix = 0ull;
+        int need = k;
+        for (int shift = 56; shift >= 0; shift -= 8) {
+            const uint64_t mask = (shift == 56) ? 0ull : (~0ull << (shift + 8));
+            for (int i = tid; i < 256; i += NT) hist[i] = 0u;
+            sync();
+            // every thread has read the previous pass's ctl[1..3] before the barrier above
+            if (tid == 0) ctl[1] = -1;
+            for (int base = 0; base < n; base += NT) {
+                const int i = base + tid;
+                const uint64_t x = i < n ? buf[i] : 0ull;
+                const bool in = (i < n) && ((x & mask) == prefix);
+                const unsigned d = in ? static_cast<unsigned>((x >> shift) & 255u) : 256u;
+                const unsigned peers = __match_any_sync(kFull, d);
+                if (in && (threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[d], __popc(peers));
+            }
+            sync();
+            if (tid < 32) {
+                // lane l scans bins 255-8l .. 248-8l (descending key order)
+                unsigned c[8];
+                unsigned sum = 0;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    c[j] = hist[255 - (tid * 8 + j)];
+                    sum += c[j];
+                }
+                unsigned incl = sum;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const unsigned v = __shfl_up_sync(kFull, incl, o);
+                    if (tid >= o) incl += v;
+                }
+                const unsigned excl = incl - sum;
+                if (excl < static_cast<unsigned>(need) && static_cast<unsigned>(need) <= incl) {
+                    unsigned above = excl;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        if (above + c[j] >= static_cast<unsigned>(need)) {
+                            ctl[1] = 255 - (tid * 8 + j);
+                            ctl[2] = static_cast<int>(above);
+                            ctl[3] = static_cast<int>(c[j]);
+                            break;
+                        }
+                        above += c[j];
+                    }
+                }
+            }
+            sync();
+            const int d = ctl[1];
+            if (d < 0) {  // no bin holds the k-th key: counts are inconsistent
+                if (tid == 0) atomicOr(err, kErrAssert);
+                break;
+            }
+            const int above = ctl[2];
+            const int inbin = ctl[3];
+            prefix |= static_cast<uint64_t>(d) << shift;
+            need -= above;
+            if (inbin == need) break;  // the whole bin is in: keys >= prefix are exactly k
+        }
+        // keep keys >= prefix (exactly k of them), compacted to the front
+        constexpr int PER = CAP / NT;
+        uint64_t v[PER];
+#pragma unroll
+        for (int j = 0; j < PER; ++j) {
+            const int i = tid + j * NT;
+            v[j] = i < n ? buf[i] : 0ull;
+        }
+        if (tid == 0) ctl[4] = 0;
+        sync();
+        const int lane = threadIdx.x & 31;
+#pragma unroll
+        for (int j = 0; j < PER; ++j) {
+            const bool keep = v[j] != 0ull && v[j] >= prefix;
+            const unsigned m = __ballot_sync(kFull, keep);
+            if (m) {
+                const int leader = __ffs(m) - 1;
+                int base = 0;
+                if (lane == leader) base = atomicAdd(&ctl[4], __popc(m));
+                base = __shfl_sync(kFull, base, leader);
+                const int pos = base + __popc(m & ((1u << lane) - 1u));
+                if (keep && pos < CAP) buf[pos] = v[j];
+            }
+        }
+        sync();
+        if (tid == 0) {
+            if (ctl[4] != k) atomicOr(err, kErrAssert);
+            ctl[0] = ctl[4] < CAP ? ctl[4] : CAP;
+            *thr = prefix;
+        }
+        sync();
+    }
+
+    // Collective: sort buf[0..P) descending (P a power of two).
+    __device__ void sort_desc(int P) {
+        for (int size = 2; size <= P; size <<= 1) {
+            for (int stride = size >> 1; stride > 0; stride >>= 1) {
+                for (int i = tid; i < (P >> 1); i += NT) {
+                    const int lo = 2 * i - (i & (stride - 1));
+                    const int hi = lo + stride;
+                    const uint64_t a = buf[lo];
+                    const uint64_t b = buf[hi];
+                    const bool desc = (lo & size) == 0;
+                    if ((a < b) == desc) {
+                        buf[lo] = b;
+                        buf[hi] = a;
+                    }
+                }
+                sync();
+            }
+        }
+    }
+
+    // Collective: write the top k in rank order; positions past the held count get
+    // -1 (and -inf scores).
+    __device__ void finalize(int k, int32_t* idx_out, float* score_out) {
+        compact(k, settled_count());
+        const int n = settled_count();
+        int P = 1;
+        while (P < n) P <<= 1;
+        for (int i = n + tid; i < P; i += NT) buf[i] = 0ull;
+        sync();
+        sort_desc(P);
+        for (int i = tid; i < k; i += NT) {
+            if (i < n) {
+                const uint64_t key = buf[i];
+                idx_out[i] = key_position(key);
+                if (score_out) score_out[i] = key_score(key);
+            } else {
+                idx_out[i] = -1;
+                if (score_out) score_out[i] = -__int_as_float(0x7f800000);
+            }
+        }
+        sync();
+    }
+
+    // Collective: reduce to at most k keys and copy them (unordered) to global memory.
+    __device__ void dump(int k, uint64_t* out, int* out_count) {
+        compact(k, settled_count());
+        const int n = settled_count();
+        for (int i = tid; i < n; i += NT) out[i] = buf[i];
+        if (tid == 0) *out_count = n;
+        sync();
+    }
+};
+
+}  // namespace tsi

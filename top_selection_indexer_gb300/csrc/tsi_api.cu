@@ -1,0 +1,213 @@
+// C ABI of libtsi.so: argument checks, path selection, error reporting.
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+
+#include "attn_generic.cuh"
+#include "indexer_generic.cuh"
+#include "kernels_tc.cuh"
+#include "tsi_common.cuh"
+
+namespace tsi {
+static std::atomic<uint64_t> g_launches{0};
+void note_launches(int n) { g_launches.fetch_add(static_cast<uint64_t>(n)); }
+}  // namespace tsi
+
+namespace {
+
+thread_local char g_msg[512] = "";
+
+tsi_status fail(tsi_status st, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_msg, sizeof g_msg, fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+tsi_status ok() {
+    g_msg[0] = '\0';
+    return TSI_OK;
+}
+
+// Device error word, one per device (context); kernels atomicOr flags into it.
+__device__ unsigned g_dev_err;
+
+constexpr int kMaxDevices = 64;
+unsigned* g_err_ptr[kMaxDevices] = {};
+std::mutex g_err_mu;
+
+tsi_status device_error_word(unsigned** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(TSI_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= kMaxDevices) return fail(TSI_ERR_CUDA, "device id %d out of range", dev);
+    std::lock_guard<std::mutex> lk(g_err_mu);
+    if (!g_err_ptr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_dev_err);
+        if (e != cudaSuccess)
+            return fail(TSI_ERR_CUDA, "cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+        g_err_ptr[dev] = static_cast<unsigned*>(p);
+    }
+    *out = g_err_ptr[dev];
+    return TSI_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool qk_dtype_ok(int dt) { return dt == TSI_F32 || dt == TSI_BF16 || dt == TSI_E4M3; }
+bool w_dtype_ok(int dt) { return dt == TSI_F32 || dt == TSI_BF16; }
+
+bool use_tc_indexer(int qk_dtype, int H_I, int d_I) {
+    return tsi::tc_indexer_supported(qk_dtype, H_I, d_I);
+}
+
+bool use_tc_attn(int H, int Hkv, int Dqk, int Dv, bool v_from_k) {
+    return tsi::tc_attn_supported(H, Hkv, Dqk, Dv, v_from_k);
+}
+
+}  // namespace
+
+extern "C" {
+
+int tsi_version(void) { return 100; }
+
+uint64_t tsi_launch_count(void) { return tsi::g_launches.load(); }
+
+const char* tsi_last_error(void) { return g_msg; }
+
+size_t tsi_indexer_topk_workspace(int B, int T, int S, int H_I, int d_I, int topk,
+                                  int qk_dtype) {
+    if (B <= 0 || T <= 0 || S < 0 || topk < 1) return 0;
+    if (use_tc_indexer(qk_dtype, H_I, d_I)) return tsi::tc_indexer_workspace_bytes(B, T, S, topk);
+    return tsi::generic_workspace_bytes(B, T, S, topk);
+}
+
+tsi_status tsi_indexer_topk(const void* qI, const void* kI, const void* w, int qk_dtype,
+                            int w_dtype, int B, int T, int S, int H_I, int d_I, int topk,
+                            const int32_t* kv_len, int32_t* idx, float* score, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+    if (!qk_dtype_ok(qk_dtype)) return fail(TSI_ERR_INVALID_ARG, "qk_dtype %d unknown", qk_dtype);
+    if (!w_dtype_ok(w_dtype)) return fail(TSI_ERR_INVALID_ARG, "w_dtype %d unknown", w_dtype);
+    if (B < 0 || T < 0 || S < 0)
+        return fail(TSI_ERR_INVALID_ARG, "negative size (B=%d T=%d S=%d)", B, T, S);
+    if (topk < 1 || topk > TSI_MAX_TOPK)
+        return fail(TSI_ERR_UNSUPPORTED, "topk=%d outside [1, %d]", topk, TSI_MAX_TOPK);
+    if (H_I < 1 || d_I < 1) return fail(TSI_ERR_INVALID_ARG, "H_I=%d d_I=%d", H_I, d_I);
+    const bool tc = use_tc_indexer(qk_dtype, H_I, d_I);
+    if (!tc && !tsi::generic_supported(H_I, d_I))
+        return fail(TSI_ERR_UNSUPPORTED, "H_I=%d d_I=%d unsupported (d_I<=256, H_I<=128, "
+                    "H_I*d_I<=8192)", H_I, d_I);
+    if (static_cast<int64_t>(B) * T > (1ll << 31) - 1 || static_cast<int64_t>(B) * S > (1ll << 31) - 1)
+        return fail(TSI_ERR_UNSUPPORTED, "B*T or B*S exceeds 2^31-1");
+    if (B == 0 || T == 0) return ok();
+    if (!qI || !w || !idx || (S > 0 && !kI))
+        return fail(TSI_ERR_INVALID_ARG, "NULL tensor pointer");
+    if (!aligned16(qI) || !aligned16(kI) || !aligned16(w) || !aligned16(idx) ||
+        !aligned16(score) || !aligned16(kv_len))
+        return fail(TSI_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+    const size_t need = tsi_indexer_topk_workspace(B, T, S, H_I, d_I, topk, qk_dtype);
+    if (workspace_bytes < need || (need > 0 && !workspace))
+        return fail(TSI_ERR_WORKSPACE, "workspace %zu bytes, need %zu", workspace_bytes, need);
+    if (need > 0 && !aligned16(workspace))
+        return fail(TSI_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+    unsigned* err = nullptr;
+    tsi_status st = device_error_word(&err);
+    if (st != TSI_OK) return st;
+    tsi::IndexerArgs a{qI, kI, w, qk_dtype, w_dtype, B, T, S, H_I, d_I, topk, kv_len,
+                       idx, score, err};
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = tc ? tsi::launch_indexer_tc(a, workspace, s)
+                       : tsi::launch_indexer_generic(a, workspace, s);
+    if (e != cudaSuccess) return fail(TSI_ERR_CUDA, "indexer launch: %s", cudaGetErrorString(e));
+    return ok();
+}
+
+size_t tsi_sparse_attn_workspace(int B, int T, int S, int H, int Hkv, int Dqk, int Dv,
+                                 int topk) {
+    if (B <= 0 || T <= 0 || topk < 1 || H < 1) return 0;
+    // the value layout does not change the workspace: ask for the larger of the two paths
+    size_t a = tsi::attn_generic_workspace_bytes(B, T, H, Dv, topk);
+    size_t b = use_tc_attn(H, Hkv, Dqk, Dv, true) ? tsi::tc_attn_workspace_bytes(B, T, H, Dv, topk)
+                                                  : 0;
+    return a > b ? a : b;
+}
+
+tsi_status tsi_sparse_attn_group(int n_layers, const void* const* q, const void* const* k,
+                                 const void* const* v, int B, int T, int S, int H, int Hkv,
+                                 int Dqk, int Dv, float scale, const int32_t* idx, int topk,
+                                 const int32_t* kv_len, void* const* out, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+    if (n_layers < 0) return fail(TSI_ERR_INVALID_ARG, "n_layers=%d", n_layers);
+    if (B < 0 || T < 0 || S < 0)
+        return fail(TSI_ERR_INVALID_ARG, "negative size (B=%d T=%d S=%d)", B, T, S);
+    if (topk < 1 || topk > TSI_MAX_TOPK)
+        return fail(TSI_ERR_UNSUPPORTED, "topk=%d outside [1, %d]", topk, TSI_MAX_TOPK);
+    if (H < 1 || Hkv < 1 || H % Hkv != 0)
+        return fail(TSI_ERR_INVALID_ARG, "H=%d must be a positive multiple of Hkv=%d", H, Hkv);
+    if (Dqk < 1 || Dv < 1) return fail(TSI_ERR_INVALID_ARG, "Dqk=%d Dv=%d", Dqk, Dv);
+    if (!std::isfinite(scale)) return fail(TSI_ERR_INVALID_ARG, "scale is not finite");
+    if (static_cast<int64_t>(B) * T > (1ll << 31) - 1 || static_cast<int64_t>(B) * S > (1ll << 31) - 1)
+        return fail(TSI_ERR_UNSUPPORTED, "B*T or B*S exceeds 2^31-1");
+    if (n_layers == 0 || B == 0 || T == 0) return ok();
+    if (!q || !k || !out || !idx) return fail(TSI_ERR_INVALID_ARG, "NULL pointer list");
+    if (!aligned16(idx) || !aligned16(kv_len))
+        return fail(TSI_ERR_INVALID_ARG, "idx / kv_len must be 16-byte aligned");
+    for (int l = 0; l < n_layers; ++l) {
+        const void* vl = v ? v[l] : nullptr;
+        const bool vk = vl == nullptr;
+        if (!q[l] || !out[l] || (S > 0 && !k[l]))
+            return fail(TSI_ERR_INVALID_ARG, "layer %d: NULL tensor pointer", l);
+        if (!aligned16(q[l]) || !aligned16(k[l]) || !aligned16(vl) || !aligned16(out[l]))
+            return fail(TSI_ERR_INVALID_ARG, "layer %d: pointers must be 16-byte aligned", l);
+        if (!use_tc_attn(H, Hkv, Dqk, Dv, vk) && !tsi::attn_generic_supported(H, Hkv, Dqk, Dv, vk))
+            return fail(TSI_ERR_UNSUPPORTED, "H=%d Hkv=%d Dqk=%d Dv=%d%s unsupported (Dqk<=576, "
+                        "Dv<=512)", H, Hkv, Dqk, Dv, vk ? " (value from key)" : "");
+    }
+    const size_t need = tsi_sparse_attn_workspace(B, T, S, H, Hkv, Dqk, Dv, topk);
+    if (workspace_bytes < need || (need > 0 && !workspace))
+        return fail(TSI_ERR_WORKSPACE, "workspace %zu bytes, need %zu", workspace_bytes, need);
+    if (need > 0 && !aligned16(workspace))
+        return fail(TSI_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+    unsigned* err = nullptr;
+    tsi_status st = device_error_word(&err);
+    if (st != TSI_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    for (int l = 0; l < n_layers; ++l) {
+        const void* vl = v ? v[l] : nullptr;
+        tsi::AttnArgs a{q[l], k[l], vl, B, T, S, H, Hkv, Dqk, Dv, scale, idx, topk, kv_len,
+                        out[l], err};
+        cudaError_t e = use_tc_attn(H, Hkv, Dqk, Dv, vl == nullptr)
+                            ? tsi::launch_attn_tc(a, workspace, s)
+                            : tsi::launch_attn_generic(a, workspace, s);
+        if (e != cudaSuccess)
+            return fail(TSI_ERR_CUDA, "attention launch (layer %d): %s", l, cudaGetErrorString(e));
+    }
+    return ok();
+}
+
+tsi_status tsi_device_status(void* stream) {
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(TSI_ERR_CUDA, "stream: %s", cudaGetErrorString(e));
+    unsigned* err = nullptr;
+    tsi_status st = device_error_word(&err);
+    if (st != TSI_OK) return st;
+    unsigned word = 0;
+    e = cudaMemcpy(&word, err, sizeof word, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return fail(TSI_ERR_CUDA, "read error word: %s", cudaGetErrorString(e));
+    if (word) {
+        const unsigned zero = 0;
+        e = cudaMemcpy(err, &zero, sizeof zero, cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return fail(TSI_ERR_CUDA, "clear error word: %s", cudaGetErrorString(e));
+    }
+    if (word & tsi::kErrTimeout)
+        return fail(TSI_ERR_TIMEOUT, "a bounded device-side wait ran out (word 0x%x)", word);
+    if (word & tsi::kErrAssert)
+        return fail(TSI_ERR_DEVICE_ASSERT, "a device-side check failed (word 0x%x)", word);
+    return ok();
+}
+
+}  // extern "C"
