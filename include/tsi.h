@@ -86,6 +86,42 @@ tsi_status tsi_indexer_topk(const void* qI, const void* kI, const void* w, int q
                             const int32_t* kv_len, int32_t* idx, float* score, void* workspace,
                             size_t workspace_bytes, void* stream);
 
+/*
+ * tsi_indexer_topk without a workspace argument and without allocating anything.
+ * The paper has no counterpart: this is a convenience of this library.
+ *
+ * Meant for callers that cannot allocate device memory while they run, such as a
+ * serving loop whose device memory is fixed at start-up, or code called from inside a
+ * custom device allocator, where a nested cudaMalloc would recurse into the allocator
+ * or synchronize the device.  The scratch that tsi_indexer_topk takes from the caller's
+ * workspace (per-split candidate lists when few rows scan long caches, as in decode)
+ * lives here in one fixed array compiled into the library: 8 MiB of device memory,
+ * held by every GPU that loads the library until the process exits
+ * (tsi_indexer_topk_noalloc_limit() returns the size).
+ *
+ * Arguments, layouts and results are those of tsi_indexer_topk; the scores always come
+ * from the CUDA-core path (identical indices on integer-valued inputs, the same
+ * near-tie behaviour otherwise).  A request whose scratch would exceed the array
+ * (tsi_indexer_topk_workspace for the same sizes, with CUDA-core shapes) returns
+ * TSI_ERR_UNSUPPORTED and launches nothing.  The call performs no cudaMalloc, cudaFree
+ * or other allocating call.
+ *
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) while that device is current; make that first call before any
+ * stream capture.  All calls on a device share the one array, which keeps whatever the
+ * last call left in it (each call writes every scratch slot before reading it, so
+ * nothing needs clearing).  Calls whose kernels overlap on the GPU -- different streams,
+ * or different host threads -- race on the array and give undefined results: serialize
+ * them on one stream.
+ */
+tsi_status tsi_indexer_topk_noalloc(const void* qI, const void* kI, const void* w, int qk_dtype,
+                                    int w_dtype, int B, int T, int S, int H_I, int d_I,
+                                    int topk, const int32_t* kv_len, int32_t* idx, float* score,
+                                    void* stream);
+
+/* Bytes of the built-in scratch array used by tsi_indexer_topk_noalloc. */
+size_t tsi_indexer_topk_noalloc_limit(void);
+
 /* Workspace bytes needed by tsi_sparse_attn_group for these sizes (0 when none). */
 size_t tsi_sparse_attn_workspace(int B, int T, int S, int H, int Hkv, int Dqk, int Dv,
                                  int topk);

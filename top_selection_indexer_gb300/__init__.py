@@ -23,7 +23,7 @@ MAX_TOPK = 2048
 
 EXPORTS = ("tsi_indexer_topk_workspace", "tsi_indexer_topk", "tsi_sparse_attn_workspace",
            "tsi_sparse_attn_group", "tsi_device_status", "tsi_last_error", "tsi_version",
-           "tsi_launch_count")
+           "tsi_launch_count", "tsi_indexer_topk_noalloc", "tsi_indexer_topk_noalloc_limit")
 
 
 class TSIError(RuntimeError):
@@ -60,6 +60,11 @@ def load():
             lib.tsi_version.restype = i32
             lib.tsi_launch_count.argtypes = []
             lib.tsi_launch_count.restype = ctypes.c_uint64
+            lib.tsi_indexer_topk_noalloc.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32,
+                                                     i32, i32, vp, vp, vp, vp]
+            lib.tsi_indexer_topk_noalloc.restype = i32
+            lib.tsi_indexer_topk_noalloc_limit.argtypes = []
+            lib.tsi_indexer_topk_noalloc_limit.restype = sz
             _lib = lib
     return _lib
 

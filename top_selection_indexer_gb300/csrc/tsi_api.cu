@@ -211,3 +211,98 @@ tsi_status tsi_device_status(void* stream) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------------------
+// Allocation-free indexer + top-k.
+//
+// For callers that cannot allocate device memory while they run: a serving loop whose
+// device memory budget is fixed at start-up, or code called from inside a custom device
+// allocator, where a nested cudaMalloc would recurse into the allocator or synchronize the
+// device.  tsi_indexer_topk needs a caller-provided workspace when rows are few and key
+// ranges are split across thread blocks (decode); this variant keeps that scratch in one
+// fixed array compiled into the library instead.
+//
+// The array below is in device memory of every GPU that loads the library and stays
+// there until the process exits.  Its host-side name is only a stand-in for the device
+// symbol, so the device address is looked up with cudaGetSymbolAddress, once per device,
+// on the first call made while that device is current.
+// ---------------------------------------------------------------------------------------
+
+static constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;  // 8 MiB per device
+static __device__ __align__(256) unsigned char tsi_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+
+void* g_noalloc_ptr[kMaxDevices] = {};
+std::mutex g_noalloc_mu;
+
+// Device address of tsi_noalloc_scratch on the current device (looked up once).
+tsi_status noalloc_scratch_address(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(TSI_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= kMaxDevices) return fail(TSI_ERR_CUDA, "device id %d out of range", dev);
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, tsi_noalloc_scratch);
+        if (e != cudaSuccess)
+            return fail(TSI_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return TSI_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t tsi_indexer_topk_noalloc_limit(void) { return kNoAllocScratchBytes; }
+
+tsi_status tsi_indexer_topk_noalloc(const void* qI, const void* kI, const void* w, int qk_dtype,
+                                    int w_dtype, int B, int T, int S, int H_I, int d_I,
+                                    int topk, const int32_t* kv_len, int32_t* idx, float* score,
+                                    void* stream) {
+    if (!qk_dtype_ok(qk_dtype)) return fail(TSI_ERR_INVALID_ARG, "qk_dtype %d unknown", qk_dtype);
+    if (!w_dtype_ok(w_dtype)) return fail(TSI_ERR_INVALID_ARG, "w_dtype %d unknown", w_dtype);
+    if (B < 0 || T < 0 || S < 0)
+        return fail(TSI_ERR_INVALID_ARG, "negative size (B=%d T=%d S=%d)", B, T, S);
+    if (topk < 1 || topk > TSI_MAX_TOPK)
+        return fail(TSI_ERR_UNSUPPORTED, "topk=%d outside [1, %d]", topk, TSI_MAX_TOPK);
+    if (H_I < 1 || d_I < 1) return fail(TSI_ERR_INVALID_ARG, "H_I=%d d_I=%d", H_I, d_I);
+    if (!tsi::generic_supported(H_I, d_I))
+        return fail(TSI_ERR_UNSUPPORTED, "H_I=%d d_I=%d unsupported (d_I<=256, H_I<=128, "
+                    "H_I*d_I<=8192)", H_I, d_I);
+    if (static_cast<int64_t>(B) * T > (1ll << 31) - 1 || static_cast<int64_t>(B) * S > (1ll << 31) - 1)
+        return fail(TSI_ERR_UNSUPPORTED, "B*T or B*S exceeds 2^31-1");
+    const size_t need = tsi::generic_workspace_bytes(B, T, S, topk);
+    if (need > kNoAllocScratchBytes)
+        return fail(TSI_ERR_UNSUPPORTED,
+                    "request needs %zu bytes of scratch, more than the %zu-byte built-in array; "
+                    "use tsi_indexer_topk with a workspace", need, kNoAllocScratchBytes);
+    if (B == 0 || T == 0) return ok();
+    if (!qI || !w || !idx || (S > 0 && !kI))
+        return fail(TSI_ERR_INVALID_ARG, "NULL tensor pointer");
+    if (!aligned16(qI) || !aligned16(kI) || !aligned16(w) || !aligned16(idx) ||
+        !aligned16(score) || !aligned16(kv_len))
+        return fail(TSI_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+    void* scratch = nullptr;
+    tsi_status st = TSI_OK;
+    if (need > 0) {
+        st = noalloc_scratch_address(&scratch);
+        if (st != TSI_OK) return st;
+    }
+    unsigned* err = nullptr;
+    st = device_error_word(&err);
+    if (st != TSI_OK) return st;
+    // Every split writes its candidate count and list before the merge reads them, so
+    // nothing in the scratch array has to start at zero.
+    tsi::IndexerArgs a{qI, kI, w, qk_dtype, w_dtype, B, T, S, H_I, d_I, topk, kv_len,
+                       idx, score, err};
+    cudaError_t e = tsi::launch_indexer_generic(a, scratch, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(TSI_ERR_CUDA, "indexer launch: %s", cudaGetErrorString(e));
+    return ok();
+}
+
+}  // extern "C"
