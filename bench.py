@@ -222,9 +222,11 @@ def run_gpu(args, rank, world):
                                        cfg.topk, cfg.v_from_k)
     attn_achieved = attn_bytes / (ms_attn / 1e3) / 1e9
     attn_tc = accounting.attn_flops(valid_k, cfg.H, cfg.Dqk, cfg.Dv) / (ms_attn / 1e3) / 1e12
-    attn_kernel = "tsi_attn_tc_kernel" if cfg.Dqk == 576 and cfg.Hkv == 1 else "attn_generic_kernel"
-    idx_kernel = "tsi_indexer_tc_kernel" if cfg.d_I == 128 and cfg.H_I == 64 else \
-        "indexer_generic_kernel"
+    qk_code = tsi.E4M3 if cfg.qk_dtype == "e4m3" else tsi.BF16 if cfg.qk_dtype == "bf16" else tsi.F32
+    attn_kernel = "tsi_attn_tc_kernel" if tsi.attn_path(cfg.H, cfg.Hkv, cfg.Dqk, cfg.Dv,
+                                                        cfg.v_from_k) == 1 else "attn_generic_kernel"
+    idx_kernel = "tsi_indexer_tc_kernel" if tsi.indexer_path(qk_code, cfg.H_I, cfg.d_I) == 1 \
+        else "indexer_generic_kernel"
     roof_attn = {"kernel": attn_kernel, "bound": "hbm", "achieved": round(attn_achieved, 1),
                  "peak": peaks["hbm_gbs"], "unit": "GB/s",
                  "frac": round(attn_achieved / peaks["hbm_gbs"], 4),

@@ -163,6 +163,11 @@ tsi_status tsi_device_status(void* stream);
 /* Message for the last non-OK status returned on this host thread ("" if none). */
 const char* tsi_last_error(void);
 
+/* Which kernels serve a shape: 1 = tensor-core (tcgen05) path, 0 = CUDA-core path,
+ * -1 = unsupported.  v_from_k != 0 means the value is the first Dv dims of the key. */
+int tsi_indexer_topk_path(int qk_dtype, int H_I, int d_I);
+int tsi_sparse_attn_path(int H, int Hkv, int Dqk, int Dv, int v_from_k);
+
 /* Number of kernels this library has launched in this process (all threads). */
 uint64_t tsi_launch_count(void);
 

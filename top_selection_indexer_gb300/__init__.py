@@ -23,7 +23,8 @@ MAX_TOPK = 2048
 
 EXPORTS = ("tsi_indexer_topk_workspace", "tsi_indexer_topk", "tsi_sparse_attn_workspace",
            "tsi_sparse_attn_group", "tsi_device_status", "tsi_last_error", "tsi_version",
-           "tsi_launch_count", "tsi_indexer_topk_noalloc", "tsi_indexer_topk_noalloc_limit")
+           "tsi_launch_count", "tsi_indexer_topk_noalloc", "tsi_indexer_topk_noalloc_limit",
+           "tsi_indexer_topk_path", "tsi_sparse_attn_path")
 
 
 class TSIError(RuntimeError):
@@ -63,6 +64,10 @@ def load():
             lib.tsi_indexer_topk_noalloc.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32,
                                                      i32, i32, vp, vp, vp, vp]
             lib.tsi_indexer_topk_noalloc.restype = i32
+            lib.tsi_indexer_topk_path.argtypes = [i32, i32, i32]
+            lib.tsi_indexer_topk_path.restype = i32
+            lib.tsi_sparse_attn_path.argtypes = [i32] * 5
+            lib.tsi_sparse_attn_path.restype = i32
             lib.tsi_indexer_topk_noalloc_limit.argtypes = []
             lib.tsi_indexer_topk_noalloc_limit.restype = sz
             _lib = lib
@@ -72,6 +77,16 @@ def load():
 def launch_count() -> int:
     """Kernels the library has launched in this process so far."""
     return int(load().tsi_launch_count())
+
+
+def indexer_path(qk_dtype, H_I, d_I) -> int:
+    """1: tensor-core kernel, 0: CUDA-core kernel, -1: unsupported."""
+    return load().tsi_indexer_topk_path(qk_dtype, H_I, d_I)
+
+
+def attn_path(H, Hkv, Dqk, Dv, v_from_k) -> int:
+    """1: tensor-core kernel, 0: CUDA-core kernel, -1: unsupported."""
+    return load().tsi_sparse_attn_path(H, Hkv, Dqk, Dv, int(bool(v_from_k)))
 
 
 def last_error() -> str:

@@ -165,3 +165,19 @@ cudaError_t launch_indexer_generic(const IndexerArgs& a, void* workspace, cudaSt
 }
 
 }  // namespace tsi
+
+namespace tsi {
+
+cudaError_t launch_topk_merge(int rows, int topk, int n_splits, const uint64_t* cand,
+                              const int* cand_cnt, int32_t* idx, float* score, unsigned* err,
+                              cudaStream_t st) {
+    const int msmem = selector_smem_bytes<kCAP>();
+    cudaError_t e = cudaFuncSetAttribute(topk_merge_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, msmem);
+    if (e != cudaSuccess) return e;
+    topk_merge_kernel<<<rows, kNT, msmem, st>>>(topk, n_splits, cand, cand_cnt, idx, score, err);
+    note_launches(1);
+    return cudaGetLastError();
+}
+
+}  // namespace tsi

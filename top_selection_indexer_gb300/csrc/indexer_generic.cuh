@@ -24,4 +24,10 @@ void generic_split_plan(int rows, int S, int* n_splits, int* chunk);
 size_t generic_workspace_bytes(int B, int T, int S, int topk);
 cudaError_t launch_indexer_generic(const IndexerArgs& a, void* workspace, cudaStream_t st);
 
+// Merge per-split candidate lists ([rows][n_splits][topk] keys + counts) into the
+// final rank-ordered rows (CUDA-core selector).
+cudaError_t launch_topk_merge(int rows, int topk, int n_splits, const uint64_t* cand,
+                              const int* cand_cnt, int32_t* idx, float* score, unsigned* err,
+                              cudaStream_t st);
+
 }  // namespace tsi

@@ -1,12 +1,419 @@
-// Tensor-core lightning indexer + streaming top-k (tcgen05 / TMEM / TMA).
+// Tensor-core lightning indexer + streaming top-k for sm_103a (tcgen05 / TMEM / TMA).
+//
+// I[t,s] = sum_j w[t,j] * ReLU(qI[t,j] . kI[s]) for s <= p_t, then the top-k keys of
+// each row ("GLM-5.2 技术报告速览", §IndexShare: the score equation, k = 2048; the
+// ReLU form is chosen there for speed and FP8 friendliness).  The L x L score matrix
+// never leaves the chip: each 128-key tile is scored in TMEM and streamed into a
+// shared-memory top-k selector.
+//
+// MMA shape: keys on M (128 rows of kI per tile, the A operand), the 64 heads of two
+// query rows on N (the B operand, 128 rows of qI), d_I = 128 on K, fp32 accumulators
+// in TMEM.  A thread of the epilogue owns one key (one TMEM lane) and reduces the 64
+// heads of its query row inside its registers: ReLU, times the gate weight, summed --
+// no cross-thread reduction.
+//
+// Roles of one persistent CTA (320 threads):
+//   warp 0      TMA producer: Q tile of the unit, key tiles into a ring of stages
+//   warp 1      TMEM allocator + single-thread MMA issuer (two TMEM accumulators)
+//   warps 2..9  two epilogue groups of 4 warps (one per query row of the unit); group
+//               g reads columns [64g, 64g+64) of the accumulator and owns a selector
+// Units (two consecutive query rows x one key range) are visited longest first and
+// spread round-robin over the CTAs.  Decode-sized requests split each row's keys into
+// chunks; chunk candidate lists are merged by the CUDA-core merge kernel.
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
 #include "kernels_tc.cuh"
+#include "tc_common.cuh"
+#include "topk_select.cuh"
 
 namespace tsi {
+namespace {
 
-bool tc_indexer_supported(int, int, int) { return false; }
-size_t tc_indexer_workspace_bytes(int, int, int, int) { return 0; }
-cudaError_t launch_indexer_tc(const IndexerArgs&, void*, cudaStream_t) {
-    return cudaErrorNotSupported;
+constexpr int kRowsPerUnit = 2;
+constexpr int kTileKeys = 128;  // MMA M
+constexpr int kN = 64 * kRowsPerUnit;  // MMA N
+constexpr int kEpiWarps = 4 * kRowsPerUnit;
+constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr int kGroupThreads = 128;
+constexpr int kCap = 4096;
+constexpr int kTmemCols = 2 * kN;  // two accumulators
+constexpr int kChunkBytes = 128 * 128;  // one 128-row x 128-byte swizzled tile
+
+template <int QK>
+struct TileCfg;
+template <>
+struct TileCfg<TSI_E4M3> {
+    static constexpr int kChunks = 1;  // 128-byte pieces of a d_I = 128 row
+    static constexpr int kStages = 6;
+    static constexpr uint32_t kIdesc = tc::instr_desc(0, kTileKeys, kN);
+    static constexpr int kKSteps = 4;  // K = 32 per MMA
+    static constexpr int kKStepBytes = 32;
+};
+template <>
+struct TileCfg<TSI_BF16> {
+    static constexpr int kChunks = 2;
+    static constexpr int kStages = 3;
+    static constexpr uint32_t kIdesc = tc::instr_desc(1, kTileKeys, kN);
+    static constexpr int kKSteps = 4;  // per chunk, K = 16 per MMA
+    static constexpr int kKStepBytes = 32;
+};
+
+struct TcParams {
+    const void* w;
+    int w_dtype;
+    int B, T, S, topk;
+    const int32_t* kv_len;
+    int32_t* idx;
+    float* score;
+    uint64_t* cand;
+    int* cand_cnt;
+    int n_chunks, chunk_keys, n_units;
+    unsigned* err;
+};
+
+struct Unit {
+    int b, t_lo, t_hi, chunk;
+    int64_t key_lo, key_hi;
+    int ntiles;
+};
+
+// Unit u: pair j = u / (B * n_chunks) counted from the end of the sequence (longest rows
+// first), sequence b, key chunk.  Rows t_lo = t_hi - 1 (may be -1) and t_hi.
+__device__ __forceinline__ Unit unit_of(const TcParams& p, int u) {
+    Unit U;
+    U.chunk = u % p.n_chunks;
+    const int pu = u / p.n_chunks;
+    const int j = pu / p.B;
+    U.b = pu % p.B;
+    U.t_hi = p.T - 1 - 2 * j;
+    U.t_lo = U.t_hi - 1;
+    const int64_t p_hi = query_position(p.kv_len, U.b, p.T, p.S, U.t_hi);
+    const int64_t end = p_hi + 1 > 0 ? p_hi + 1 : 0;
+    U.key_lo = static_cast<int64_t>(U.chunk) * p.chunk_keys;
+    U.key_hi = U.key_lo + p.chunk_keys < end ? U.key_lo + p.chunk_keys : end;
+    if (U.key_hi < U.key_lo) U.key_hi = U.key_lo;
+    U.ntiles = static_cast<int>((U.key_hi - U.key_lo + kTileKeys - 1) / kTileKeys);
+    return U;
+}
+
+template <int QK>
+constexpr int smem_bytes() {
+    using C = TileCfg<QK>;
+    return 1024 /* alignment slack */ + C::kStages * C::kChunks * kChunkBytes +
+           C::kChunks * kChunkBytes + 2 * ((selector_smem_bytes<kCap>() + 15) & ~15) +
+           2 * 64 * 4 + 256;
+}
+
+template <int QK>
+__global__ void __launch_bounds__(kThreads, 1)
+    tsi_indexer_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                          const __grid_constant__ CUtensorMap tmap_q, const TcParams p) {
+    using C = TileCfg<QK>;
+    constexpr int kStageBytes = C::kChunks * kChunkBytes;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* base = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t* stages = base;
+    uint8_t* qbuf = stages + C::kStages * kStageBytes;
+    uint8_t* sel_mem = qbuf + kStageBytes;
+    constexpr int kSelBytes = (selector_smem_bytes<kCap>() + 15) & ~15;
+    float* w_s = reinterpret_cast<float*>(sel_mem + 2 * kSelBytes);  // [2][64]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(w_s + 2 * 64);
+    uint64_t* full = bars;
+    uint64_t* empty = full + C::kStages;
+    uint64_t* tfull = empty + C::kStages;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* qfull = tempty + 2;
+    uint64_t* qempty = qfull + 1;
+    uint64_t* done = qempty + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+    volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            tc::mbar_init(&full[s], 1);
+            tc::mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            tc::mbar_init(&tfull[a], 1);
+            tc::mbar_init(&tempty[a], kEpiWarps);
+        }
+        tc::mbar_init(qfull, 1);
+        tc::mbar_init(qempty, 1);
+        tc::mbar_init(done, 1);
+        *abort = 0;
+        tc::fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tc::prefetch_tmap(&tmap_k);
+        tc::prefetch_tmap(&tmap_q);
+    }
+    if (warp == 1) tc::tmem_alloc(tmem_slot, kTmemCols);
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int it = 0, unit_it = 0;
+            for (int u = blockIdx.x; u < p.n_units; u += gridDim.x, ++unit_it) {
+                const Unit U = unit_of(p, u);
+                tc::mbar_wait(qempty, (unit_it & 1) ^ 1, abort, p.err);
+                if (!*abort) {
+                    tc::mbar_expect_tx(qfull, kStageBytes);
+                    const int qrow = (U.b * p.T + U.t_lo) * 64;
+                    for (int c = 0; c < C::kChunks; ++c)
+                        tc::tma_load_2d(qbuf + c * kChunkBytes, &tmap_q, c * 64, qrow, qfull);
+                }
+                for (int i = 0; i < U.ntiles; ++i, ++it) {
+                    const int s = it % C::kStages;
+                    tc::mbar_wait(&empty[s], ((it / C::kStages) & 1) ^ 1, abort, p.err);
+                    if (*abort) continue;
+                    tc::mbar_expect_tx(&full[s], kStageBytes);
+                    const int krow = static_cast<int>(static_cast<int64_t>(U.b) * p.S + U.key_lo +
+                                                      static_cast<int64_t>(i) * kTileKeys);
+                    for (int c = 0; c < C::kChunks; ++c)
+                        tc::tma_load_2d(stages + s * kStageBytes + c * kChunkBytes, &tmap_k,
+                                        c * 64, krow, &full[s]);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int it = 0, acc_it = 0, unit_it = 0;
+            const uint32_t q_addr = tc::smem_addr(qbuf);
+            const uint32_t st_addr = tc::smem_addr(stages);
+            for (int u = blockIdx.x; u < p.n_units; u += gridDim.x, ++unit_it) {
+                const Unit U = unit_of(p, u);
+                tc::mbar_wait(qfull, unit_it & 1, abort, p.err);
+                for (int i = 0; i < U.ntiles; ++i, ++it, ++acc_it) {
+                    const int s = it % C::kStages;
+                    const int a = acc_it & 1;
+                    tc::mbar_wait(&full[s], (it / C::kStages) & 1, abort, p.err);
+                    tc::mbar_wait(&tempty[a], ((acc_it >> 1) & 1) ^ 1, abort, p.err);
+                    tc::tc_fence_after();
+                    if (!*abort) {
+                        const uint32_t d = tmem + a * kN;
+                        const uint32_t a0 = st_addr + s * kStageBytes;
+#pragma unroll
+                        for (int c = 0; c < C::kChunks; ++c) {
+#pragma unroll
+                            for (int k = 0; k < C::kKSteps; ++k) {
+                                const uint32_t off = c * kChunkBytes + k * C::kKStepBytes;
+                                const uint64_t da = tc::smem_desc(a0 + off, 16, 1024);
+                                const uint64_t db = tc::smem_desc(q_addr + off, 16, 1024);
+                                const uint32_t acc = (c | k) ? 1u : 0u;
+                                if (QK == TSI_E4M3)
+                                    tc::mma_f8(d, da, db, C::kIdesc, acc);
+                                else
+                                    tc::mma_bf16(d, da, db, C::kIdesc, acc);
+                            }
+                        }
+                    }
+                    tc::mma_commit(&empty[s]);
+                    tc::mma_commit(&tfull[a]);
+                }
+                tc::mma_commit(qempty);
+            }
+            // every MMA issued by this thread has finished before TMEM is released
+            tc::mma_commit(done);
+            tc::mbar_wait(done, 0, abort, p.err);
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue groups
+        const int ew = warp - 2;
+        const int g = ew >> 2;  // query row of the unit handled by this group
+        const int quad = warp & 3;  // TMEM lanes [32*quad, 32*quad+32) this warp may read
+        const int gtid = (ew & 3) * 32 + lane;
+        TopKSelector<kGroupThreads, kCap> sel;
+        sel.bind(sel_mem + g * kSelBytes, gtid, 1 + g, p.err);
+        float* wg = w_s + g * 64;
+        int acc_it = 0;
+        for (int u = blockIdx.x; u < p.n_units; u += gridDim.x) {
+            const Unit U = unit_of(p, u);
+            const int t = g == 0 ? U.t_lo : U.t_hi;
+            const bool row_ok = t >= 0;
+            int64_t limit = 0;  // keys s < limit belong to this row
+            if (row_ok) {
+                const int64_t pr = query_position(p.kv_len, U.b, p.T, p.S, t);
+                limit = pr + 1 < U.key_hi ? pr + 1 : U.key_hi;
+                const int64_t wrow = (static_cast<int64_t>(U.b) * p.T + t) * 64;
+                if (gtid < 64) wg[gtid] = load_elem(p.w, wrow + gtid, p.w_dtype);
+            }
+            sel.reset();
+            for (int i = 0; i < U.ntiles; ++i, ++acc_it) {
+                const int a = acc_it & 1;
+                tc::mbar_wait(&tfull[a], (acc_it >> 1) & 1, abort, p.err);
+                tc::tc_fence_after();
+                uint32_t r[64];
+                const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + a * kN + g * 64;
+                TSI_TMEM_LD32(taddr, r);
+                TSI_TMEM_LD32(taddr + 32, (r + 32));
+                tc::tmem_wait_ld();
+                tc::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&tempty[a]);
+                float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+                const float4* w4 = reinterpret_cast<const float4*>(wg);
+#pragma unroll
+                for (int h = 0; h < 64; h += 4) {
+                    const float4 wv = w4[h >> 2];
+                    acc0 = fmaf(wv.x, fmaxf(__uint_as_float(r[h + 0]), 0.f), acc0);
+                    acc1 = fmaf(wv.y, fmaxf(__uint_as_float(r[h + 1]), 0.f), acc1);
+                    acc2 = fmaf(wv.z, fmaxf(__uint_as_float(r[h + 2]), 0.f), acc2);
+                    acc3 = fmaf(wv.w, fmaxf(__uint_as_float(r[h + 3]), 0.f), acc3);
+                }
+                const float score = (acc0 + acc1) + (acc2 + acc3);
+                const int64_t s = U.key_lo + static_cast<int64_t>(i) * kTileKeys + quad * 32 + lane;
+                sel.make_room(p.topk);
+                sel.offer(row_ok && s < limit, make_key(score, static_cast<uint32_t>(s)));
+            }
+            if (row_ok) {
+                const int64_t row = static_cast<int64_t>(U.b) * p.T + t;
+                if (p.n_chunks == 1) {
+                    sel.finalize(p.topk, p.idx + row * p.topk,
+                                 p.score ? p.score + row * p.topk : nullptr);
+                } else {
+                    const int64_t slot = row * p.n_chunks + U.chunk;
+                    sel.dump(p.topk, p.cand + slot * p.topk, p.cand_cnt + slot);
+                }
+            }
+        }
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ------------------------------------------------------------------------------ host
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        cudaDriverEntryPointQueryResult q;
+        void* f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+// Row-major [rows, 128 elements] tensor, 128-row boxes of 128 bytes, 128-byte swizzle.
+bool encode_rows128(CUtensorMap* map, const void* ptr, int64_t rows, int qk_dtype) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const bool bf16 = qk_dtype == TSI_BF16;
+    cuuint64_t dims[2] = {128, static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(bf16 ? 256 : 128)};
+    cuuint32_t box[2] = {bf16 ? 64u : 128u, 128u};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+                    const_cast<void*>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+constexpr int kPlanSMs = 152;
+
+void tc_plan(int B, int T, int S, int* n_chunks, int* chunk_keys) {
+    const int64_t pairs = static_cast<int64_t>(B) * ((T + 1) / 2);
+    int nc = 1;
+    if (pairs < kPlanSMs && S > 4096) {
+        const int by_keys = (S + 2047) / 2048;
+        const int by_sm = static_cast<int>((kPlanSMs + pairs - 1) / pairs);
+        nc = by_keys < by_sm ? by_keys : by_sm;
+        if (nc < 1) nc = 1;
+    }
+    int ck = (S + nc - 1) / nc;
+    ck = (ck + kTileKeys - 1) / kTileKeys * kTileKeys;
+    if (ck < kTileKeys) ck = kTileKeys;
+    *n_chunks = nc;
+    *chunk_keys = ck;
+}
+
+int sm_count() {
+    static int n = 0;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (n <= 0) n = kPlanSMs;
+    });
+    return n;
+}
+
+template <int QK>
+cudaError_t launch_qk(const IndexerArgs& a, void* workspace, cudaStream_t st) {
+    CUtensorMap tk, tq;
+    if (!encode_rows128(&tk, a.kI, static_cast<int64_t>(a.B) * a.S, QK) ||
+        !encode_rows128(&tq, a.qI, static_cast<int64_t>(a.B) * a.T * 64, QK))
+        return cudaErrorInvalidValue;
+    TcParams p{};
+    p.w = a.w;
+    p.w_dtype = a.w_dtype;
+    p.B = a.B;
+    p.T = a.T;
+    p.S = a.S;
+    p.topk = a.topk;
+    p.kv_len = a.kv_len;
+    p.idx = a.idx;
+    p.score = a.score;
+    p.err = a.err;
+    tc_plan(a.B, a.T, a.S, &p.n_chunks, &p.chunk_keys);
+    const int64_t pairs = static_cast<int64_t>(a.B) * ((a.T + 1) / 2);
+    p.n_units = static_cast<int>(pairs * p.n_chunks);
+    const int rows = a.B * a.T;
+    if (p.n_chunks > 1) {
+        p.cand = static_cast<uint64_t*>(workspace);
+        p.cand_cnt = reinterpret_cast<int*>(p.cand + static_cast<size_t>(rows) * p.n_chunks * a.topk);
+    }
+    constexpr int smem = smem_bytes<QK>();
+    cudaError_t e = cudaFuncSetAttribute(tsi_indexer_tc_kernel<QK>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    const int grid = p.n_units < sm_count() ? p.n_units : sm_count();
+    tsi_indexer_tc_kernel<QK><<<grid, kThreads, smem, st>>>(tk, tq, p);
+    note_launches(1);
+    e = cudaGetLastError();
+    if (e != cudaSuccess || p.n_chunks == 1) return e;
+    return launch_topk_merge(rows, a.topk, p.n_chunks, p.cand, p.cand_cnt, a.idx, a.score, a.err,
+                             st);
+}
+
+}  // namespace
+
+bool tc_indexer_supported(int qk_dtype, int H_I, int d_I) {
+    return (qk_dtype == TSI_BF16 || qk_dtype == TSI_E4M3) && H_I == 64 && d_I == 128;
+}
+
+size_t tc_indexer_workspace_bytes(int B, int T, int S, int topk) {
+    int nc, ck;
+    tc_plan(B, T, S, &nc, &ck);
+    if (nc <= 1) return 0;
+    const size_t slots = static_cast<size_t>(B) * T * nc;
+    return slots * topk * sizeof(uint64_t) + ((slots * sizeof(int) + 255) & ~size_t(255));
+}
+
+cudaError_t launch_indexer_tc(const IndexerArgs& a, void* workspace, cudaStream_t st) {
+    if (a.B * a.T == 0) return cudaSuccess;
+    return a.qk_dtype == TSI_E4M3 ? launch_qk<TSI_E4M3>(a, workspace, st)
+                                  : launch_qk<TSI_BF16>(a, workspace, st);
 }
 
 }  // namespace tsi

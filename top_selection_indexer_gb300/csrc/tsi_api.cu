@@ -77,6 +77,17 @@ int tsi_version(void) { return 100; }
 
 uint64_t tsi_launch_count(void) { return tsi::g_launches.load(); }
 
+int tsi_indexer_topk_path(int qk_dtype, int H_I, int d_I) {
+    if (!qk_dtype_ok(qk_dtype)) return -1;
+    if (use_tc_indexer(qk_dtype, H_I, d_I)) return 1;
+    return tsi::generic_supported(H_I, d_I) ? 0 : -1;
+}
+
+int tsi_sparse_attn_path(int H, int Hkv, int Dqk, int Dv, int v_from_k) {
+    if (use_tc_attn(H, Hkv, Dqk, Dv, v_from_k != 0)) return 1;
+    return tsi::attn_generic_supported(H, Hkv, Dqk, Dv, v_from_k != 0) ? 0 : -1;
+}
+
 const char* tsi_last_error(void) { return g_msg; }
 
 size_t tsi_indexer_topk_workspace(int B, int T, int S, int H_I, int d_I, int topk,
