@@ -179,3 +179,14 @@ cudaError_t launch_attn_generic(const AttnArgs& a, void* workspace, cudaStream_t
 }
 
 }  // namespace tsi
+
+namespace tsi {
+
+cudaError_t launch_attn_combine(const AttnArgs& a, int n_splits, const float* part_o,
+                                const float* part_ml, cudaStream_t st) {
+    attn_combine_kernel<<<dim3(a.B * a.T, a.H), 128, 0, st>>>(a, n_splits, part_o, part_ml);
+    note_launches(1);
+    return cudaGetLastError();
+}
+
+}  // namespace tsi

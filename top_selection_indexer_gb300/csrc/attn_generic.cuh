@@ -24,4 +24,9 @@ void attn_generic_split_plan(int rows, int topk, int* n_splits, int* per_split);
 size_t attn_generic_workspace_bytes(int B, int T, int H, int Dv, int topk);
 cudaError_t launch_attn_generic(const AttnArgs& a, void* workspace, cudaStream_t st);
 
+// Merge split partials (slot = (row*n_splits + split)*H + h: unnormalized O [Dv], then
+// (max, sum) in base-2 units) into bf16 rows of a.out.
+cudaError_t launch_attn_combine(const AttnArgs& a, int n_splits, const float* part_o,
+                                const float* part_ml, cudaStream_t st);
+
 }  // namespace tsi

@@ -1,10 +1,528 @@
 // Tensor-core sparse MQA attention over the shared index rows (tcgen05 / TMEM).
+//
+// For every query row t (64 heads) of a layer and its selected keys S_t:
+//   O[t,h] = sum_{s in S_t} softmax_s(scale * Q[t,h] . K[s]) V[s]
+// with K = the 576-d latent row of key s and V = its first 512 dims ("GLM-5.2
+// 技术报告速览" §IndexShare: each layer runs its own sparse attention over the Full
+// layer's index set; "GLM 5.2: Built for Long Horizon Tasks" discussion §3: 576-d MLA
+// latent, 512 compressed + 64 RoPE dims, sparse attention over the indices).
+//
+// Both products are computed transposed so that the 128 gathered keys of a tile are the
+// MMA's M dimension and the 64 heads its N dimension:
+//   S^T[key, h] = K_tile . Q^T         (A = key rows, K-major; B = Q rows, K-major)
+//   O^T[d, h]  += V_tile^T . P^T       (A = the same key rows read MN-major as V^T,
+//                                       B = P^T written by the softmax threads)
+// O^T (512 x 64 fp32) lives in TMEM for the whole row; S^T takes 64 more columns.  One
+// softmax thread owns one key (one TMEM lane of S^T) and all 64 heads of it, so the
+// exponentials, the bf16 rounding of P and the running row sums need no cross-thread
+// traffic; the running max per head is refreshed only when a logit exceeds it by 2^16
+// (always on the first tile of a row), and then O^T is rescaled in place.
+//
+// Roles of one persistent CTA (288 threads):
+//   warp 0      TMEM allocator + single-thread MMA issuer
+//   warps 1..4  gather: 16-byte cp.async of the selected latent rows into nine 128-byte-
+//               swizzled 64-dim chunk tiles (per-chunk mbarriers), plus the Q TMA load
+//   warps 5..8  softmax (writes P^T over the RoPE chunk once S^T is done) and the
+//               row epilogue (1/l normalisation, bf16 stores)
+// Few rows (decode): a row's key tiles are split over CTAs and the unnormalised partials
+// are merged by the combine kernel.
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
 #include "kernels_tc.cuh"
+#include "tc_common.cuh"
+#include "topk_select.cuh"
 
 namespace tsi {
+namespace {
 
-bool tc_attn_supported(int, int, int, int, bool) { return false; }
-size_t tc_attn_workspace_bytes(int, int, int, int, int) { return 0; }
-cudaError_t launch_attn_tc(const AttnArgs&, void*, cudaStream_t) { return cudaErrorNotSupported; }
+constexpr int kKeys = 128;  // keys per tile: MMA M of S^T, MMA K of O^T
+constexpr int kHeads = 64;  // MMA N
+constexpr int kDqk = 576;
+constexpr int kDv = 512;
+constexpr int kChunks = kDqk / 64;  // 9 chunks of 64 dims (128 bytes) per latent row
+constexpr int kKVChunkBytes = kKeys * 128;
+constexpr int kQChunkBytes = kHeads * 128;
+constexpr int kPSlot = 8;  // the RoPE chunk's slot holds P^T once S^T is done
+constexpr int kThreads = 288;
+constexpr int kProdThread0 = 32;
+constexpr int kSoftThread0 = 160;
+constexpr int kSoftBar = 1;
+constexpr int kTmemCols = 512;
+constexpr int kColS = 0;
+constexpr int kColO = 64;  // O^T block m (d rows 128m..128m+127) at columns 64 + 64m
+constexpr float kRescaleLog2 = 16.f;
+constexpr uint32_t kIdescS = tc::instr_desc(1, 128, 64, 0, 0);
+constexpr uint32_t kIdescO = tc::instr_desc(1, 128, 64, 1, 1);
+
+constexpr int kMiscBytes = 64 * 4 * 4 + 4 * 64 * 4 + 32 * 8 + 16;
+constexpr int kSmemBytes = 1024 + kChunks * kQChunkBytes + kChunks * kKVChunkBytes + kMiscBytes;
+
+struct AttnTcParams {
+    const uint16_t* k;  // latent [B, S, 576] bf16
+    const int32_t* idx;  // [B*T, topk]
+    const int32_t* kv_len;
+    __nv_bfloat16* out;  // [B*T, 64, 512]
+    float* part_o;  // split partials or nullptr
+    float* part_ml;
+    int B, T, S, topk;
+    int tiles_per_row, n_splits, tiles_per_split, n_units;
+    float scale_log2;
+    unsigned* err;
+};
+
+struct Work {
+    int row, b, split, tile0, tile1;
+};
+
+__device__ __forceinline__ Work work_of(const AttnTcParams& p, int u) {
+    Work w;
+    w.split = u % p.n_splits;
+    w.row = u / p.n_splits;
+    w.b = w.row / p.T;
+    w.tile0 = w.split * p.tiles_per_split;
+    w.tile1 = w.tile0 + p.tiles_per_split < p.tiles_per_row ? w.tile0 + p.tiles_per_split
+                                                             : p.tiles_per_row;
+    return w;
+}
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+    const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(a));
+    const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(b));
+    return lo | (hi << 16);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    tsi_attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const AttnTcParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* base = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t* qs = base;
+    uint8_t* kv = qs + kChunks * kQChunkBytes;
+    float* m_s = reinterpret_cast<float*>(kv + kChunks * kKVChunkBytes);  // running max [64]
+    uint32_t* tmax_s = reinterpret_cast<uint32_t*>(m_s + 64);  // tile max (order bits) [64]
+    float* alpha_s = reinterpret_cast<float*>(tmax_s + 64);  // rescale factors [64]
+    float* inv_l = alpha_s + 64;  // [64]
+    float* lred = inv_l + 64;  // [4][64]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(lred + 4 * 64);
+    uint64_t* kv_full = bars;
+    uint64_t* kv_empty = bars + kChunks;
+    uint64_t* q_full = bars + 2 * kChunks;
+    uint64_t* q_empty = q_full + 1;
+    uint64_t* s_full = q_full + 2;
+    uint64_t* p_full = q_full + 3;
+    uint64_t* o_full = q_full + 4;
+    uint64_t* o_empty = q_full + 5;
+    uint64_t* done = q_full + 6;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_full + 7);
+    volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int c = 0; c < kChunks; ++c) {
+            tc::mbar_init(&kv_full[c], 128);
+            tc::mbar_init(&kv_empty[c], 1);
+        }
+        tc::mbar_init(q_full, 1);
+        tc::mbar_init(q_empty, 1);
+        tc::mbar_init(s_full, 1);
+        tc::mbar_init(p_full, 128);
+        tc::mbar_init(o_full, 1);
+        tc::mbar_init(o_empty, 128);
+        tc::mbar_init(done, 1);
+        *abort = 0;
+        tc::fence_barrier_init();
+    }
+    if (warp == 0) {
+        tc::tmem_alloc(tmem_slot, kTmemCols);
+        if (lane == 0) tc::prefetch_tmap(&tmap_q);
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t q_addr = tc::smem_addr(qs);
+    const uint32_t kv_addr = tc::smem_addr(kv);
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int it = 0, r_it = 0;
+            for (int u = blockIdx.x; u < p.n_units; u += gridDim.x, ++r_it) {
+                const Work W = work_of(p, u);
+                tc::mbar_wait(q_full, r_it & 1, abort, p.err);
+                for (int t = W.tile0; t < W.tile1; ++t, ++it) {
+                    const bool first = t == W.tile0;
+                    for (int c = 0; c < kChunks; ++c) {
+                        tc::mbar_wait(&kv_full[c], it & 1, abort, p.err);
+                        tc::fence_proxy_async();  // cp.async landed via the generic proxy
+                        tc::tc_fence_after();
+                        if (!*abort) {
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk) {
+                                const uint64_t da = tc::smem_desc(
+                                    kv_addr + c * kKVChunkBytes + kk * 32, 16, 1024);
+                                const uint64_t db = tc::smem_desc(
+                                    q_addr + c * kQChunkBytes + kk * 32, 16, 1024);
+                                tc::mma_bf16(tmem + kColS, da, db, kIdescS, (c | kk) ? 1u : 0u);
+                            }
+                        }
+                    }
+                    tc::mma_commit(s_full);
+                    if (t == W.tile1 - 1) tc::mma_commit(q_empty);
+                    tc::mbar_wait(p_full, it & 1, abort, p.err);
+                    if (first) tc::mbar_wait(o_empty, (r_it & 1) ^ 1, abort, p.err);
+                    tc::fence_proxy_async();  // P^T written with generic stores
+                    tc::tc_fence_after();
+                    for (int m = 0; m < 4; ++m) {
+                        if (!*abort) {
+#pragma unroll
+                            for (int kk = 0; kk < 8; ++kk) {
+                                const uint64_t da = tc::smem_desc(
+                                    kv_addr + 2 * m * kKVChunkBytes + kk * 2048, kKVChunkBytes, 1024);
+                                const uint64_t db = tc::smem_desc(
+                                    kv_addr + kPSlot * kKVChunkBytes + kk * 2048, kKVChunkBytes, 1024);
+                                tc::mma_bf16(tmem + kColO + 64 * m, da, db, kIdescO,
+                                             (first && kk == 0) ? 0u : 1u);
+                            }
+                        }
+                        tc::mma_commit(&kv_empty[2 * m]);
+                        tc::mma_commit(&kv_empty[2 * m + 1]);
+                    }
+                    tc::mma_commit(&kv_empty[kPSlot]);
+                }
+                tc::mma_commit(o_full);
+            }
+            tc::mma_commit(done);
+            tc::mbar_wait(done, 0, abort, p.err);
+        }
+    } else if (warp <= 4) {
+        // ------------------------------------------------------------ gather producers
+        const int pt = threadIdx.x - kProdThread0;
+        const int sub = pt & 7;  // 16-byte piece within a 128-byte chunk row
+        const int kr = pt >> 3;  // keys kr, kr+16, ..., kr+112 of the tile
+        int it = 0, r_it = 0;
+        for (int u = blockIdx.x; u < p.n_units; u += gridDim.x, ++r_it) {
+            const Work W = work_of(p, u);
+            if (pt == 0) {
+                tc::mbar_wait(q_empty, (r_it & 1) ^ 1, abort, p.err);
+                if (!*abort) {
+                    tc::mbar_expect_tx(q_full, kChunks * kQChunkBytes);
+                    for (int c = 0; c < kChunks; ++c)
+                        tc::tma_load_2d(qs + c * kQChunkBytes, &tmap_q, c * 64, W.row * kHeads,
+                                        q_full);
+                }
+            }
+            const int64_t len = seq_len(p.kv_len, W.b, p.S);
+            const int32_t* irow = p.idx + static_cast<int64_t>(W.row) * p.topk;
+            for (int t = W.tile0; t < W.tile1; ++t, ++it) {
+                const uint16_t* src[8];
+                uint32_t nbytes[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int e = t * kKeys + kr + 16 * i;
+                    const int s = e < p.topk ? irow[e] : -1;
+                    const bool ok = s >= 0 && s < len;
+                    src[i] = ok ? p.k + (static_cast<int64_t>(W.b) * p.S + s) * kDqk + sub * 8 : p.k;
+                    nbytes[i] = ok ? 16u : 0u;
+                }
+                for (int c = 0; c < kChunks; ++c) {
+                    tc::mbar_wait(&kv_empty[c], (it & 1) ^ 1, abort, p.err);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int k = kr + 16 * i;
+                        const uint32_t dst = kv_addr + c * kKVChunkBytes + (k >> 3) * 1024 +
+                                             (k & 7) * 128 + ((sub ^ (k & 7)) << 4);
+                        tc::cp_async16(dst, src[i] + (nbytes[i] ? c * 64 : 0), nbytes[i]);
+                    }
+                    tc::cp_async_arrive_noinc(&kv_full[c]);
+                }
+            }
+        }
+        asm volatile("cp.async.wait_all;" ::: "memory");
+    } else {
+        // ------------------------------------------------------------ softmax + epilogue
+        const int st = threadIdx.x - kSoftThread0;
+        const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31
+        const int k = quad * 32 + lane;  // key slot of the tile owned by this thread
+        const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+        const float neg_inf = -__int_as_float(0x7f800000);
+        uint8_t* prow = kv + kPSlot * kKVChunkBytes + (k >> 3) * 1024 + (k & 7) * 128;
+        int it = 0, r_it = 0;
+        for (int u = blockIdx.x; u < p.n_units; u += gridDim.x, ++r_it) {
+            const Work W = work_of(p, u);
+            const int64_t len = seq_len(p.kv_len, W.b, p.S);
+            const int32_t* irow = p.idx + static_cast<int64_t>(W.row) * p.topk;
+            if (st < 64) {
+                m_s[st] = neg_inf;
+                tmax_s[st] = 0u;
+            }
+            float l_part[64];
+#pragma unroll
+            for (int h = 0; h < 64; ++h) l_part[h] = 0.f;
+            named_bar(kSoftBar, 128);
+            for (int t = W.tile0; t < W.tile1; ++t, ++it) {
+                const int e = t * kKeys + k;
+                const int s = e < p.topk ? irow[e] : -1;
+                const bool valid = s >= 0 && s < len;
+                tc::mbar_wait(s_full, it & 1, abort, p.err);
+                tc::tc_fence_after();
+                // pass 1: does any logit of this key exceed the running max by 2^16?
+                const uint32_t s_addr = tmem + lane_base + kColS;
+                bool over = false;
+                {
+                    uint32_t z[64];
+                    TSI_TMEM_LD32(s_addr, z);
+                    TSI_TMEM_LD32(s_addr + 32, (z + 32));
+                    tc::tmem_wait_ld();
+#pragma unroll
+                    for (int h = 0; h < 64; ++h)
+                        over |= valid && (__uint_as_float(z[h]) * p.scale_log2 > m_s[h] + kRescaleLog2);
+                }
+                if (tc::bar_red_or(kSoftBar, 128, over)) {
+                    // exact tile max per head, new running max, rescale what O^T holds
+                    {
+                        uint32_t z[64];
+                        TSI_TMEM_LD32(s_addr, z);
+                        TSI_TMEM_LD32(s_addr + 32, (z + 32));
+                        tc::tmem_wait_ld();
+#pragma unroll
+                        for (int h = 0; h < 64; ++h) {
+                            const float zh = valid ? __uint_as_float(z[h]) * p.scale_log2 : neg_inf;
+                            const uint32_t v = __reduce_max_sync(kFull, score_order_bits(zh));
+                            if (lane == 0) atomicMax(&tmax_s[h], v);
+                        }
+                    }
+                    named_bar(kSoftBar, 128);
+                    if (st < 64) {
+                        const float mo = m_s[st];
+                        const float mn = fmaxf(mo, order_bits_score(tmax_s[st]));
+                        alpha_s[st] = mo == neg_inf ? 0.f : ex2(mo - mn);
+                        m_s[st] = mn;
+                        tmax_s[st] = 0u;
+                    }
+                    named_bar(kSoftBar, 128);
+                    if (t != W.tile0) {
+                        for (int m = 0; m < 4; ++m) {
+#pragma unroll
+                            for (int half = 0; half < 2; ++half) {
+                                uint32_t o[32];
+                                const uint32_t ta = tmem + lane_base + kColO + 64 * m + 32 * half;
+                                TSI_TMEM_LD32(ta, o);
+                                tc::tmem_wait_ld();
+#pragma unroll
+                                for (int j = 0; j < 32; ++j)
+                                    o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha_s[32 * half + j]);
+                                TSI_TMEM_ST32(ta, o);
+                            }
+                        }
+                        tc::tmem_wait_st();
+                    }
+#pragma unroll
+                    for (int h = 0; h < 64; ++h) l_part[h] *= alpha_s[h];
+                }
+                // pass 2: P^T row of this key, 64 heads as bf16, 128-byte swizzled (MN-major B)
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t z[32];
+                    TSI_TMEM_LD32(s_addr + 32 * half, z);
+                    tc::tmem_wait_ld();
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj) {
+                        const int j = 4 * half + jj;
+                        float pv[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const int h = 8 * j + i;
+                            const float zh = __uint_as_float(z[8 * jj + i]) * p.scale_log2;
+                            const float pe = valid ? ex2(zh - m_s[h]) : 0.f;
+                            const float pr = __bfloat162float(__float2bfloat16_rn(pe));
+                            l_part[h] += pr;
+                            pv[i] = pr;
+                        }
+                        uint4 v;
+                        v.x = pack_bf16(pv[0], pv[1]);
+                        v.y = pack_bf16(pv[2], pv[3]);
+                        v.z = pack_bf16(pv[4], pv[5]);
+                        v.w = pack_bf16(pv[6], pv[7]);
+                        *reinterpret_cast<uint4*>(prow + ((j ^ (k & 7)) << 4)) = v;
+                    }
+                }
+                tc::fence_proxy_async();
+                tc::tc_fence_before();
+                tc::mbar_arrive(p_full);
+            }
+            // ---------------------------------------------------------- row epilogue
+            // row sums: reduce the 64 per-thread partials over the 32 lanes (each lane ends
+            // with heads 2*lane, 2*lane+1), then over the 4 warps
+#pragma unroll
+            for (int o = 16, n = 64; o >= 1; o >>= 1, n >>= 1) {
+                const bool upper = (lane & o) != 0;
+#pragma unroll
+                for (int i = 0; i < n / 2; ++i) {
+                    const float send = upper ? l_part[i] : l_part[i + n / 2];
+                    const float keep = upper ? l_part[i + n / 2] : l_part[i];
+                    l_part[i] = keep + __shfl_xor_sync(kFull, send, o);
+                }
+            }
+            lred[quad * 64 + 2 * lane] = l_part[0];
+            lred[quad * 64 + 2 * lane + 1] = l_part[1];
+            tc::mbar_wait(o_full, r_it & 1, abort, p.err);
+            tc::tc_fence_after();
+            named_bar(kSoftBar, 128);
+            if (st < 64) {
+                const float L = (lred[st] + lred[64 + st]) + (lred[128 + st] + lred[192 + st]);
+                inv_l[st] = L > 0.f ? 1.f / L : 0.f;
+                if (p.part_o) {
+                    const int64_t slot = (static_cast<int64_t>(W.row) * p.n_splits + W.split) * kHeads + st;
+                    p.part_ml[2 * slot] = m_s[st];
+                    p.part_ml[2 * slot + 1] = L;
+                }
+            }
+            named_bar(kSoftBar, 128);
+            for (int m = 0; m < 4; ++m) {
+                const int d = 128 * m + 32 * quad + lane;
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t o[32];
+                    TSI_TMEM_LD32(tmem + lane_base + kColO + 64 * m + 32 * half, o);
+                    tc::tmem_wait_ld();
+                    if (p.part_o) {
+                        float* po = p.part_o +
+                                    ((static_cast<int64_t>(W.row) * p.n_splits + W.split) * kHeads) * kDv + d;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            po[static_cast<int64_t>(32 * half + j) * kDv] = __uint_as_float(o[j]);
+                    } else {
+                        __nv_bfloat16* out = p.out + static_cast<int64_t>(W.row) * kHeads * kDv + d;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const int h = 32 * half + j;
+                            out[static_cast<int64_t>(h) * kDv] =
+                                __float2bfloat16_rn(__uint_as_float(o[j]) * inv_l[h]);
+                        }
+                    }
+                }
+            }
+            tc::tc_fence_before();
+            tc::mbar_arrive(o_empty);
+        }
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ------------------------------------------------------------------------------ host
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        cudaDriverEntryPointQueryResult q;
+        void* f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+constexpr int kPlanSMs = 152;
+
+void attn_tc_plan(int rows, int topk, int* n_splits, int* tiles_per_split, int* tiles) {
+    const int nt = (topk + kKeys - 1) / kKeys;
+    int ns = 1;
+    if (rows > 0 && rows < kPlanSMs) {
+        ns = (2 * kPlanSMs + rows - 1) / rows;
+        if (ns > nt) ns = nt;
+        if (ns < 1) ns = 1;
+    }
+    const int tps = (nt + ns - 1) / ns;
+    *tiles = nt;
+    *tiles_per_split = tps;
+    *n_splits = (nt + tps - 1) / tps;
+}
+
+int sm_count() {
+    static int n = 0;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (n <= 0) n = kPlanSMs;
+    });
+    return n;
+}
+
+}  // namespace
+
+bool tc_attn_supported(int H, int Hkv, int Dqk, int Dv, bool v_from_k) {
+    return H == kHeads && Hkv == 1 && Dqk == kDqk && Dv == kDv && v_from_k;
+}
+
+size_t tc_attn_workspace_bytes(int B, int T, int H, int Dv, int topk) {
+    int ns, tps, nt;
+    attn_tc_plan(B * T, topk, &ns, &tps, &nt);
+    if (ns <= 1) return 0;
+    const size_t slots = static_cast<size_t>(B) * T * ns * H;
+    return slots * Dv * sizeof(float) + slots * 2 * sizeof(float);
+}
+
+cudaError_t launch_attn_tc(const AttnArgs& a, void* workspace, cudaStream_t st) {
+    const int rows = a.B * a.T;
+    if (rows == 0) return cudaSuccess;
+    auto fn = encode_fn();
+    if (!fn) return cudaErrorNotSupported;
+    CUtensorMap tq;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(kDqk), static_cast<cuuint64_t>(rows) * kHeads};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(kDqk) * 2};
+    cuuint32_t box[2] = {64, kHeads};
+    cuuint32_t estr[2] = {1, 1};
+    if (fn(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.q), dims, strides, box,
+           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    AttnTcParams p{};
+    p.k = static_cast<const uint16_t*>(a.k);
+    p.idx = a.idx;
+    p.kv_len = a.kv_len;
+    p.out = static_cast<__nv_bfloat16*>(a.out);
+    p.B = a.B;
+    p.T = a.T;
+    p.S = a.S;
+    p.topk = a.topk;
+    attn_tc_plan(rows, a.topk, &p.n_splits, &p.tiles_per_split, &p.tiles_per_row);
+    p.n_units = rows * p.n_splits;
+    p.scale_log2 = a.scale * 1.4426950408889634f;
+    p.err = a.err;
+    if (p.n_splits > 1) {
+        p.part_o = static_cast<float*>(workspace);
+        p.part_ml = p.part_o + static_cast<size_t>(rows) * p.n_splits * kHeads * kDv;
+    }
+    cudaError_t e = cudaFuncSetAttribute(tsi_attn_tc_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const int grid = p.n_units < sm_count() ? p.n_units : sm_count();
+    tsi_attn_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(tq, p);
+    note_launches(1);
+    e = cudaGetLastError();
+    if (e != cudaSuccess || p.n_splits == 1) return e;
+    return launch_attn_combine(a, p.n_splits, p.part_o, p.part_ml, st);
+}
 
 }  // namespace tsi
