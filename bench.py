@@ -137,7 +137,11 @@ def run_gpu(args, rank, world):
     torch.cuda.set_device(dev)
     tsi.load()
     cfg = get_config(args.config)
-    G, L = cfg.n_groups, cfg.T
+    if args.groups:
+        cfg = cfg.with_(n_layers=min(cfg.n_layers, args.groups * cfg.group))
+    if args.tail_rows:  # chunked prefill: only the last R query rows over the full cache
+        cfg = cfg.with_(T=min(args.tail_rows, cfg.S))
+    G, L = cfg.n_groups, cfg.S
     stream = torch.cuda.current_stream()
 
     # --- resident inputs (every layer distinct) --------------------------------------
@@ -253,7 +257,8 @@ def run_gpu(args, rank, world):
                                f"(1 Full + {cfg.group - 1} Shared), indexer H_I={cfg.H_I} "
                                f"d_I={cfg.d_I} {cfg.qk_dtype}, k={cfg.topk}, MQA {cfg.H} heads "
                                f"over a {cfg.Dqk}-d bf16 latent (value = first {cfg.Dv})",
-                   "config_id": cfg.id, "L": L, "layers": cfg.n_layers, "topk": cfg.topk,
+                   "config_id": cfg.id, "L": L, "query_rows": cfg.B * cfg.T,
+                   "layers": cfg.n_layers, "topk": cfg.topk,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "inputs larger than L2 (not flushed)"},
         "indexer_topk_rows_per_s": round(world * rows / (ms_idx / 1e3), 1),
@@ -414,6 +419,9 @@ def main():
     ap.add_argument("--config", type=int, default=4)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--tail-rows", type=int, default=0,
+                    help="profiling: only the last R query rows of the prefill")
+    ap.add_argument("--groups", type=int, default=0, help="profiling: only the first G groups")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
