@@ -18,12 +18,17 @@
 // traffic; the running max per head is refreshed only when a logit exceeds it by 2^16
 // (always on the first tile of a row), and then O^T is rescaled in place.
 //
-// Roles of one persistent CTA (288 threads):
-//   warp 0      TMEM allocator + single-thread MMA issuer
-//   warps 1..4  gather: 16-byte cp.async of the selected latent rows into nine 128-byte-
-//               swizzled 64-dim chunk tiles (per-chunk mbarriers), plus the Q TMA load
-//   warps 5..8  softmax (writes P^T over the RoPE chunk once S^T is done) and the
-//               row epilogue (1/l normalisation, bf16 stores)
+// Roles of one persistent CTA (512 threads):
+//   warps 0..3   softmax (writes P^T over the RoPE chunk once S^T is done) and the row
+//                epilogue (1/l normalisation, bf16 stores)
+//   warp 4       TMEM allocator + single-thread MMA issuer
+//   warps 5..15  gather: 16-byte cp.async of the selected latent rows into nine 128-byte-
+//                swizzled 64-dim chunk tiles (per-chunk mbarriers), plus the Q TMA load.
+//                The gather rate of cp.async grows with the number of issuing warps, so it
+//                gets most of the CTA's warps.
+// Row sums l[h] = sum_s P[h,s] come from the tensor core too: a fifth M=128 block
+// multiplies a 128-byte tile of ones (no-swizzle descriptor, zero strides: every core
+// matrix reads the same bytes) by P^T, so l sums exactly the bf16 P that multiplies V.
 // Few rows (decode): a row's key tiles are split over CTAs and the unnormalised partials
 // are merged by the combine kernel.
 #include <mutex>
@@ -45,16 +50,22 @@ constexpr int kChunks = kDqk / 64;  // 9 chunks of 64 dims (128 bytes) per laten
 constexpr int kKVChunkBytes = kKeys * 128;
 constexpr int kQChunkBytes = kHeads * 128;
 constexpr int kPSlot = 8;  // the RoPE chunk's slot holds P^T once S^T is done
-constexpr int kThreads = 288;
-constexpr int kProdThread0 = 32;
-constexpr int kSoftThread0 = 160;
+// 16 warps = 4 warpgroups: warpgroup 0 softmax/epilogue (registers raised), warp 4 MMA,
+// warps 5..15 gather producers (warpgroups 1..3, registers lowered).
+constexpr int kThreads = 512;
+constexpr int kMmaWarp = 4;
+constexpr int kProdThread0 = 160;
+constexpr int kProducers = kThreads - kProdThread0;  // 352
+constexpr int kSoftThread0 = 0;
 constexpr int kSoftBar = 1;
 constexpr int kTmemCols = 512;
 constexpr int kColS = 0;
 constexpr int kColO = 64;  // O^T block m (d rows 128m..128m+127) at columns 64 + 64m
+constexpr int kColL = kColO + 256;  // row sums (every lane holds the same 64 values)
 constexpr float kRescaleLog2 = 16.f;
 constexpr uint32_t kIdescS = tc::instr_desc(1, 128, 64, 0, 0);
 constexpr uint32_t kIdescO = tc::instr_desc(1, 128, 64, 1, 1);
+constexpr uint32_t kIdescL = tc::instr_desc(1, 128, 64, 0, 1);
 
 constexpr int kMiscBytes = 64 * 4 * 4 + 4 * 64 * 4 + 32 * 8 + 16;
 constexpr int kSmemBytes = 1024 + kChunks * kQChunkBytes + kChunks * kKVChunkBytes + kMiscBytes;
@@ -109,9 +120,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* m_s = reinterpret_cast<float*>(kv + kChunks * kKVChunkBytes);  // running max [64]
     uint32_t* tmax_s = reinterpret_cast<uint32_t*>(m_s + 64);  // tile max (order bits) [64]
     float* alpha_s = reinterpret_cast<float*>(tmax_s + 64);  // rescale factors [64]
-    float* inv_l = alpha_s + 64;  // [64]
-    float* lred = inv_l + 64;  // [4][64]
-    uint64_t* bars = reinterpret_cast<uint64_t*>(lred + 4 * 64);
+    float* l_s = alpha_s + 64;  // row sums of the unit [64]
+    uint16_t* ones = reinterpret_cast<uint16_t*>(l_s + 64);  // 64 x bf16 1.0 (128 bytes)
+    uint64_t* bars = reinterpret_cast<uint64_t*>(l_s + 64 + 4 * 64);
     uint64_t* kv_full = bars;
     uint64_t* kv_empty = bars + kChunks;
     uint64_t* q_full = bars + 2 * kChunks;
@@ -127,9 +138,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
+    if (threadIdx.x < 64) ones[threadIdx.x] = 0x3F80;  // bf16 1.0
+    tc::fence_proxy_async();  // read by the tensor core
     if (threadIdx.x == 0) {
         for (int c = 0; c < kChunks; ++c) {
-            tc::mbar_init(&kv_full[c], 128);
+            tc::mbar_init(&kv_full[c], kProducers);
             tc::mbar_init(&kv_empty[c], 1);
         }
         tc::mbar_init(q_full, 1);
@@ -142,7 +155,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort = 0;
         tc::fence_barrier_init();
     }
-    if (warp == 0) {
+    if (warp == kMmaWarp) {
         tc::tmem_alloc(tmem_slot, kTmemCols);
         if (lane == 0) tc::prefetch_tmap(&tmap_q);
     }
@@ -153,7 +166,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t q_addr = tc::smem_addr(qs);
     const uint32_t kv_addr = tc::smem_addr(kv);
 
-    if (warp == 0) {
+    if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             int it = 0, r_it = 0;
@@ -198,6 +211,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tc::mma_commit(&kv_empty[2 * m]);
                         tc::mma_commit(&kv_empty[2 * m + 1]);
                     }
+                    if (!*abort) {  // row sums: ones[128 x 16] . P^T per 16-key step
+                        const uint64_t da = tc::smem_desc(tc::smem_addr(ones), 0, 0, 0);
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const uint64_t db = tc::smem_desc(
+                                kv_addr + kPSlot * kKVChunkBytes + kk * 2048, kKVChunkBytes, 1024);
+                            tc::mma_bf16(tmem + kColL, da, db, kIdescL, (first && kk == 0) ? 0u : 1u);
+                        }
+                    }
                     tc::mma_commit(&kv_empty[kPSlot]);
                 }
                 tc::mma_commit(o_full);
@@ -205,11 +227,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::mma_commit(done);
             tc::mbar_wait(done, 0, abort, p.err);
         }
-    } else if (warp <= 4) {
+    } else if (warp > kMmaWarp) {
         // ------------------------------------------------------------ gather producers
+        // a chunk is 128 keys x 8 pieces of 16 bytes; thread pt copies pieces pt, pt+352,
+        // pt+704 of every chunk (at most 3 keys per thread and tile)
         const int pt = threadIdx.x - kProdThread0;
-        const int sub = pt & 7;  // 16-byte piece within a 128-byte chunk row
-        const int kr = pt >> 3;  // keys kr, kr+16, ..., kr+112 of the tile
         int it = 0, r_it = 0;
         for (int u = blockIdx.x; u < p.n_units; u += gridDim.x, ++r_it) {
             const Work W = work_of(p, u);
@@ -225,24 +247,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int64_t len = seq_len(p.kv_len, W.b, p.S);
             const int32_t* irow = p.idx + static_cast<int64_t>(W.row) * p.topk;
             for (int t = W.tile0; t < W.tile1; ++t, ++it) {
-                const uint16_t* src[8];
-                uint32_t nbytes[8];
+                const uint16_t* src[3];
+                uint32_t nbytes[3];
+                uint32_t dst0[3];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int e = t * kKeys + kr + 16 * i;
-                    const int s = e < p.topk ? irow[e] : -1;
+                for (int j = 0; j < 3; ++j) {
+                    const int piece = pt + kProducers * j;
+                    const int k = (piece >> 3) & (kKeys - 1);
+                    const int sub = piece & 7;
+                    const int e = t * kKeys + k;
+                    const int s = (piece < kKeys * 8 && e < p.topk) ? irow[e] : -1;
                     const bool ok = s >= 0 && s < len;
-                    src[i] = ok ? p.k + (static_cast<int64_t>(W.b) * p.S + s) * kDqk + sub * 8 : p.k;
-                    nbytes[i] = ok ? 16u : 0u;
+                    src[j] = ok ? p.k + (static_cast<int64_t>(W.b) * p.S + s) * kDqk + sub * 8 : p.k;
+                    nbytes[j] = ok ? 16u : 0u;
+                    dst0[j] = kv_addr + (k >> 3) * 1024 + (k & 7) * 128 + ((sub ^ (k & 7)) << 4);
                 }
                 for (int c = 0; c < kChunks; ++c) {
                     tc::mbar_wait(&kv_empty[c], (it & 1) ^ 1, abort, p.err);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int k = kr + 16 * i;
-                        const uint32_t dst = kv_addr + c * kKVChunkBytes + (k >> 3) * 1024 +
-                                             (k & 7) * 128 + ((sub ^ (k & 7)) << 4);
-                        tc::cp_async16(dst, src[i] + (nbytes[i] ? c * 64 : 0), nbytes[i]);
+                    for (int j = 0; j < 3; ++j) {
+                        if (pt + kProducers * j < kKeys * 8)
+                            tc::cp_async16(dst0[j] + c * kKVChunkBytes,
+                                           src[j] + (nbytes[j] ? c * 64 : 0), nbytes[j]);
                     }
                     tc::cp_async_arrive_noinc(&kv_full[c]);
                 }
@@ -252,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ------------------------------------------------------------ softmax + epilogue
         const int st = threadIdx.x - kSoftThread0;
-        const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31
+        const int quad = warp;  // TMEM lanes 32*quad .. 32*quad+31
         const int k = quad * 32 + lane;  // key slot of the tile owned by this thread
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
         const float neg_inf = -__int_as_float(0x7f800000);
@@ -266,9 +292,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 m_s[st] = neg_inf;
                 tmax_s[st] = 0u;
             }
-            float l_part[64];
-#pragma unroll
-            for (int h = 0; h < 64; ++h) l_part[h] = 0.f;
             named_bar(kSoftBar, 128);
             for (int t = W.tile0; t < W.tile1; ++t, ++it) {
                 const int e = t * kKeys + k;
@@ -312,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     named_bar(kSoftBar, 128);
                     if (t != W.tile0) {
-                        for (int m = 0; m < 4; ++m) {
+                        for (int m = 0; m < 5; ++m) {  // the 4 O^T blocks and the row sums
 #pragma unroll
                             for (int half = 0; half < 2; ++half) {
                                 uint32_t o[32];
@@ -327,8 +350,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         tc::tmem_wait_st();
                     }
-#pragma unroll
-                    for (int h = 0; h < 64; ++h) l_part[h] *= alpha_s[h];
                 }
                 // pass 2: P^T row of this key, 64 heads as bf16, 128-byte swizzled (MN-major B)
 #pragma unroll
@@ -345,9 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const int h = 8 * j + i;
                             const float zh = __uint_as_float(z[8 * jj + i]) * p.scale_log2;
                             const float pe = valid ? ex2(zh - m_s[h]) : 0.f;
-                            const float pr = __bfloat162float(__float2bfloat16_rn(pe));
-                            l_part[h] += pr;
-                            pv[i] = pr;
+                            pv[i] = pe;
                         }
                         uint4 v;
                         v.x = pack_bf16(pv[0], pv[1]);
@@ -362,37 +381,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc::mbar_arrive(p_full);
             }
             // ---------------------------------------------------------- row epilogue
-            // row sums: reduce the 64 per-thread partials over the 32 lanes (each lane ends
-            // with heads 2*lane, 2*lane+1), then over the 4 warps
-#pragma unroll
-            for (int o = 16, n = 64; o >= 1; o >>= 1, n >>= 1) {
-                const bool upper = (lane & o) != 0;
-#pragma unroll
-                for (int i = 0; i < n / 2; ++i) {
-                    const float send = upper ? l_part[i] : l_part[i + n / 2];
-                    const float keep = upper ? l_part[i + n / 2] : l_part[i];
-                    l_part[i] = keep + __shfl_xor_sync(kFull, send, o);
-                }
-            }
-            lred[quad * 64 + 2 * lane] = l_part[0];
-            lred[quad * 64 + 2 * lane + 1] = l_part[1];
             tc::mbar_wait(o_full, r_it & 1, abort, p.err);
             tc::tc_fence_after();
-            named_bar(kSoftBar, 128);
-            if (st < 64) {
-                const float L = (lred[st] + lred[64 + st]) + (lred[128 + st] + lred[192 + st]);
-                inv_l[st] = L > 0.f ? 1.f / L : 0.f;
-                if (p.part_o) {
-                    const int64_t slot = (static_cast<int64_t>(W.row) * p.n_splits + W.split) * kHeads + st;
-                    p.part_ml[2 * slot] = m_s[st];
-                    p.part_ml[2 * slot + 1] = L;
-                }
-            }
-            named_bar(kSoftBar, 128);
-            for (int m = 0; m < 4; ++m) {
-                const int d = 128 * m + 32 * quad + lane;
+            for (int half = 0; half < 2; ++half) {
+                uint32_t lv[32];  // row sums of heads 32*half .. 32*half+31 (same in every lane)
+                TSI_TMEM_LD32(tmem + lane_base + kColL + 32 * half, lv);
+                tc::tmem_wait_ld();
+                if (st == 0) {
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
+                    for (int j = 0; j < 32; ++j) l_s[32 * half + j] = __uint_as_float(lv[j]);
+                }
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const float L = __uint_as_float(lv[j]);
+                    lv[j] = __float_as_uint(L > 0.f ? 1.f / L : 0.f);
+                }
+                for (int m = 0; m < 4; ++m) {
+                    const int d = 128 * m + 32 * quad + lane;
                     uint32_t o[32];
                     TSI_TMEM_LD32(tmem + lane_base + kColO + 64 * m + 32 * half, o);
                     tc::tmem_wait_ld();
@@ -405,12 +410,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     } else {
                         __nv_bfloat16* out = p.out + static_cast<int64_t>(W.row) * kHeads * kDv + d;
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            const int h = 32 * half + j;
-                            out[static_cast<int64_t>(h) * kDv] =
-                                __float2bfloat16_rn(__uint_as_float(o[j]) * inv_l[h]);
-                        }
+                        for (int j = 0; j < 32; ++j)
+                            out[static_cast<int64_t>(32 * half + j) * kDv] =
+                                __float2bfloat16_rn(__uint_as_float(o[j]) * __uint_as_float(lv[j]));
                     }
+                }
+            }
+            if (p.part_o) {
+                named_bar(kSoftBar, 128);
+                if (st < 64) {
+                    const int64_t slot = (static_cast<int64_t>(W.row) * p.n_splits + W.split) * kHeads + st;
+                    p.part_ml[2 * slot] = m_s[st];
+                    p.part_ml[2 * slot + 1] = l_s[st];
                 }
             }
             tc::tc_fence_before();
@@ -419,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc::tc_fence_before();
     __syncthreads();
-    if (warp == 0) {
+    if (warp == kMmaWarp) {
         tc::tc_fence_after();
         tc::tmem_dealloc(tmem, kTmemCols);
     }

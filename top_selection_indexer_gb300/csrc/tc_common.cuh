@@ -170,6 +170,12 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32
                  : "memory");
 }
 
+// Bring `bytes` (a multiple of 16, 16-byte aligned) of global memory into L2 without
+// landing anywhere else.
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // Arrive on `bar` once every cp.async issued so far by this thread has landed (the
 // barrier's expected count includes this arrival).
 __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
