@@ -12,11 +12,12 @@
 // heads of its query row inside its registers: ReLU, times the gate weight, summed --
 // no cross-thread reduction.
 //
-// Roles of one persistent CTA (320 threads):
-//   warp 0      TMA producer: Q tile of the unit, key tiles into a ring of stages
-//   warp 1      TMEM allocator + single-thread MMA issuer (two TMEM accumulators)
-//   warps 2..9  two epilogue groups of 4 warps (one per query row of the unit); group
-//               g reads columns [64g, 64g+64) of the accumulator and owns a selector
+// Roles of one persistent CTA (576 threads):
+//   warp 0       TMA producer: Q tile of the unit, key tiles into a ring of stages
+//   warp 1       TMEM allocator + single-thread MMA issuer (four TMEM accumulators)
+//   warps 2..17  two epilogue groups of 8 warps (one per query row of the unit); group g
+//                reads columns [64g, 64g+64) of an accumulator and owns a selector; its
+//                first 4 warps score the even tiles, the other 4 the odd tiles, in parallel
 // Units (two consecutive query rows x one key range) are visited longest first and
 // spread round-robin over the CTAs.  Decode-sized requests split each row's keys into
 // chunks; chunk candidate lists are merged by the CUDA-core merge kernel.
@@ -34,11 +35,12 @@ namespace {
 constexpr int kRowsPerUnit = 2;
 constexpr int kTileKeys = 128;  // MMA M
 constexpr int kN = 64 * kRowsPerUnit;  // MMA N
-constexpr int kEpiWarps = 4 * kRowsPerUnit;
+constexpr int kAccBufs = 4;  // TMEM accumulators: the MMA runs up to 4 tiles ahead
+constexpr int kEpiWarps = 8 * kRowsPerUnit;  // per row: 4 warps for even, 4 for odd tiles
 constexpr int kThreads = 64 + 32 * kEpiWarps;
-constexpr int kGroupThreads = 128;
+constexpr int kGroupThreads = 256;
 constexpr int kCap = 4096;
-constexpr int kTmemCols = 2 * kN;  // two accumulators
+constexpr int kTmemCols = kAccBufs * kN;
 constexpr int kChunkBytes = 128 * 128;  // one 128-row x 128-byte swizzled tile
 
 template <int QK>
@@ -106,6 +108,50 @@ constexpr int smem_bytes() {
            2 * 64 * 4 + 256;
 }
 
+// Score of this thread's key (TMEM lane) for query row g of the unit, from accumulator
+// buffer acc_it % 4: sum over the 64 heads of w[h] * max(0, q[h].k), in packed fp32 pairs.
+__device__ __forceinline__ float tile_score(uint32_t tmem, int quad, int g, int acc_it,
+                                            uint64_t* tfull, uint64_t* tempty, const float* wg,
+                                            volatile int* abort, unsigned* err) {
+    const int a = acc_it & (kAccBufs - 1);
+    tc::mbar_wait(&tfull[a], (acc_it / kAccBufs) & 1, abort, err);
+    tc::tc_fence_after();
+    uint32_t r[64];
+    const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + a * kN + g * 64;
+    TSI_TMEM_LD32(taddr, r);
+    TSI_TMEM_LD32(taddr + 32, (r + 32));
+    tc::tmem_wait_ld();
+    tc::tc_fence_before();
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) tc::mbar_arrive(&tempty[a]);
+    float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                     make_float2(0.f, 0.f)};
+    const float4* w4 = reinterpret_cast<const float4*>(wg);
+#pragma unroll
+    for (int h = 0; h < 64; h += 8) {
+        const float4 wa = w4[h >> 2];
+        const float4 wb = w4[(h >> 2) + 1];
+        acc[0] = __ffma2_rn(make_float2(wa.x, wa.y),
+                            make_float2(fmaxf(__uint_as_float(r[h + 0]), 0.f),
+                                        fmaxf(__uint_as_float(r[h + 1]), 0.f)),
+                            acc[0]);
+        acc[1] = __ffma2_rn(make_float2(wa.z, wa.w),
+                            make_float2(fmaxf(__uint_as_float(r[h + 2]), 0.f),
+                                        fmaxf(__uint_as_float(r[h + 3]), 0.f)),
+                            acc[1]);
+        acc[2] = __ffma2_rn(make_float2(wb.x, wb.y),
+                            make_float2(fmaxf(__uint_as_float(r[h + 4]), 0.f),
+                                        fmaxf(__uint_as_float(r[h + 5]), 0.f)),
+                            acc[2]);
+        acc[3] = __ffma2_rn(make_float2(wb.z, wb.w),
+                            make_float2(fmaxf(__uint_as_float(r[h + 6]), 0.f),
+                                        fmaxf(__uint_as_float(r[h + 7]), 0.f)),
+                            acc[3]);
+    }
+    return ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) +
+           ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
+}
+
 template <int QK>
 __global__ void __launch_bounds__(kThreads, 1)
     tsi_indexer_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
@@ -124,8 +170,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* full = bars;
     uint64_t* empty = full + C::kStages;
     uint64_t* tfull = empty + C::kStages;
-    uint64_t* tempty = tfull + 2;
-    uint64_t* qfull = tempty + 2;
+    uint64_t* tempty = tfull + kAccBufs;
+    uint64_t* qfull = tempty + kAccBufs;
     uint64_t* qempty = qfull + 1;
     uint64_t* done = qempty + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
@@ -139,9 +185,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::mbar_init(&full[s], 1);
             tc::mbar_init(&empty[s], 1);
         }
-        for (int a = 0; a < 2; ++a) {
+        for (int a = 0; a < kAccBufs; ++a) {
             tc::mbar_init(&tfull[a], 1);
-            tc::mbar_init(&tempty[a], kEpiWarps);
+            tc::mbar_init(&tempty[a], kEpiWarps / 2);  // the 4 warps of each row reading it
         }
         tc::mbar_init(qfull, 1);
         tc::mbar_init(qempty, 1);
@@ -196,9 +242,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc::mbar_wait(qfull, unit_it & 1, abort, p.err);
                 for (int i = 0; i < U.ntiles; ++i, ++it, ++acc_it) {
                     const int s = it % C::kStages;
-                    const int a = acc_it & 1;
+                    const int a = acc_it & (kAccBufs - 1);
                     tc::mbar_wait(&full[s], (it / C::kStages) & 1, abort, p.err);
-                    tc::mbar_wait(&tempty[a], ((acc_it >> 1) & 1) ^ 1, abort, p.err);
+                    tc::mbar_wait(&tempty[a], ((acc_it / kAccBufs) & 1) ^ 1, abort, p.err);
                     tc::tc_fence_after();
                     if (!*abort) {
                         const uint32_t d = tmem + a * kN;
@@ -230,13 +276,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ------------------------------------------------------------ epilogue groups
         const int ew = warp - 2;
-        const int g = ew >> 2;  // query row of the unit handled by this group
+        const int g = ew >> 3;  // query row of the unit handled by this group
+        const int sub = (ew >> 2) & 1;  // this warp scores the unit's tiles i with i % 2 == sub
         const int quad = warp & 3;  // TMEM lanes [32*quad, 32*quad+32) this warp may read
-        const int gtid = (ew & 3) * 32 + lane;
+        const int gtid = (ew & 7) * 32 + lane;
         TopKSelector<kGroupThreads, kCap> sel;
         sel.bind(sel_mem + g * kSelBytes, gtid, 1 + g, p.err);
         float* wg = w_s + g * 64;
-        int acc_it = 0;
+        int acc_base = 0;  // accumulator counter of the unit's first tile
         for (int u = blockIdx.x; u < p.n_units; u += gridDim.x) {
             const Unit U = unit_of(p, u);
             const int t = g == 0 ? U.t_lo : U.t_hi;
@@ -249,33 +296,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (gtid < 64) wg[gtid] = load_elem(p.w, wrow + gtid, p.w_dtype);
             }
             sel.reset();
-            for (int i = 0; i < U.ntiles; ++i, ++acc_it) {
-                const int a = acc_it & 1;
-                tc::mbar_wait(&tfull[a], (acc_it >> 1) & 1, abort, p.err);
-                tc::tc_fence_after();
-                uint32_t r[64];
-                const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + a * kN + g * 64;
-                TSI_TMEM_LD32(taddr, r);
-                TSI_TMEM_LD32(taddr + 32, (r + 32));
-                tc::tmem_wait_ld();
-                tc::tc_fence_before();
-                __syncwarp();
-                if (lane == 0) tc::mbar_arrive(&tempty[a]);
-                float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
-                const float4* w4 = reinterpret_cast<const float4*>(wg);
-#pragma unroll
-                for (int h = 0; h < 64; h += 4) {
-                    const float4 wv = w4[h >> 2];
-                    acc0 = fmaf(wv.x, fmaxf(__uint_as_float(r[h + 0]), 0.f), acc0);
-                    acc1 = fmaf(wv.y, fmaxf(__uint_as_float(r[h + 1]), 0.f), acc1);
-                    acc2 = fmaf(wv.z, fmaxf(__uint_as_float(r[h + 2]), 0.f), acc2);
-                    acc3 = fmaf(wv.w, fmaxf(__uint_as_float(r[h + 3]), 0.f), acc3);
-                }
-                const float score = (acc0 + acc1) + (acc2 + acc3);
-                const int64_t s = U.key_lo + static_cast<int64_t>(i) * kTileKeys + quad * 32 + lane;
-                sel.make_room(p.topk);
-                sel.offer(row_ok && s < limit, make_key(score, static_cast<uint32_t>(s)));
+            // per round the two halves of the group score tiles i0 and i0 + 1 side by side,
+            // then offer together (one room check for 256 keys)
+            for (int i0 = 0; i0 < U.ntiles; i0 += 2) {
+                const int i = i0 + sub;
+                const bool has = i < U.ntiles;
+                const float sc =
+                    has ? tile_score(tmem, quad, g, acc_base + i, tfull, tempty, wg, abort, p.err) : 0.f;
+                const int64_t key = U.key_lo + static_cast<int64_t>(i) * kTileKeys + quad * 32 + lane;
+                const uint64_t thr = sel.make_room(p.topk);
+                sel.offer_thr(has && row_ok && key < limit, make_key(sc, static_cast<uint32_t>(key)), thr);
             }
+            acc_base += U.ntiles;
             if (row_ok) {
                 const int64_t row = static_cast<int64_t>(U.b) * p.T + t;
                 if (p.n_chunks == 1) {

@@ -120,10 +120,32 @@ struct TopKSelector {
         return n;
     }
 
-    // Collective: ensure room for one more round of NT offers.
-    __device__ __forceinline__ void make_room(int k) {
+    // Collective: ensure room for `rounds` more rounds of NT offers.  Returns the admission
+    // threshold to offer against until the next make_room (the same in every thread).
+    __device__ __forceinline__ uint64_t make_room(int k, int rounds = 1) {
         const int n = settled_count();
-        if (n > CAP - NT) compact(k, n);
+        if (n > CAP - rounds * NT) compact(k, n);
+        return *reinterpret_cast<volatile uint64_t*>(thr);
+    }
+
+    // Collective: offer against a threshold returned by make_room.
+    __device__ __forceinline__ void offer_thr(bool has, uint64_t key, uint64_t threshold) {
+        const int lane = threadIdx.x & 31;
+        const bool take = has && key >= threshold;
+        const unsigned m = __ballot_sync(kFull, take);
+        if (m) {
+            const int leader = __ffs(m) - 1;
+            int base = 0;
+            if (lane == leader) base = atomicAdd(&ctl[0], __popc(m));
+            base = __shfl_sync(kFull, base, leader);
+            const int pos = base + __popc(m & ((1u << lane) - 1u));
+            if (take) {
+                if (pos < CAP)
+                    buf[pos] = key;
+                else
+                    atomicOr(err, kErrAssert);
+            }
+        }
     }
 
     // Collective: keep exactly the k largest of the n held keys (no-op when n <= k).
