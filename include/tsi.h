@@ -57,8 +57,10 @@ typedef enum { TSI_F32 = 0, TSI_BF16 = 1, TSI_E4M3 = 2 } tsi_dtype;
 
 /*
  * Workspace bytes needed by tsi_indexer_topk for these sizes (0 when none is needed).
- * The workspace holds per-split candidate lists when rows are few and key ranges are
- * split across thread blocks (decode).
+ * The workspace holds candidate lists of 8-byte keys, topk per row and key split,
+ * plus a count per list: the tensor-core path always leaves each row's best keys there
+ * unordered for a ranking pass; the CUDA-core path only when rows are few and key
+ * ranges are split across thread blocks (decode).
  */
 size_t tsi_indexer_topk_workspace(int B, int T, int S, int H_I, int d_I, int topk,
                                   int qk_dtype);

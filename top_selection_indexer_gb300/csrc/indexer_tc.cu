@@ -4,23 +4,28 @@
 // each row ("GLM-5.2 技术报告速览", §IndexShare: the score equation, k = 2048; the
 // ReLU form is chosen there for speed and FP8 friendliness).  The L x L score matrix
 // never leaves the chip: each 128-key tile is scored in TMEM and streamed into a
-// shared-memory top-k selector.
+// shared-memory top-k selector per query row.
 //
-// MMA shape: keys on M (128 rows of kI per tile, the A operand), the 64 heads of two
-// query rows on N (the B operand, 128 rows of qI), d_I = 128 on K, fp32 accumulators
-// in TMEM.  A thread of the epilogue owns one key (one TMEM lane) and reduces the 64
-// heads of its query row inside its registers: ReLU, times the gate weight, summed --
-// no cross-thread reduction.
+// MMA shape: keys on M (128 rows of kI per tile, the A operand), the 64 heads of R
+// consecutive query rows on N = 64 R (the B operand), d_I = 128 on K, fp32 accumulators
+// in TMEM.  R = 4 for e4m3 (N = 256) and 2 for bf16 (N = 128, where shared memory holds
+// fewer selectors).  A thread of the epilogue owns one key (one TMEM lane) and reduces
+// the 64 heads of its query row inside its registers: ReLU, times the gate weight,
+// summed -- no cross-thread reduction.  The larger R, the more query rows share each
+// key tile: fewer tiles, fewer MMA issues and barrier round trips, less L2 traffic.
 //
 // Roles of one persistent CTA (576 threads):
 //   warp 0       TMA producer: Q tile of the unit, key tiles into a ring of stages
-//   warp 1       TMEM allocator + single-thread MMA issuer (four TMEM accumulators)
-//   warps 2..17  two epilogue groups of 8 warps (one per query row of the unit); group g
-//                reads columns [64g, 64g+64) of an accumulator and owns a selector; its
-//                first 4 warps score the even tiles, the other 4 the odd tiles, in parallel
-// Units (two consecutive query rows x one key range) are visited longest first and
-// spread round-robin over the CTAs.  Decode-sized requests split each row's keys into
-// chunks; chunk candidate lists are merged by the CUDA-core merge kernel.
+//   warp 1       TMEM allocator + single-thread MMA issuer (512 TMEM columns: 512 / N
+//                accumulators, so the MMA runs that many tiles ahead)
+//   warps 2..17  R epilogue groups of 16 / R warps, one per query row of the unit; group
+//                r reads columns [64r, 64r+64) of an accumulator and owns a selector.
+//                With R = 2 the group's first 4 warps take the even tiles, the other 4
+//                the odd tiles.
+// Units (R consecutive query rows x one key range) are visited longest first and spread
+// round-robin over the CTAs.  Decode-sized requests split each row's keys into chunks.
+// Each row (chunk) leaves its k best keys unordered in the workspace; the CUDA-core merge
+// kernel ranks them (and merges a row's chunks), so no sort stalls the MMA pipeline.
 #include <mutex>
 
 #include <cudaTypedefs.h>
@@ -32,34 +37,52 @@
 namespace tsi {
 namespace {
 
-constexpr int kRowsPerUnit = 2;
 constexpr int kTileKeys = 128;  // MMA M
-constexpr int kN = 64 * kRowsPerUnit;  // MMA N
-constexpr int kAccBufs = 4;  // TMEM accumulators: the MMA runs up to 4 tiles ahead
-constexpr int kEpiWarps = 8 * kRowsPerUnit;  // per row: 4 warps for even, 4 for odd tiles
+constexpr int kEpiWarps = 16;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
-constexpr int kGroupThreads = 256;
-constexpr int kCap = 4096;
-constexpr int kTmemCols = kAccBufs * kN;
+constexpr int kTmemCols = 512;
 constexpr int kChunkBytes = 128 * 128;  // one 128-row x 128-byte swizzled tile
 
 template <int QK>
 struct TileCfg;
 template <>
 struct TileCfg<TSI_E4M3> {
+    static constexpr int kRows = 4;    // query rows per unit
     static constexpr int kChunks = 1;  // 128-byte pieces of a d_I = 128 row
-    static constexpr int kStages = 6;
-    static constexpr uint32_t kIdesc = tc::instr_desc(0, kTileKeys, kN);
+    static constexpr int kStages = 4;
+    static constexpr int kCap = 3584;  // selector capacity per row
+    static constexpr uint32_t kFmt = 0;
     static constexpr int kKSteps = 4;  // K = 32 per MMA
-    static constexpr int kKStepBytes = 32;
 };
 template <>
 struct TileCfg<TSI_BF16> {
+    static constexpr int kRows = 2;
     static constexpr int kChunks = 2;
     static constexpr int kStages = 3;
-    static constexpr uint32_t kIdesc = tc::instr_desc(1, kTileKeys, kN);
+    static constexpr int kCap = 4096;
+    static constexpr uint32_t kFmt = 1;
     static constexpr int kKSteps = 4;  // per chunk, K = 16 per MMA
-    static constexpr int kKStepBytes = 32;
+};
+
+template <int QK>
+struct Lay {
+    using C = TileCfg<QK>;
+    static constexpr int kR = C::kRows;
+    static constexpr int kN = 64 * kR;             // MMA N
+    static constexpr int kAccBufs = kTmemCols / kN;
+    static constexpr int kSubs = 4 / kR;           // warp sets per row sharing out the tiles
+    static constexpr int kGroupThreads = 128 * kSubs;
+    static constexpr int kReaders = 4 * kR;        // warps reading each accumulator
+    static constexpr int kStageBytes = C::kChunks * kChunkBytes;
+    static constexpr int kQChunkBytes = kN * 128;  // kN rows of 128 bytes per K chunk
+    static constexpr int kQBytes = C::kChunks * kQChunkBytes;
+    static constexpr int kSelBytes = (selector_smem_bytes<C::kCap>() + 15) & ~15;
+    static constexpr uint32_t kIdesc = tc::instr_desc(C::kFmt, kTileKeys, kN);
+    static constexpr int kBars = 2 * C::kStages + 2 * kAccBufs + 3;
+    static constexpr int kSmem = 1024 /* alignment slack */ + C::kStages * kStageBytes +
+                                 kQBytes + kR * kSelBytes + kR * 64 * 4 + kBars * 8 + 16;
+    static_assert(kSmem <= 227 * 1024, "shared memory");
+    static_assert(kEpiWarps == 4 * kR * kSubs, "every epilogue warp has a row");
 };
 
 struct TcParams {
@@ -76,21 +99,21 @@ struct TcParams {
 };
 
 struct Unit {
-    int b, t_lo, t_hi, chunk;
+    int b, t_hi, chunk;
     int64_t key_lo, key_hi;
     int ntiles;
 };
 
-// Unit u: pair j = u / (B * n_chunks) counted from the end of the sequence (longest rows
-// first), sequence b, key chunk.  Rows t_lo = t_hi - 1 (may be -1) and t_hi.
+// Unit u: row group j = u / (B * n_chunks) counted from the end of the sequence (longest
+// rows first), sequence b, key chunk.  Rows t_hi - R + 1 .. t_hi (the first may be < 0).
+template <int R>
 __device__ __forceinline__ Unit unit_of(const TcParams& p, int u) {
     Unit U;
     U.chunk = u % p.n_chunks;
     const int pu = u / p.n_chunks;
     const int j = pu / p.B;
     U.b = pu % p.B;
-    U.t_hi = p.T - 1 - 2 * j;
-    U.t_lo = U.t_hi - 1;
+    U.t_hi = p.T - 1 - R * j;
     const int64_t p_hi = query_position(p.kv_len, U.b, p.T, p.S, U.t_hi);
     const int64_t end = p_hi + 1 > 0 ? p_hi + 1 : 0;
     U.key_lo = static_cast<int64_t>(U.chunk) * p.chunk_keys;
@@ -100,53 +123,55 @@ __device__ __forceinline__ Unit unit_of(const TcParams& p, int u) {
     return U;
 }
 
-template <int QK>
-constexpr int smem_bytes() {
-    using C = TileCfg<QK>;
-    return 1024 /* alignment slack */ + C::kStages * C::kChunks * kChunkBytes +
-           C::kChunks * kChunkBytes + 2 * ((selector_smem_bytes<kCap>() + 15) & ~15) +
-           2 * 64 * 4 + 256;
+// Wait for a phase that is usually complete already: one probe, then the bounded wait.
+__device__ __forceinline__ bool wait_fast(uint64_t* bar, uint32_t parity, bool probed,
+                                          volatile int* abort, unsigned* err) {
+    return probed || tc::mbar_wait(bar, parity, abort, err);
 }
 
-// Score of this thread's key (TMEM lane) for query row g of the unit, from accumulator
-// buffer acc_it % 4: sum over the 64 heads of w[h] * max(0, q[h].k), in packed fp32 pairs.
-__device__ __forceinline__ float tile_score(uint32_t tmem, int quad, int g, int acc_it,
-                                            uint64_t* tfull, uint64_t* tempty, const float* wg,
-                                            volatile int* abort, unsigned* err) {
-    const int a = acc_it & (kAccBufs - 1);
-    tc::mbar_wait(&tfull[a], (acc_it / kAccBufs) & 1, abort, err);
+// Score of this thread's key (TMEM lane) for query row r of the unit from accumulator
+// buffer a: sum over the 64 heads of w[h] * max(0, q[h].k), in packed fp32 pairs.  The
+// 64 columns come in two halves (fewer live registers); the buffer is released to the
+// MMA once the second half is in registers.
+template <int N>
+__device__ __forceinline__ float tile_score(uint32_t tmem, int quad, int r, int a, uint64_t* tempty,
+                                            const float* wg) {
     tc::tc_fence_after();
-    uint32_t r[64];
-    const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + a * kN + g * 64;
-    TSI_TMEM_LD32(taddr, r);
-    TSI_TMEM_LD32(taddr + 32, (r + 32));
-    tc::tmem_wait_ld();
-    tc::tc_fence_before();
-    __syncwarp();
-    if ((threadIdx.x & 31) == 0) tc::mbar_arrive(&tempty[a]);
+    const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + a * N + r * 64;
     float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                      make_float2(0.f, 0.f)};
     const float4* w4 = reinterpret_cast<const float4*>(wg);
 #pragma unroll
-    for (int h = 0; h < 64; h += 8) {
-        const float4 wa = w4[h >> 2];
-        const float4 wb = w4[(h >> 2) + 1];
-        acc[0] = __ffma2_rn(make_float2(wa.x, wa.y),
-                            make_float2(fmaxf(__uint_as_float(r[h + 0]), 0.f),
-                                        fmaxf(__uint_as_float(r[h + 1]), 0.f)),
-                            acc[0]);
-        acc[1] = __ffma2_rn(make_float2(wa.z, wa.w),
-                            make_float2(fmaxf(__uint_as_float(r[h + 2]), 0.f),
-                                        fmaxf(__uint_as_float(r[h + 3]), 0.f)),
-                            acc[1]);
-        acc[2] = __ffma2_rn(make_float2(wb.x, wb.y),
-                            make_float2(fmaxf(__uint_as_float(r[h + 4]), 0.f),
-                                        fmaxf(__uint_as_float(r[h + 5]), 0.f)),
-                            acc[2]);
-        acc[3] = __ffma2_rn(make_float2(wb.z, wb.w),
-                            make_float2(fmaxf(__uint_as_float(r[h + 6]), 0.f),
-                                        fmaxf(__uint_as_float(r[h + 7]), 0.f)),
-                            acc[3]);
+    for (int half = 0; half < 2; ++half) {
+        uint32_t v[32];
+        TSI_TMEM_LD32(taddr + half * 32, v);
+        tc::tmem_wait_ld();
+        if (half == 1) {
+            tc::tc_fence_before();
+            __syncwarp();
+            if ((threadIdx.x & 31) == 0) tc::mbar_arrive(&tempty[a]);
+        }
+#pragma unroll
+        for (int h = 0; h < 32; h += 8) {
+            const float4 wa = w4[(half * 32 + h) >> 2];
+            const float4 wb = w4[((half * 32 + h) >> 2) + 1];
+            acc[0] = __ffma2_rn(make_float2(wa.x, wa.y),
+                                make_float2(fmaxf(__uint_as_float(v[h + 0]), 0.f),
+                                            fmaxf(__uint_as_float(v[h + 1]), 0.f)),
+                                acc[0]);
+            acc[1] = __ffma2_rn(make_float2(wa.z, wa.w),
+                                make_float2(fmaxf(__uint_as_float(v[h + 2]), 0.f),
+                                            fmaxf(__uint_as_float(v[h + 3]), 0.f)),
+                                acc[1]);
+            acc[2] = __ffma2_rn(make_float2(wb.x, wb.y),
+                                make_float2(fmaxf(__uint_as_float(v[h + 4]), 0.f),
+                                            fmaxf(__uint_as_float(v[h + 5]), 0.f)),
+                                acc[2]);
+            acc[3] = __ffma2_rn(make_float2(wb.z, wb.w),
+                                make_float2(fmaxf(__uint_as_float(v[h + 6]), 0.f),
+                                            fmaxf(__uint_as_float(v[h + 7]), 0.f)),
+                                acc[3]);
+        }
     }
     return ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) +
            ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
@@ -157,21 +182,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     tsi_indexer_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                           const __grid_constant__ CUtensorMap tmap_q, const TcParams p) {
     using C = TileCfg<QK>;
-    constexpr int kStageBytes = C::kChunks * kChunkBytes;
+    using L = Lay<QK>;
+    constexpr int R = L::kR;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t* stages = base;
-    uint8_t* qbuf = stages + C::kStages * kStageBytes;
-    uint8_t* sel_mem = qbuf + kStageBytes;
-    constexpr int kSelBytes = (selector_smem_bytes<kCap>() + 15) & ~15;
-    float* w_s = reinterpret_cast<float*>(sel_mem + 2 * kSelBytes);  // [2][64]
-    uint64_t* bars = reinterpret_cast<uint64_t*>(w_s + 2 * 64);
+    uint8_t* qbuf = stages + C::kStages * L::kStageBytes;
+    uint8_t* sel_mem = qbuf + L::kQBytes;
+    float* w_s = reinterpret_cast<float*>(sel_mem + R * L::kSelBytes);  // [R][64]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(w_s + R * 64);
     uint64_t* full = bars;
     uint64_t* empty = full + C::kStages;
     uint64_t* tfull = empty + C::kStages;
-    uint64_t* tempty = tfull + kAccBufs;
-    uint64_t* qfull = tempty + kAccBufs;
+    uint64_t* tempty = tfull + L::kAccBufs;
+    uint64_t* qfull = tempty + L::kAccBufs;
     uint64_t* qempty = qfull + 1;
     uint64_t* done = qempty + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
@@ -185,9 +210,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::mbar_init(&full[s], 1);
             tc::mbar_init(&empty[s], 1);
         }
-        for (int a = 0; a < kAccBufs; ++a) {
+        for (int a = 0; a < L::kAccBufs; ++a) {
             tc::mbar_init(&tfull[a], 1);
-            tc::mbar_init(&tempty[a], kEpiWarps / 2);  // the 4 warps of each row reading it
+            tc::mbar_init(&tempty[a], L::kReaders);
         }
         tc::mbar_init(qfull, 1);
         tc::mbar_init(qempty, 1);
@@ -208,64 +233,83 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
-            int it = 0, unit_it = 0;
+            int s = 0;
+            uint32_t ph = 0;  // phase of the ring slot s
+            int unit_it = 0;
             for (int u = blockIdx.x; u < p.n_units; u += gridDim.x, ++unit_it) {
-                const Unit U = unit_of(p, u);
+                const Unit U = unit_of<R>(p, u);
                 tc::mbar_wait(qempty, (unit_it & 1) ^ 1, abort, p.err);
                 if (!*abort) {
-                    tc::mbar_expect_tx(qfull, kStageBytes);
-                    const int qrow = (U.b * p.T + U.t_lo) * 64;
+                    tc::mbar_expect_tx(qfull, L::kQBytes);
+                    const int qrow = (U.b * p.T + U.t_hi - (R - 1)) * 64;
                     for (int c = 0; c < C::kChunks; ++c)
-                        tc::tma_load_2d(qbuf + c * kChunkBytes, &tmap_q, c * 64, qrow, qfull);
+                        for (int h = 0; h < L::kN; h += 128)
+                            tc::tma_load_2d(qbuf + c * L::kQChunkBytes + h * 128, &tmap_q, c * 64,
+                                            qrow + h, qfull);
                 }
-                for (int i = 0; i < U.ntiles; ++i, ++it) {
-                    const int s = it % C::kStages;
-                    tc::mbar_wait(&empty[s], ((it / C::kStages) & 1) ^ 1, abort, p.err);
-                    if (*abort) continue;
-                    tc::mbar_expect_tx(&full[s], kStageBytes);
-                    const int krow = static_cast<int>(static_cast<int64_t>(U.b) * p.S + U.key_lo +
-                                                      static_cast<int64_t>(i) * kTileKeys);
-                    for (int c = 0; c < C::kChunks; ++c)
-                        tc::tma_load_2d(stages + s * kStageBytes + c * kChunkBytes, &tmap_k,
-                                        c * 64, krow, &full[s]);
+                for (int i = 0; i < U.ntiles; ++i) {
+                    const bool ready = tc::mbar_try_wait(&empty[s], ph ^ 1);
+                    if (wait_fast(&empty[s], ph ^ 1, ready, abort, p.err) && !*abort) {
+                        tc::mbar_expect_tx(&full[s], L::kStageBytes);
+                        const int krow = static_cast<int>(static_cast<int64_t>(U.b) * p.S + U.key_lo +
+                                                          static_cast<int64_t>(i) * kTileKeys);
+                        for (int c = 0; c < C::kChunks; ++c)
+                            tc::tma_load_2d(stages + s * L::kStageBytes + c * kChunkBytes, &tmap_k,
+                                            c * 64, krow, &full[s]);
+                    }
+                    if (++s == C::kStages) {
+                        s = 0;
+                        ph ^= 1;
+                    }
                 }
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            int it = 0, acc_it = 0, unit_it = 0;
-            const uint32_t q_addr = tc::smem_addr(qbuf);
-            const uint32_t st_addr = tc::smem_addr(stages);
+            int s = 0, a = 0;
+            uint32_t ph = 0, aph = 0;  // phases of ring slot s and accumulator a
+            int unit_it = 0;
+            const uint64_t adesc = tc::smem_desc(tc::smem_addr(stages), 16, 1024);
+            const uint64_t bdesc = tc::smem_desc(tc::smem_addr(qbuf), 16, 1024);
             for (int u = blockIdx.x; u < p.n_units; u += gridDim.x, ++unit_it) {
-                const Unit U = unit_of(p, u);
+                const Unit U = unit_of<R>(p, u);
                 tc::mbar_wait(qfull, unit_it & 1, abort, p.err);
-                for (int i = 0; i < U.ntiles; ++i, ++it, ++acc_it) {
-                    const int s = it % C::kStages;
-                    const int a = acc_it & (kAccBufs - 1);
-                    tc::mbar_wait(&full[s], (it / C::kStages) & 1, abort, p.err);
-                    tc::mbar_wait(&tempty[a], ((acc_it / kAccBufs) & 1) ^ 1, abort, p.err);
+                for (int i = 0; i < U.ntiles; ++i) {
+                    // probe both barriers back to back so their latencies overlap
+                    const bool f_ok = tc::mbar_try_wait(&full[s], ph);
+                    const bool e_ok = tc::mbar_try_wait(&tempty[a], aph ^ 1);
+                    const bool go = wait_fast(&full[s], ph, f_ok, abort, p.err) &&
+                                    wait_fast(&tempty[a], aph ^ 1, e_ok, abort, p.err);
                     tc::tc_fence_after();
-                    if (!*abort) {
-                        const uint32_t d = tmem + a * kN;
-                        const uint32_t a0 = st_addr + s * kStageBytes;
+                    if (go) {
+                        const uint32_t d = tmem + a * L::kN;
+                        const uint64_t a0 = adesc + ((s * L::kStageBytes) >> 4);
 #pragma unroll
                         for (int c = 0; c < C::kChunks; ++c) {
 #pragma unroll
                             for (int k = 0; k < C::kKSteps; ++k) {
-                                const uint32_t off = c * kChunkBytes + k * C::kKStepBytes;
-                                const uint64_t da = tc::smem_desc(a0 + off, 16, 1024);
-                                const uint64_t db = tc::smem_desc(q_addr + off, 16, 1024);
-                                const uint32_t acc = (c | k) ? 1u : 0u;
+                                // descriptors address 16-byte units: offsets add directly
+                                const uint64_t da = a0 + ((c * kChunkBytes + k * 32) >> 4);
+                                const uint64_t db = bdesc + ((c * L::kQChunkBytes + k * 32) >> 4);
+                                const uint32_t accum = (c | k) ? 1u : 0u;
                                 if (QK == TSI_E4M3)
-                                    tc::mma_f8(d, da, db, C::kIdesc, acc);
+                                    tc::mma_f8(d, da, db, L::kIdesc, accum);
                                 else
-                                    tc::mma_bf16(d, da, db, C::kIdesc, acc);
+                                    tc::mma_bf16(d, da, db, L::kIdesc, accum);
                             }
                         }
                     }
                     tc::mma_commit(&empty[s]);
                     tc::mma_commit(&tfull[a]);
+                    if (++s == C::kStages) {
+                        s = 0;
+                        ph ^= 1;
+                    }
+                    if (++a == L::kAccBufs) {
+                        a = 0;
+                        aph ^= 1;
+                    }
                 }
                 tc::mma_commit(qempty);
             }
@@ -276,17 +320,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ------------------------------------------------------------ epilogue groups
         const int ew = warp - 2;
-        const int g = ew >> 3;  // query row of the unit handled by this group
-        const int sub = (ew >> 2) & 1;  // this warp scores the unit's tiles i with i % 2 == sub
+        const int r = ew / (4 * L::kSubs);  // query row of the unit handled by this group
+        const int sub = (ew >> 2) % L::kSubs;  // this warp scores tiles i with i % kSubs == sub
         const int quad = warp & 3;  // TMEM lanes [32*quad, 32*quad+32) this warp may read
-        const int gtid = (ew & 7) * 32 + lane;
-        TopKSelector<kGroupThreads, kCap> sel;
-        sel.bind(sel_mem + g * kSelBytes, gtid, 1 + g, p.err);
-        float* wg = w_s + g * 64;
+        const int gtid = (ew % (4 * L::kSubs)) * 32 + lane;
+        TopKSelector<L::kGroupThreads, C::kCap> sel;
+        sel.bind(sel_mem + r * L::kSelBytes, gtid, 1 + r, p.err);
+        float* wg = w_s + r * 64;
         int acc_base = 0;  // accumulator counter of the unit's first tile
         for (int u = blockIdx.x; u < p.n_units; u += gridDim.x) {
-            const Unit U = unit_of(p, u);
-            const int t = g == 0 ? U.t_lo : U.t_hi;
+            const Unit U = unit_of<R>(p, u);
+            const int t = U.t_hi - (R - 1) + r;
             const bool row_ok = t >= 0;
             int64_t limit = 0;  // keys s < limit belong to this row
             if (row_ok) {
@@ -296,27 +340,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (gtid < 64) wg[gtid] = load_elem(p.w, wrow + gtid, p.w_dtype);
             }
             sel.reset();
-            // per round the two halves of the group score tiles i0 and i0 + 1 side by side,
-            // then offer together (one room check for 256 keys)
-            for (int i0 = 0; i0 < U.ntiles; i0 += 2) {
-                const int i = i0 + sub;
-                const bool has = i < U.ntiles;
-                const float sc =
-                    has ? tile_score(tmem, quad, g, acc_base + i, tfull, tempty, wg, abort, p.err) : 0.f;
-                const int64_t key = U.key_lo + static_cast<int64_t>(i) * kTileKeys + quad * 32 + lane;
-                const uint64_t thr = sel.make_room(p.topk);
-                sel.offer_thr(has && row_ok && key < limit, make_key(sc, static_cast<uint32_t>(key)), thr);
+            // per round each warp scores two of its tiles, then one room check covers the
+            // group's offers of both
+            for (int i0 = 0; i0 < U.ntiles; i0 += 2 * L::kSubs) {
+                float sc[2];
+                int64_t key[2];
+                bool has[2];
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int i = i0 + j * L::kSubs + sub;
+                    has[j] = i < U.ntiles;
+                    key[j] = U.key_lo + static_cast<int64_t>(i) * kTileKeys + quad * 32 + lane;
+                    sc[j] = 0.f;
+                    if (has[j]) {
+                        const int acc = acc_base + i;
+                        const int a = acc % L::kAccBufs;
+                        tc::mbar_wait(&tfull[a], (acc / L::kAccBufs) & 1, abort, p.err);
+                        sc[j] = tile_score<L::kN>(tmem, quad, r, a, tempty, wg);
+                    }
+                }
+                const uint64_t thr = sel.make_room(p.topk, 2);
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+                    sel.offer_thr(has[j] && row_ok && key[j] < limit,
+                                  make_key(sc[j], static_cast<uint32_t>(key[j])), thr);
             }
             acc_base += U.ntiles;
             if (row_ok) {
+                // the row's (chunk's) k best keys, unordered; the merge kernel ranks them
                 const int64_t row = static_cast<int64_t>(U.b) * p.T + t;
-                if (p.n_chunks == 1) {
-                    sel.finalize(p.topk, p.idx + row * p.topk,
-                                 p.score ? p.score + row * p.topk : nullptr);
-                } else {
-                    const int64_t slot = row * p.n_chunks + U.chunk;
-                    sel.dump(p.topk, p.cand + slot * p.topk, p.cand_cnt + slot);
-                }
+                const int64_t slot = row * p.n_chunks + U.chunk;
+                sel.dump(p.topk, p.cand + slot * p.topk, p.cand_cnt + slot);
             }
         }
     }
@@ -362,12 +416,16 @@ bool encode_rows128(CUtensorMap* map, const void* ptr, int64_t rows, int qk_dtyp
 
 constexpr int kPlanSMs = 152;
 
-void tc_plan(int B, int T, int S, int* n_chunks, int* chunk_keys) {
-    const int64_t pairs = static_cast<int64_t>(B) * ((T + 1) / 2);
+int rows_per_unit(int qk_dtype) { return qk_dtype == TSI_E4M3 ? 4 : 2; }
+
+// Key chunks per row for decode-sized requests (too few units to fill the GPU).
+void tc_plan(int qk_dtype, int B, int T, int S, int* n_chunks, int* chunk_keys) {
+    const int R = rows_per_unit(qk_dtype);
+    const int64_t groups = static_cast<int64_t>(B) * ((T + R - 1) / R);
     int nc = 1;
-    if (pairs < kPlanSMs && S > 4096) {
+    if (groups < kPlanSMs && S > 4096) {
         const int by_keys = (S + 2047) / 2048;
-        const int by_sm = static_cast<int>((kPlanSMs + pairs - 1) / pairs);
+        const int by_sm = static_cast<int>((kPlanSMs + groups - 1) / groups);
         nc = by_keys < by_sm ? by_keys : by_sm;
         if (nc < 1) nc = 1;
     }
@@ -407,15 +465,14 @@ cudaError_t launch_qk(const IndexerArgs& a, void* workspace, cudaStream_t st) {
     p.idx = a.idx;
     p.score = a.score;
     p.err = a.err;
-    tc_plan(a.B, a.T, a.S, &p.n_chunks, &p.chunk_keys);
-    const int64_t pairs = static_cast<int64_t>(a.B) * ((a.T + 1) / 2);
-    p.n_units = static_cast<int>(pairs * p.n_chunks);
+    tc_plan(QK, a.B, a.T, a.S, &p.n_chunks, &p.chunk_keys);
+    constexpr int R = Lay<QK>::kR;
+    const int64_t groups = static_cast<int64_t>(a.B) * ((a.T + R - 1) / R);
+    p.n_units = static_cast<int>(groups * p.n_chunks);
     const int rows = a.B * a.T;
-    if (p.n_chunks > 1) {
-        p.cand = static_cast<uint64_t*>(workspace);
-        p.cand_cnt = reinterpret_cast<int*>(p.cand + static_cast<size_t>(rows) * p.n_chunks * a.topk);
-    }
-    constexpr int smem = smem_bytes<QK>();
+    p.cand = static_cast<uint64_t*>(workspace);
+    p.cand_cnt = reinterpret_cast<int*>(p.cand + static_cast<size_t>(rows) * p.n_chunks * a.topk);
+    constexpr int smem = Lay<QK>::kSmem;
     cudaError_t e = cudaFuncSetAttribute(tsi_indexer_tc_kernel<QK>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
@@ -423,7 +480,7 @@ cudaError_t launch_qk(const IndexerArgs& a, void* workspace, cudaStream_t st) {
     tsi_indexer_tc_kernel<QK><<<grid, kThreads, smem, st>>>(tk, tq, p);
     note_launches(1);
     e = cudaGetLastError();
-    if (e != cudaSuccess || p.n_chunks == 1) return e;
+    if (e != cudaSuccess) return e;
     return launch_topk_merge(rows, a.topk, p.n_chunks, p.cand, p.cand_cnt, a.idx, a.score, a.err,
                              st);
 }
@@ -434,10 +491,9 @@ bool tc_indexer_supported(int qk_dtype, int H_I, int d_I) {
     return (qk_dtype == TSI_BF16 || qk_dtype == TSI_E4M3) && H_I == 64 && d_I == 128;
 }
 
-size_t tc_indexer_workspace_bytes(int B, int T, int S, int topk) {
+size_t tc_indexer_workspace_bytes(int qk_dtype, int B, int T, int S, int topk) {
     int nc, ck;
-    tc_plan(B, T, S, &nc, &ck);
-    if (nc <= 1) return 0;
+    tc_plan(qk_dtype, B, T, S, &nc, &ck);
     const size_t slots = static_cast<size_t>(B) * T * nc;
     return slots * topk * sizeof(uint64_t) + ((slots * sizeof(int) + 255) & ~size_t(255));
 }

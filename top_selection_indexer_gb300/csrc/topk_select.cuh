@@ -45,19 +45,20 @@ __device__ __forceinline__ float key_score(uint64_t key) {
 // Shared-memory footprint of one selector (bytes), excluding alignment slack.
 template <int CAP>
 constexpr int selector_smem_bytes() {
-    return CAP * 8 + 256 * 4 + 8 * 4 + 8;
+    return CAP * 8 + 256 * 4 + 8 * 4 + 8 + 16;
 }
 
 template <int NT, int CAP>
 struct TopKSelector {
     static_assert(NT % 32 == 0, "whole warps");
     static_assert(CAP % NT == 0, "CAP must be a multiple of NT");
-    static_assert(CAP >= 2 * TSI_MAX_TOPK, "room for k keys plus one round");
+    static_assert(CAP >= TSI_MAX_TOPK + 2 * NT, "room for k keys plus two rounds");
 
     uint64_t* buf;   // [CAP]
     unsigned* hist;  // [256]
     int* ctl;        // [8]: 0 count, 1 digit, 2 above, 3 in-bin, 4 write cursor
     uint64_t* thr;   // admission threshold
+    uint64_t* rng;   // [2]: smallest and largest held key during a compaction
     int tid;         // 0..NT-1 within the group
     int bar_id;      // named barrier of the group
     unsigned* err;   // device error word: consistency checks record kErrAssert here
@@ -69,6 +70,7 @@ struct TopKSelector {
         hist = reinterpret_cast<unsigned*>(smem + CAP * 8);
         ctl = reinterpret_cast<int*>(smem + CAP * 8 + 256 * 4);
         thr = reinterpret_cast<uint64_t*>(smem + CAP * 8 + 256 * 4 + 8 * 4);
+        rng = thr + 1;
         tid = tid_;
         bar_id = bar_id_;
         return selector_smem_bytes<CAP>();
@@ -124,7 +126,7 @@ struct TopKSelector {
     // threshold to offer against until the next make_room (the same in every thread).
     __device__ __forceinline__ uint64_t make_room(int k, int rounds = 1) {
         const int n = settled_count();
-        if (n > CAP - rounds * NT) compact(k, n);
+        if (n > CAP - rounds * NT) compact(k, n, false, (CAP - rounds * NT - k) / 4);
         return *reinterpret_cast<volatile uint64_t*>(thr);
     }
 
@@ -148,23 +150,69 @@ struct TopKSelector {
         }
     }
 
-    // Collective: keep exactly the k largest of the n held keys (no-op when n <= k).
+    // Collective: drop held keys that cannot be among the k largest (no-op when n <= k).
     // `n` must be a settled_count() result (the same value in every thread).
-    __device__ void compact(int k, int n) {
+    //
+    // An MSD radix select over the 64-bit keys.  The bits above the highest bit in which
+    // the smallest and the largest held key differ are common to all keys and skipped;
+    // then one digit of up to 8 bits per pass narrows down the bin holding the k-th
+    // largest key.  exact: refine until exactly k keys are kept.  Otherwise stop at the
+    // first digit whose bin keeps at most k + slack keys: every key dropped is below the
+    // k-th largest, so nothing of the final top k is lost.  The admission threshold rises
+    // to the kept bin's lower edge.
+    __device__ void compact(int k, int n, bool exact = true, int slack = 0) {
         if (n <= k) return;
-        uint64_t prefix = 0ull;
+        // smallest and largest held key
+        uint64_t lo = ~0ull, hi = 0ull;
+        for (int i = tid; i < n; i += NT) {
+            const uint64_t x = buf[i];
+            lo = x < lo ? x : lo;
+            hi = x > hi ? x : hi;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const uint64_t l2 = __shfl_xor_sync(kFull, lo, o);
+            const uint64_t h2 = __shfl_xor_sync(kFull, hi, o);
+            lo = l2 < lo ? l2 : lo;
+            hi = h2 > hi ? h2 : hi;
+        }
+        if (tid == 0) {
+            rng[0] = ~0ull;
+            rng[1] = 0ull;
+        }
+        sync();
+        if ((threadIdx.x & 31) == 0) {
+            atomicMin(reinterpret_cast<unsigned long long*>(&rng[0]),
+                      static_cast<unsigned long long>(lo));
+            atomicMax(reinterpret_cast<unsigned long long*>(&rng[1]),
+                      static_cast<unsigned long long>(hi));
+        }
+        sync();
+        lo = rng[0];
+        hi = rng[1];
+        if (lo == hi) {  // keys are distinct, so n >= 2 keys cannot all be equal
+            if (tid == 0) atomicOr(err, kErrAssert);
+            return;
+        }
+        const int top = 63 - __clzll(static_cast<long long>(lo ^ hi));
+        uint64_t prefix = top == 63 ? 0ull : (hi & ~((2ull << top) - 1ull));
+        int width = top + 1 < 8 ? top + 1 : 8;
+        int shift = top + 1 - width;
         int need = k;
-        for (int shift = 56; shift >= 0; shift -= 8) {
-            const uint64_t mask = (shift == 56) ? 0ull : (~0ull << (shift + 8));
+        int inbin = 0;
+        while (true) {
+            const int end = shift + width;
+            const uint64_t hmask = end >= 64 ? 0ull : ~((1ull << end) - 1ull);
+            const unsigned dmask = (1u << width) - 1u;
             for (int i = tid; i < 256; i += NT) hist[i] = 0u;
             sync();
             // every thread has read the previous pass's ctl[1..3] before the barrier above
             if (tid == 0) ctl[1] = -1;
-            for (int base = 0; base < n; base += NT) {
-                const int i = base + tid;
+            for (int b = 0; b < n; b += NT) {
+                const int i = b + tid;
                 const uint64_t x = i < n ? buf[i] : 0ull;
-                const bool in = (i < n) && ((x & mask) == prefix);
-                const unsigned d = in ? static_cast<unsigned>((x >> shift) & 255u) : 256u;
+                const bool in = (i < n) && ((x & hmask) == prefix);
+                const unsigned d = in ? static_cast<unsigned>(x >> shift) & dmask : 256u;
                 const unsigned peers = __match_any_sync(kFull, d);
                 if (in && (threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[d], __popc(peers));
             }
@@ -203,41 +251,48 @@ struct TopKSelector {
             const int d = ctl[1];
             if (d < 0) {  // no bin holds the k-th key: counts are inconsistent
                 if (tid == 0) atomicOr(err, kErrAssert);
-                break;
+                return;
             }
-            const int above = ctl[2];
-            const int inbin = ctl[3];
             prefix |= static_cast<uint64_t>(d) << shift;
-            need -= above;
-            if (inbin == need) break;  // the whole bin is in: keys >= prefix are exactly k
+            need -= ctl[2];
+            inbin = ctl[3];
+            // keys >= prefix: the k - need above the bin plus the whole bin
+            if (inbin == need || shift == 0 || (!exact && k - need + inbin <= k + slack)) break;
+            width = shift < 8 ? shift : 8;
+            shift -= width;
         }
-        // keep keys >= prefix (exactly k of them), compacted to the front
-        constexpr int PER = CAP / NT;
-        uint64_t v[PER];
-#pragma unroll
-        for (int j = 0; j < PER; ++j) {
-            const int i = tid + j * NT;
-            v[j] = i < n ? buf[i] : 0ull;
-        }
+        const int kept = k - need + inbin;
+        // keep keys >= prefix, compacted to the front in place.  Each round reads the next
+        // kRound * NT slots into registers before any thread writes; a write lands below
+        // the count kept so far, which is below every later read.
+        constexpr int kRound = 4;
         if (tid == 0) ctl[4] = 0;
-        sync();
         const int lane = threadIdx.x & 31;
+        for (int base = 0; base < n; base += kRound * NT) {
+            uint64_t v[kRound];
 #pragma unroll
-        for (int j = 0; j < PER; ++j) {
-            const bool keep = v[j] != 0ull && v[j] >= prefix;
-            const unsigned m = __ballot_sync(kFull, keep);
-            if (m) {
-                const int leader = __ffs(m) - 1;
-                int base = 0;
-                if (lane == leader) base = atomicAdd(&ctl[4], __popc(m));
-                base = __shfl_sync(kFull, base, leader);
-                const int pos = base + __popc(m & ((1u << lane) - 1u));
-                if (keep && pos < CAP) buf[pos] = v[j];
+            for (int j = 0; j < kRound; ++j) {
+                const int i = base + j * NT + tid;
+                v[j] = i < n ? buf[i] : 0ull;
+            }
+            sync();
+#pragma unroll
+            for (int j = 0; j < kRound; ++j) {
+                const bool keep = v[j] != 0ull && v[j] >= prefix;
+                const unsigned m = __ballot_sync(kFull, keep);
+                if (m) {
+                    const int leader = __ffs(m) - 1;
+                    int at = 0;
+                    if (lane == leader) at = atomicAdd(&ctl[4], __popc(m));
+                    at = __shfl_sync(kFull, at, leader);
+                    const int pos = at + __popc(m & ((1u << lane) - 1u));
+                    if (keep && pos < CAP) buf[pos] = v[j];
+                }
             }
         }
         sync();
         if (tid == 0) {
-            if (ctl[4] != k) atomicOr(err, kErrAssert);
+            if (ctl[4] != kept || (exact && kept != k)) atomicOr(err, kErrAssert);
             ctl[0] = ctl[4] < CAP ? ctl[4] : CAP;
             *thr = prefix;
         }

@@ -93,7 +93,7 @@ const char* tsi_last_error(void) { return g_msg; }
 size_t tsi_indexer_topk_workspace(int B, int T, int S, int H_I, int d_I, int topk,
                                   int qk_dtype) {
     if (B <= 0 || T <= 0 || S < 0 || topk < 1) return 0;
-    if (use_tc_indexer(qk_dtype, H_I, d_I)) return tsi::tc_indexer_workspace_bytes(B, T, S, topk);
+    if (use_tc_indexer(qk_dtype, H_I, d_I)) return tsi::tc_indexer_workspace_bytes(qk_dtype, B, T, S, topk);
     return tsi::generic_workspace_bytes(B, T, S, topk);
 }
 
