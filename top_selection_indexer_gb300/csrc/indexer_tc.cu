@@ -42,6 +42,7 @@ constexpr int kEpiWarps = 16;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kTmemCols = 512;
 constexpr int kChunkBytes = 128 * 128;  // one 128-row x 128-byte swizzled tile
+constexpr int kAllBar = 8;  // named barrier of all epilogue warps (selectors use 1..4)
 
 template <int QK>
 struct TileCfg;
@@ -359,7 +360,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                         sc[j] = tile_score<L::kN>(tmem, quad, r, a, tempty, wg);
                     }
                 }
-                const uint64_t thr = sel.make_room(p.topk, 2);
+                // Room for the round's offers.  All epilogue warps meet here (they wait for
+                // the same accumulators anyway): when some row is about to fill, every row
+                // past half full compacts in the same stall of the MMA pipeline instead of
+                // each stalling it on its own.
+                named_bar(kAllBar, 32 * kEpiWarps);  // every offer of the last round landed
+                const int held = sel.count();
+                const bool full = held > C::kCap - 2 * L::kGroupThreads;
+                if (tc::bar_red_or(kAllBar, 32 * kEpiWarps, full) &&
+                    held > (p.topk + C::kCap - 2 * L::kGroupThreads) / 2)
+                    sel.compact(p.topk, held, false, (C::kCap - 2 * L::kGroupThreads - p.topk) / 4);
+                const uint64_t thr = *reinterpret_cast<volatile uint64_t*>(sel.thr);
 #pragma unroll
                 for (int j = 0; j < 2; ++j)
                     sel.offer_thr(has[j] && row_ok && key[j] < limit,

@@ -58,7 +58,7 @@ struct TopKSelector {
     unsigned* hist;  // [256]
     int* ctl;        // [8]: 0 count, 1 digit, 2 above, 3 in-bin, 4 write cursor
     uint64_t* thr;   // admission threshold
-    uint64_t* rng;   // [2]: smallest and largest held key during a compaction
+    uint64_t* rng;   // largest held key, during a compaction
     int tid;         // 0..NT-1 within the group
     int bar_id;      // named barrier of the group
     unsigned* err;   // device error word: consistency checks record kErrAssert here
@@ -86,8 +86,11 @@ struct TopKSelector {
         sync();
         if (tid == 0) {
             ctl[0] = 0;
+            ctl[4] = 0;
             *thr = 0ull;
+            *rng = 0ull;
         }
+        for (int i = tid; i < 256; i += NT) hist[i] = 0u;
         sync();
     }
 
@@ -153,44 +156,39 @@ struct TopKSelector {
     // Collective: drop held keys that cannot be among the k largest (no-op when n <= k).
     // `n` must be a settled_count() result (the same value in every thread).
     //
-    // An MSD radix select over the 64-bit keys.  The bits above the highest bit in which
-    // the smallest and the largest held key differ are common to all keys and skipped;
-    // then one digit of up to 8 bits per pass narrows down the bin holding the k-th
-    // largest key.  exact: refine until exactly k keys are kept.  Otherwise stop at the
-    // first digit whose bin keeps at most k + slack keys: every key dropped is below the
-    // k-th largest, so nothing of the final top k is lost.  The admission threshold rises
-    // to the kept bin's lower edge.
+    // An MSD radix select over the 64-bit keys.  Every held key lies between the admission
+    // threshold and the largest held key, so the bits above the highest bit in which
+    // those two differ are common to all keys and skipped; then one digit of up to 8 bits
+    // per pass narrows down the bin holding the k-th largest key.  exact: refine until
+    // exactly k keys are kept.  Otherwise stop at the first digit whose bin keeps at most
+    // k + slack keys: every key dropped is below the k-th largest, so nothing of the
+    // final top k is lost.  The admission threshold rises to the kept bin's lower edge.
+    // Between compactions hist[] is all zero and rng[0] is 0.
     __device__ void compact(int k, int n, bool exact = true, int slack = 0) {
         if (n <= k) return;
-        // smallest and largest held key
-        uint64_t lo = ~0ull, hi = 0ull;
-        for (int i = tid; i < n; i += NT) {
-            const uint64_t x = buf[i];
-            lo = x < lo ? x : lo;
-            hi = x > hi ? x : hi;
+        constexpr int U = 4;  // keys in flight per thread
+        uint64_t hi = 0ull;
+        for (int b = 0; b < n; b += U * NT) {
+            uint64_t x[U];
+#pragma unroll
+            for (int j = 0; j < U; ++j) {
+                const int i = b + j * NT + tid;
+                x[j] = i < n ? buf[i] : 0ull;
+            }
+#pragma unroll
+            for (int j = 0; j < U; ++j) hi = x[j] > hi ? x[j] : hi;
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
-            const uint64_t l2 = __shfl_xor_sync(kFull, lo, o);
             const uint64_t h2 = __shfl_xor_sync(kFull, hi, o);
-            lo = l2 < lo ? l2 : lo;
             hi = h2 > hi ? h2 : hi;
         }
-        if (tid == 0) {
-            rng[0] = ~0ull;
-            rng[1] = 0ull;
-        }
+        if ((threadIdx.x & 31) == 0)
+            atomicMax(reinterpret_cast<unsigned long long*>(rng), static_cast<unsigned long long>(hi));
         sync();
-        if ((threadIdx.x & 31) == 0) {
-            atomicMin(reinterpret_cast<unsigned long long*>(&rng[0]),
-                      static_cast<unsigned long long>(lo));
-            atomicMax(reinterpret_cast<unsigned long long*>(&rng[1]),
-                      static_cast<unsigned long long>(hi));
-        }
-        sync();
-        lo = rng[0];
-        hi = rng[1];
-        if (lo == hi) {  // keys are distinct, so n >= 2 keys cannot all be equal
+        hi = *rng;
+        const uint64_t lo = *thr;
+        if (hi <= lo) {  // n >= 2 distinct keys, all >= lo: the largest is above lo
             if (tid == 0) atomicOr(err, kErrAssert);
             return;
         }
@@ -204,21 +202,22 @@ struct TopKSelector {
             const int end = shift + width;
             const uint64_t hmask = end >= 64 ? 0ull : ~((1ull << end) - 1ull);
             const unsigned dmask = (1u << width) - 1u;
-            for (int i = tid; i < 256; i += NT) hist[i] = 0u;
-            sync();
-            // every thread has read the previous pass's ctl[1..3] before the barrier above
-            if (tid == 0) ctl[1] = -1;
-            for (int b = 0; b < n; b += NT) {
-                const int i = b + tid;
-                const uint64_t x = i < n ? buf[i] : 0ull;
-                const bool in = (i < n) && ((x & hmask) == prefix);
-                const unsigned d = in ? static_cast<unsigned>(x >> shift) & dmask : 256u;
-                const unsigned peers = __match_any_sync(kFull, d);
-                if (in && (threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[d], __popc(peers));
+            for (int b = 0; b < n; b += U * NT) {
+                uint64_t x[U];
+#pragma unroll
+                for (int j = 0; j < U; ++j) {
+                    const int i = b + j * NT + tid;
+                    x[j] = i < n ? buf[i] : 0ull;
+                }
+#pragma unroll
+                for (int j = 0; j < U; ++j) {
+                    if (b + j * NT + tid < n && (x[j] & hmask) == prefix)
+                        atomicAdd(&hist[static_cast<unsigned>(x[j] >> shift) & dmask], 1u);
+                }
             }
             sync();
             if (tid < 32) {
-                // lane l scans bins 255-8l .. 248-8l (descending key order)
+                // lane l scans bins 255-8l .. 248-8l (descending key order), then clears them
                 unsigned c[8];
                 unsigned sum = 0;
 #pragma unroll
@@ -226,6 +225,13 @@ struct TopKSelector {
                     c[j] = hist[255 - (tid * 8 + j)];
                     sum += c[j];
                 }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) hist[255 - (tid * 8 + j)] = 0u;
+                if (tid == 0) {
+                    ctl[1] = -1;
+                    *rng = 0ull;  // every thread read it before the barrier above
+                }
+                __syncwarp();
                 unsigned incl = sum;
 #pragma unroll
                 for (int o = 1; o < 32; o <<= 1) {
@@ -264,9 +270,9 @@ struct TopKSelector {
         const int kept = k - need + inbin;
         // keep keys >= prefix, compacted to the front in place.  Each round reads the next
         // kRound * NT slots into registers before any thread writes; a write lands below
-        // the count kept so far, which is below every later read.
-        constexpr int kRound = 4;
-        if (tid == 0) ctl[4] = 0;
+        // the count kept so far, which is below every later read.  ctl[4] is 0 here: the
+        // last user set it back (or reset() did).
+        constexpr int kRound = 8;
         const int lane = threadIdx.x & 31;
         for (int base = 0; base < n; base += kRound * NT) {
             uint64_t v[kRound];
@@ -278,7 +284,7 @@ struct TopKSelector {
             sync();
 #pragma unroll
             for (int j = 0; j < kRound; ++j) {
-                const bool keep = v[j] != 0ull && v[j] >= prefix;
+                const bool keep = base + j * NT + tid < n && v[j] >= prefix;
                 const unsigned m = __ballot_sync(kFull, keep);
                 if (m) {
                     const int leader = __ffs(m) - 1;
@@ -292,8 +298,10 @@ struct TopKSelector {
         }
         sync();
         if (tid == 0) {
-            if (ctl[4] != kept || (exact && kept != k)) atomicOr(err, kErrAssert);
-            ctl[0] = ctl[4] < CAP ? ctl[4] : CAP;
+            const int got = ctl[4];
+            if (got != kept || (exact && kept != k)) atomicOr(err, kErrAssert);
+            ctl[0] = got < CAP ? got : CAP;
+            ctl[4] = 0;
             *thr = prefix;
         }
         sync();
