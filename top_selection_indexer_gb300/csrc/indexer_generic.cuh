@@ -30,4 +30,9 @@ cudaError_t launch_topk_merge(int rows, int topk, int n_splits, const uint64_t* 
                               const int* cand_cnt, int32_t* idx, float* score, unsigned* err,
                               cudaStream_t st);
 
+// Rank one unordered list of at most topk distinct keys per row ([rows][topk] keys +
+// counts) into rank-ordered idx / score rows.
+cudaError_t launch_topk_rank(int rows, int topk, const uint64_t* cand, const int* cand_cnt,
+                             int32_t* idx, float* score, unsigned* err, cudaStream_t st);
+
 }  // namespace tsi

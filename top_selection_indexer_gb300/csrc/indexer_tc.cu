@@ -492,6 +492,8 @@ cudaError_t launch_qk(const IndexerArgs& a, void* workspace, cudaStream_t st) {
     note_launches(1);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    if (p.n_chunks == 1)
+        return launch_topk_rank(rows, a.topk, p.cand, p.cand_cnt, a.idx, a.score, a.err, st);
     return launch_topk_merge(rows, a.topk, p.n_chunks, p.cand, p.cand_cnt, a.idx, a.score, a.err,
                              st);
 }
