@@ -81,7 +81,7 @@ struct Lay {
     static constexpr uint32_t kIdesc = tc::instr_desc(C::kFmt, kTileKeys, kN);
     static constexpr int kBars = 2 * C::kStages + 2 * kAccBufs + 3;
     static constexpr int kSmem = 1024 /* alignment slack */ + C::kStages * kStageBytes +
-                                 kQBytes + kR * kSelBytes + kR * 64 * 4 + kBars * 8 + 16;
+                                 kQBytes + kR * kSelBytes + kBars * 8 + 16;
     static_assert(kSmem <= 227 * 1024, "shared memory");
     static_assert(kEpiWarps == 4 * kR * kSubs, "every epilogue warp has a row");
 };
@@ -130,52 +130,61 @@ __device__ __forceinline__ bool wait_fast(uint64_t* bar, uint32_t parity, bool p
     return probed || tc::mbar_wait(bar, parity, abort, err);
 }
 
-// Score of this thread's key (TMEM lane) for query row r of the unit from accumulator
-// buffer a: sum over the 64 heads of w[h] * max(0, q[h].k), in packed fp32 pairs.  The
-// 64 columns come in two halves (fewer live registers); the buffer is released to the
-// MMA once the second half is in registers.
+__device__ __forceinline__ float2 relu2(uint32_t a, uint32_t b) {
+    return make_float2(fmaxf(__uint_as_float(a), 0.f), fmaxf(__uint_as_float(b), 0.f));
+}
+
+// Key lane (within the warp's 32 TMEM lanes) whose score tile_score returns to this
+// thread: lane 8 (T % 4) + T / 4 of thread T.
+__device__ __forceinline__ int scored_lane(int lane) { return 8 * (lane & 3) + (lane >> 2); }
+
+// Scores of query row r of the unit from accumulator buffer a: sum over the 64 heads of
+// w[h] * max(0, q[h].k), in packed fp32 pairs.
+//
+// The warp reads its 32 TMEM lanes (keys) as two 16-lane slices of the row's 64 columns
+// (16x256b shape).  Thread T then holds, for two keys, the head pairs 8m + 2c + {0, 1}
+// (c = T % 4, m = 0..7), so it needs only those 16 gate weights -- w2[m], kept in
+// registers for the whole unit instead of being re-read from shared memory for every
+// tile.  The four threads with equal T / 4 add their partial sums with two butterfly
+// shuffles (every one of them ends with the same value).  Thread T returns the score of
+// key lane scored_lane(T).  The buffer is released to the MMA once the second slice is in
+// registers.
 template <int N>
 __device__ __forceinline__ float tile_score(uint32_t tmem, int quad, int r, int a, uint64_t* tempty,
-                                            const float* wg) {
+                                            const float2 (&w2)[8]) {
     tc::tc_fence_after();
+    const int c = threadIdx.x & 3;
     const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + a * N + r * 64;
-    float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                     make_float2(0.f, 0.f)};
-    const float4* w4 = reinterpret_cast<const float4*>(wg);
+    float mine = 0.f;
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
+    for (int slice = 0; slice < 2; ++slice) {
         uint32_t v[32];
-        TSI_TMEM_LD32(taddr + half * 32, v);
+        TSI_TMEM_LD16x256_X8(taddr + (static_cast<uint32_t>(16 * slice) << 16), v);
         tc::tmem_wait_ld();
-        if (half == 1) {
+        if (slice == 1) {
             tc::tc_fence_before();
             __syncwarp();
             if ((threadIdx.x & 31) == 0) tc::mbar_arrive(&tempty[a]);
         }
+        // two accumulators per key for a shorter dependency chain
+        float2 a0 = make_float2(0.f, 0.f), a1 = a0, b0 = a0, b1 = a0;
 #pragma unroll
-        for (int h = 0; h < 32; h += 8) {
-            const float4 wa = w4[(half * 32 + h) >> 2];
-            const float4 wb = w4[((half * 32 + h) >> 2) + 1];
-            acc[0] = __ffma2_rn(make_float2(wa.x, wa.y),
-                                make_float2(fmaxf(__uint_as_float(v[h + 0]), 0.f),
-                                            fmaxf(__uint_as_float(v[h + 1]), 0.f)),
-                                acc[0]);
-            acc[1] = __ffma2_rn(make_float2(wa.z, wa.w),
-                                make_float2(fmaxf(__uint_as_float(v[h + 2]), 0.f),
-                                            fmaxf(__uint_as_float(v[h + 3]), 0.f)),
-                                acc[1]);
-            acc[2] = __ffma2_rn(make_float2(wb.x, wb.y),
-                                make_float2(fmaxf(__uint_as_float(v[h + 4]), 0.f),
-                                            fmaxf(__uint_as_float(v[h + 5]), 0.f)),
-                                acc[2]);
-            acc[3] = __ffma2_rn(make_float2(wb.z, wb.w),
-                                make_float2(fmaxf(__uint_as_float(v[h + 6]), 0.f),
-                                            fmaxf(__uint_as_float(v[h + 7]), 0.f)),
-                                acc[3]);
+        for (int m = 0; m < 8; m += 2) {
+            a0 = __ffma2_rn(w2[m], relu2(v[4 * m + 0], v[4 * m + 1]), a0);
+            b0 = __ffma2_rn(w2[m], relu2(v[4 * m + 2], v[4 * m + 3]), b0);
+            a1 = __ffma2_rn(w2[m + 1], relu2(v[4 * m + 4], v[4 * m + 5]), a1);
+            b1 = __ffma2_rn(w2[m + 1], relu2(v[4 * m + 6], v[4 * m + 7]), b1);
         }
+        float sa = (a0.x + a0.y) + (a1.x + a1.y);  // key lane 16 slice + T / 4
+        float sb = (b0.x + b0.y) + (b1.x + b1.y);  // key lane 16 slice + 8 + T / 4
+        sa += __shfl_xor_sync(0xFFFFFFFFu, sa, 1);
+        sb += __shfl_xor_sync(0xFFFFFFFFu, sb, 1);
+        sa += __shfl_xor_sync(0xFFFFFFFFu, sa, 2);
+        sb += __shfl_xor_sync(0xFFFFFFFFu, sb, 2);
+        if (c == 2 * slice) mine = sa;
+        if (c == 2 * slice + 1) mine = sb;
     }
-    return ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) +
-           ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
+    return mine;
 }
 
 template <int QK>
@@ -191,8 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* stages = base;
     uint8_t* qbuf = stages + C::kStages * L::kStageBytes;
     uint8_t* sel_mem = qbuf + L::kQBytes;
-    float* w_s = reinterpret_cast<float*>(sel_mem + R * L::kSelBytes);  // [R][64]
-    uint64_t* bars = reinterpret_cast<uint64_t*>(w_s + R * 64);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sel_mem + R * L::kSelBytes);
     uint64_t* full = bars;
     uint64_t* empty = full + C::kStages;
     uint64_t* tfull = empty + C::kStages;
@@ -327,18 +335,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int gtid = (ew % (4 * L::kSubs)) * 32 + lane;
         TopKSelector<L::kGroupThreads, C::kCap> sel;
         sel.bind(sel_mem + r * L::kSelBytes, gtid, 1 + r, p.err);
-        float* wg = w_s + r * 64;
         int acc_base = 0;  // accumulator counter of the unit's first tile
         for (int u = blockIdx.x; u < p.n_units; u += gridDim.x) {
             const Unit U = unit_of<R>(p, u);
             const int t = U.t_hi - (R - 1) + r;
             const bool row_ok = t >= 0;
             int64_t limit = 0;  // keys s < limit belong to this row
+            float2 w2[8];
+#pragma unroll
+            for (int m = 0; m < 8; ++m) w2[m] = make_float2(0.f, 0.f);
             if (row_ok) {
                 const int64_t pr = query_position(p.kv_len, U.b, p.T, p.S, t);
                 limit = pr + 1 < U.key_hi ? pr + 1 : U.key_hi;
                 const int64_t wrow = (static_cast<int64_t>(U.b) * p.T + t) * 64;
-                if (gtid < 64) wg[gtid] = load_elem(p.w, wrow + gtid, p.w_dtype);
+                // this thread's 16 gate weights (see tile_score)
+#pragma unroll
+                for (int m = 0; m < 8; ++m) {
+                    const int64_t h = wrow + 8 * m + 2 * (lane & 3);
+                    w2[m] = make_float2(load_elem(p.w, h, p.w_dtype), load_elem(p.w, h + 1, p.w_dtype));
+                }
             }
             sel.reset();
             // per round each warp scores two of its tiles, then one room check covers the
@@ -351,13 +366,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int j = 0; j < 2; ++j) {
                     const int i = i0 + j * L::kSubs + sub;
                     has[j] = i < U.ntiles;
-                    key[j] = U.key_lo + static_cast<int64_t>(i) * kTileKeys + quad * 32 + lane;
+                    key[j] = U.key_lo + static_cast<int64_t>(i) * kTileKeys + quad * 32 +
+                             scored_lane(lane);
                     sc[j] = 0.f;
                     if (has[j]) {
                         const int acc = acc_base + i;
                         const int a = acc % L::kAccBufs;
                         tc::mbar_wait(&tfull[a], (acc / L::kAccBufs) & 1, abort, p.err);
-                        sc[j] = tile_score<L::kN>(tmem, quad, r, a, tempty, wg);
+                        sc[j] = tile_score<L::kN>(tmem, quad, r, a, tempty, w2);
                     }
                 }
                 // Room for the round's offers.  All epilogue warps meet here (they wait for
