@@ -19,13 +19,15 @@
 // (always on the first tile of a row), and then O^T is rescaled in place.
 //
 // Roles of one persistent CTA (512 threads):
-//   warps 0..3   softmax (writes P^T over the RoPE chunk once S^T is done) and the row
-//                epilogue (1/l normalisation, bf16 stores)
-//   warp 4       TMEM allocator + single-thread MMA issuer
-//   warps 5..15  gather: 16-byte cp.async of the selected latent rows into nine 128-byte-
-//                swizzled 64-dim chunk tiles (per-chunk mbarriers), plus the Q TMA load.
-//                The gather rate of cp.async grows with the number of issuing warps, so it
-//                gets most of the CTA's warps.
+//   warp 4        TMEM allocator + single-thread MMA issuer
+//   other warps   gather: 16-byte cp.async of the selected latent rows into nine 128-byte-
+//                 swizzled 64-dim chunk tiles (per-chunk mbarriers); warp 5 also loads Q
+//                 by TMA.  The gather rate of cp.async grows with the number of issuing
+//                 warps, so all 15 take part.
+//   warps 0..3,   softmax (writes P^T over the RoPE chunk once S^T is done) and the row
+//   8..11         epilogue (1/l normalisation, bf16 stores), heads 0..31 on warps 0..3 and
+//                 32..63 on warps 8..11: two warps per TMEM lane quadrant.  They gather
+//                 the next tile after writing P, when its chunks start to free up.
 // Row sums l[h] = sum_s P[h,s] come from the tensor core too: a fifth M=128 block
 // multiplies a 128-byte tile of ones (no-swizzle descriptor, zero strides: every core
 // matrix reads the same bytes) by P^T, so l sums exactly the bf16 P that multiplies V.
@@ -50,14 +52,16 @@ constexpr int kChunks = kDqk / 64;  // 9 chunks of 64 dims (128 bytes) per laten
 constexpr int kKVChunkBytes = kKeys * 128;
 constexpr int kQChunkBytes = kHeads * 128;
 constexpr int kPSlot = 8;  // the RoPE chunk's slot holds P^T once S^T is done
-// 16 warps = 4 warpgroups: warpgroup 0 softmax/epilogue (registers raised), warp 4 MMA,
-// warps 5..15 gather producers (warpgroups 1..3, registers lowered).
+// 16 warps: warp 4 issues the MMAs; the other 15 gather.  Warps 0..3 and 8..11 also run
+// the softmax and the row epilogue, warps 0..3 for heads 0..31 and 8..11 for heads
+// 32..63 of the keys in their TMEM lane quadrant (warp % 4).
 constexpr int kThreads = 512;
 constexpr int kMmaWarp = 4;
-constexpr int kProdThread0 = 160;
-constexpr int kProducers = kThreads - kProdThread0;  // 352
-constexpr int kSoftThread0 = 0;
+constexpr int kGather = kThreads - 32;  // gathering threads (all but the MMA warp)
+constexpr int kGatherQ = 128;  // gather index of the thread that loads Q (warp 5, lane 0)
+constexpr int kSoftThreads = 256;
 constexpr int kSoftBar = 1;
+__device__ __forceinline__ bool is_softmax_warp(int w) { return (w & 4) == 0; }
 constexpr int kTmemCols = 512;
 constexpr int kColS = 0;
 constexpr int kColO = 64;  // O^T block m (d rows 128m..128m+127) at columns 64 + 64m
@@ -110,6 +114,41 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     return lo | (hi << 16);
 }
 
+// This thread's share of the gather of key tile t of work item W: a chunk is 128 keys x 8
+// pieces of 16 bytes, and gather thread g copies pieces g, g + kGather, g + 2 kGather of
+// every chunk, each chunk as soon as the MMA has released its slot (ring phase it).
+__device__ __forceinline__ void gather_tile(const AttnTcParams& p, const Work& W, int t, int it,
+                                            int g, uint32_t kv_addr, uint64_t* kv_empty,
+                                            uint64_t* kv_full, volatile int* abort) {
+    const int64_t len = seq_len(p.kv_len, W.b, p.S);
+    const int32_t* irow = p.idx + static_cast<int64_t>(W.row) * p.topk;
+    const uint16_t* src[3];
+    uint32_t nbytes[3];
+    uint32_t dst0[3];
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+        const int piece = g + kGather * j;
+        const int k = (piece >> 3) & (kKeys - 1);
+        const int sub = piece & 7;
+        const int e = t * kKeys + k;
+        const int s = (piece < kKeys * 8 && e < p.topk) ? irow[e] : -1;
+        const bool ok = s >= 0 && s < len;
+        src[j] = ok ? p.k + (static_cast<int64_t>(W.b) * p.S + s) * kDqk + sub * 8 : p.k;
+        nbytes[j] = ok ? 16u : 0u;
+        dst0[j] = kv_addr + (k >> 3) * 1024 + (k & 7) * 128 + ((sub ^ (k & 7)) << 4);
+    }
+    for (int c = 0; c < kChunks; ++c) {
+        tc::mbar_wait(&kv_empty[c], (it & 1) ^ 1, abort, p.err);
+#pragma unroll
+        for (int j = 0; j < 3; ++j) {
+            if (g + kGather * j < kKeys * 8)
+                tc::cp_async16(dst0[j] + c * kKVChunkBytes, src[j] + (nbytes[j] ? c * 64 : 0),
+                               nbytes[j]);
+        }
+        tc::cp_async_arrive_noinc(&kv_full[c]);
+    }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     tsi_attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const AttnTcParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -142,15 +181,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::fence_proxy_async();  // read by the tensor core
     if (threadIdx.x == 0) {
         for (int c = 0; c < kChunks; ++c) {
-            tc::mbar_init(&kv_full[c], kProducers);
+            tc::mbar_init(&kv_full[c], kGather);
             tc::mbar_init(&kv_empty[c], 1);
         }
         tc::mbar_init(q_full, 1);
         tc::mbar_init(q_empty, 1);
         tc::mbar_init(s_full, 1);
-        tc::mbar_init(p_full, 128);
+        tc::mbar_init(p_full, kSoftThreads);
         tc::mbar_init(o_full, 1);
-        tc::mbar_init(o_empty, 128);
+        tc::mbar_init(o_empty, kSoftThreads);
         tc::mbar_init(done, 1);
         *abort = 0;
         tc::fence_barrier_init();
@@ -227,146 +266,105 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::mma_commit(done);
             tc::mbar_wait(done, 0, abort, p.err);
         }
-    } else if (warp > kMmaWarp) {
-        // ------------------------------------------------------------ gather producers
-        // a chunk is 128 keys x 8 pieces of 16 bytes; thread pt copies pieces pt, pt+352,
-        // pt+704 of every chunk (at most 3 keys per thread and tile)
-        const int pt = threadIdx.x - kProdThread0;
-        int it = 0, r_it = 0;
-        for (int u = blockIdx.x; u < p.n_units; u += gridDim.x, ++r_it) {
-            const Work W = work_of(p, u);
-            if (pt == 0) {
-                tc::mbar_wait(q_empty, (r_it & 1) ^ 1, abort, p.err);
-                if (!*abort) {
-                    tc::mbar_expect_tx(q_full, kChunks * kQChunkBytes);
-                    for (int c = 0; c < kChunks; ++c)
-                        tc::tma_load_2d(qs + c * kQChunkBytes, &tmap_q, c * 64, W.row * kHeads,
-                                        q_full);
-                }
-            }
-            const int64_t len = seq_len(p.kv_len, W.b, p.S);
-            const int32_t* irow = p.idx + static_cast<int64_t>(W.row) * p.topk;
-            for (int t = W.tile0; t < W.tile1; ++t, ++it) {
-                const uint16_t* src[3];
-                uint32_t nbytes[3];
-                uint32_t dst0[3];
-#pragma unroll
-                for (int j = 0; j < 3; ++j) {
-                    const int piece = pt + kProducers * j;
-                    const int k = (piece >> 3) & (kKeys - 1);
-                    const int sub = piece & 7;
-                    const int e = t * kKeys + k;
-                    const int s = (piece < kKeys * 8 && e < p.topk) ? irow[e] : -1;
-                    const bool ok = s >= 0 && s < len;
-                    src[j] = ok ? p.k + (static_cast<int64_t>(W.b) * p.S + s) * kDqk + sub * 8 : p.k;
-                    nbytes[j] = ok ? 16u : 0u;
-                    dst0[j] = kv_addr + (k >> 3) * 1024 + (k & 7) * 128 + ((sub ^ (k & 7)) << 4);
-                }
-                for (int c = 0; c < kChunks; ++c) {
-                    tc::mbar_wait(&kv_empty[c], (it & 1) ^ 1, abort, p.err);
-#pragma unroll
-                    for (int j = 0; j < 3; ++j) {
-                        if (pt + kProducers * j < kKeys * 8)
-                            tc::cp_async16(dst0[j] + c * kKVChunkBytes,
-                                           src[j] + (nbytes[j] ? c * 64 : 0), nbytes[j]);
-                    }
-                    tc::cp_async_arrive_noinc(&kv_full[c]);
-                }
-            }
-        }
-        asm volatile("cp.async.wait_all;" ::: "memory");
     } else {
-        // ------------------------------------------------------------ softmax + epilogue
-        const int st = threadIdx.x - kSoftThread0;
-        const int quad = warp;  // TMEM lanes 32*quad .. 32*quad+31
-        const int k = quad * 32 + lane;  // key slot of the tile owned by this thread
-        const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-        const float neg_inf = -__int_as_float(0x7f800000);
-        uint8_t* prow = kv + kPSlot * kKVChunkBytes + (k >> 3) * 1024 + (k & 7) * 128;
+        // gather index: threads 0..127 and 160..511 (warp 4 issues the MMAs)
+        const int g = threadIdx.x < 128 ? static_cast<int>(threadIdx.x) : threadIdx.x - 32;
         int it = 0, r_it = 0;
-        for (int u = blockIdx.x; u < p.n_units; u += gridDim.x, ++r_it) {
-            const Work W = work_of(p, u);
-            const int64_t len = seq_len(p.kv_len, W.b, p.S);
-            const int32_t* irow = p.idx + static_cast<int64_t>(W.row) * p.topk;
-            if (st < 64) {
-                m_s[st] = neg_inf;
-                tmax_s[st] = 0u;
-            }
-            named_bar(kSoftBar, 128);
-            for (int t = W.tile0; t < W.tile1; ++t, ++it) {
-                const int e = t * kKeys + k;
-                const int s = e < p.topk ? irow[e] : -1;
-                const bool valid = s >= 0 && s < len;
-                tc::mbar_wait(s_full, it & 1, abort, p.err);
-                tc::tc_fence_after();
-                // pass 1: does any logit of this key exceed the running max by 2^16?
-                const uint32_t s_addr = tmem + lane_base + kColS;
-                bool over = false;
-                {
-                    uint32_t z[64];
-                    TSI_TMEM_LD32(s_addr, z);
-                    TSI_TMEM_LD32(s_addr + 32, (z + 32));
-                    tc::tmem_wait_ld();
-#pragma unroll
-                    for (int h = 0; h < 64; ++h)
-                        over |= valid && (__uint_as_float(z[h]) * p.scale_log2 > m_s[h] + kRescaleLog2);
+        if (!is_softmax_warp(warp)) {
+            // -------------------------------------------------------- gather only
+            for (int u = blockIdx.x; u < p.n_units; u += gridDim.x, ++r_it) {
+                const Work W = work_of(p, u);
+                if (g == kGatherQ) {
+                    tc::mbar_wait(q_empty, (r_it & 1) ^ 1, abort, p.err);
+                    if (!*abort) {
+                        tc::mbar_expect_tx(q_full, kChunks * kQChunkBytes);
+                        for (int c = 0; c < kChunks; ++c)
+                            tc::tma_load_2d(qs + c * kQChunkBytes, &tmap_q, c * 64,
+                                            W.row * kHeads, q_full);
+                    }
                 }
-                if (tc::bar_red_or(kSoftBar, 128, over)) {
-                    // exact tile max per head, new running max, rescale what O^T holds
-                    {
-                        uint32_t z[64];
-                        TSI_TMEM_LD32(s_addr, z);
-                        TSI_TMEM_LD32(s_addr + 32, (z + 32));
-                        tc::tmem_wait_ld();
+                for (int t = W.tile0; t < W.tile1; ++t, ++it)
+                    gather_tile(p, W, t, it, g, kv_addr, kv_empty, kv_full, abort);
+            }
+        } else {
+            // -------------------------------------------- gather, softmax + row epilogue
+            const int sw = warp < 4 ? warp : warp - 4;  // softmax warp 0..7
+            const int st = sw * 32 + lane;
+            const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31
+            const int h0 = 32 * (warp >> 3);  // this warp's heads h0 .. h0+31
+            const int k = quad * 32 + lane;  // key slot of the tile owned by this thread
+            const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+            const float neg_inf = -__int_as_float(0x7f800000);
+            uint8_t* prow = kv + kPSlot * kKVChunkBytes + (k >> 3) * 1024 + (k & 7) * 128;
+            for (int u = blockIdx.x; u < p.n_units; u += gridDim.x, ++r_it) {
+                const Work W = work_of(p, u);
+                const int64_t len = seq_len(p.kv_len, W.b, p.S);
+                const int32_t* irow = p.idx + static_cast<int64_t>(W.row) * p.topk;
+                if (st < 64) {
+                    m_s[st] = neg_inf;
+                    tmax_s[st] = 0u;
+                }
+                named_bar(kSoftBar, kSoftThreads);
+                for (int t = W.tile0; t < W.tile1; ++t, ++it) {
+                    // the chunks of tile t free up as the MMA finishes tile t-1 with them,
+                    // and this warp has already written that tile's P
+                    gather_tile(p, W, t, it, g, kv_addr, kv_empty, kv_full, abort);
+                    const int e = t * kKeys + k;
+                    const int s = e < p.topk ? irow[e] : -1;
+                    const bool valid = s >= 0 && s < len;
+                    tc::mbar_wait(s_full, it & 1, abort, p.err);
+                    tc::tc_fence_after();
+                    const uint32_t s_addr = tmem + lane_base + kColS + h0;
+                    uint32_t z[32];  // logits of this key for heads h0 .. h0+31
+                    TSI_TMEM_LD32(s_addr, z);
+                    tc::tmem_wait_ld();
+                    // does any logit of the tile exceed the running max of its head by 2^16?
+                    bool over = false;
 #pragma unroll
-                        for (int h = 0; h < 64; ++h) {
-                            const float zh = valid ? __uint_as_float(z[h]) * p.scale_log2 : neg_inf;
+                    for (int j = 0; j < 32; ++j)
+                        over |= valid && (__uint_as_float(z[j]) * p.scale_log2 > m_s[h0 + j] + kRescaleLog2);
+                    if (tc::bar_red_or(kSoftBar, kSoftThreads, over)) {
+                        // exact tile max per head, new running max, rescale what O^T holds
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const float zh = valid ? __uint_as_float(z[j]) * p.scale_log2 : neg_inf;
                             const uint32_t v = __reduce_max_sync(kFull, score_order_bits(zh));
-                            if (lane == 0) atomicMax(&tmax_s[h], v);
+                            if (lane == 0) atomicMax(&tmax_s[h0 + j], v);
                         }
-                    }
-                    named_bar(kSoftBar, 128);
-                    if (st < 64) {
-                        const float mo = m_s[st];
-                        const float mn = fmaxf(mo, order_bits_score(tmax_s[st]));
-                        alpha_s[st] = mo == neg_inf ? 0.f : ex2(mo - mn);
-                        m_s[st] = mn;
-                        tmax_s[st] = 0u;
-                    }
-                    named_bar(kSoftBar, 128);
-                    if (t != W.tile0) {
-                        for (int m = 0; m < 5; ++m) {  // the 4 O^T blocks and the row sums
-#pragma unroll
-                            for (int half = 0; half < 2; ++half) {
+                        named_bar(kSoftBar, kSoftThreads);
+                        if (st < 64) {
+                            const float mo = m_s[st];
+                            const float mn = fmaxf(mo, order_bits_score(tmax_s[st]));
+                            alpha_s[st] = mo == neg_inf ? 0.f : ex2(mo - mn);
+                            m_s[st] = mn;
+                            tmax_s[st] = 0u;
+                        }
+                        named_bar(kSoftBar, kSoftThreads);
+                        if (t != W.tile0) {
+                            for (int m = 0; m < 5; ++m) {  // the 4 O^T blocks and the row sums
                                 uint32_t o[32];
-                                const uint32_t ta = tmem + lane_base + kColO + 64 * m + 32 * half;
+                                const uint32_t ta = tmem + lane_base + kColO + 64 * m + h0;
                                 TSI_TMEM_LD32(ta, o);
                                 tc::tmem_wait_ld();
 #pragma unroll
                                 for (int j = 0; j < 32; ++j)
-                                    o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha_s[32 * half + j]);
+                                    o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha_s[h0 + j]);
                                 TSI_TMEM_ST32(ta, o);
                             }
+                            tc::tmem_wait_st();
                         }
-                        tc::tmem_wait_st();
                     }
-                }
-                // pass 2: P^T row of this key, 64 heads as bf16, 128-byte swizzled (MN-major B)
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t z[32];
-                    TSI_TMEM_LD32(s_addr + 32 * half, z);
-                    tc::tmem_wait_ld();
+                    // P^T row of this key: heads h0 .. h0+31 as bf16, four 16-byte pieces of
+                    // the 128-byte-swizzled row (MN-major B operand)
 #pragma unroll
                     for (int jj = 0; jj < 4; ++jj) {
-                        const int j = 4 * half + jj;
+                        const int j = (h0 >> 3) + jj;
                         float pv[8];
 #pragma unroll
                         for (int i = 0; i < 8; ++i) {
                             const int h = 8 * j + i;
                             const float zh = __uint_as_float(z[8 * jj + i]) * p.scale_log2;
-                            const float pe = valid ? ex2(zh - m_s[h]) : 0.f;
-                            pv[i] = pe;
+                            pv[i] = valid ? ex2(zh - m_s[h]) : 0.f;
                         }
                         uint4 v;
                         v.x = pack_bf16(pv[0], pv[1]);
@@ -375,21 +373,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                         v.w = pack_bf16(pv[6], pv[7]);
                         *reinterpret_cast<uint4*>(prow + ((j ^ (k & 7)) << 4)) = v;
                     }
+                    tc::fence_proxy_async();
+                    tc::tc_fence_before();
+                    tc::mbar_arrive(p_full);
                 }
-                tc::fence_proxy_async();
-                tc::tc_fence_before();
-                tc::mbar_arrive(p_full);
-            }
-            // ---------------------------------------------------------- row epilogue
-            tc::mbar_wait(o_full, r_it & 1, abort, p.err);
-            tc::tc_fence_after();
-            for (int half = 0; half < 2; ++half) {
-                uint32_t lv[32];  // row sums of heads 32*half .. 32*half+31 (same in every lane)
-                TSI_TMEM_LD32(tmem + lane_base + kColL + 32 * half, lv);
+                // ------------------------------------------------------ row epilogue
+                tc::mbar_wait(o_full, r_it & 1, abort, p.err);
+                tc::tc_fence_after();
+                uint32_t lv[32];  // row sums of heads h0 .. h0+31 (same in every lane)
+                TSI_TMEM_LD32(tmem + lane_base + kColL + h0, lv);
                 tc::tmem_wait_ld();
-                if (st == 0) {
+                if (quad == 0 && lane == 0) {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) l_s[32 * half + j] = __uint_as_float(lv[j]);
+                    for (int j = 0; j < 32; ++j) l_s[h0 + j] = __uint_as_float(lv[j]);
                 }
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
@@ -399,34 +395,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int m = 0; m < 4; ++m) {
                     const int d = 128 * m + 32 * quad + lane;
                     uint32_t o[32];
-                    TSI_TMEM_LD32(tmem + lane_base + kColO + 64 * m + 32 * half, o);
+                    TSI_TMEM_LD32(tmem + lane_base + kColO + 64 * m + h0, o);
                     tc::tmem_wait_ld();
                     if (p.part_o) {
                         float* po = p.part_o +
-                                    ((static_cast<int64_t>(W.row) * p.n_splits + W.split) * kHeads) * kDv + d;
+                                    ((static_cast<int64_t>(W.row) * p.n_splits + W.split) * kHeads + h0) * kDv + d;
 #pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            po[static_cast<int64_t>(32 * half + j) * kDv] = __uint_as_float(o[j]);
+                        for (int j = 0; j < 32; ++j) po[static_cast<int64_t>(j) * kDv] = __uint_as_float(o[j]);
                     } else {
-                        __nv_bfloat16* out = p.out + static_cast<int64_t>(W.row) * kHeads * kDv + d;
+                        __nv_bfloat16* out = p.out + (static_cast<int64_t>(W.row) * kHeads + h0) * kDv + d;
 #pragma unroll
                         for (int j = 0; j < 32; ++j)
-                            out[static_cast<int64_t>(32 * half + j) * kDv] =
+                            out[static_cast<int64_t>(j) * kDv] =
                                 __float2bfloat16_rn(__uint_as_float(o[j]) * __uint_as_float(lv[j]));
                     }
                 }
-            }
-            if (p.part_o) {
-                named_bar(kSoftBar, 128);
-                if (st < 64) {
-                    const int64_t slot = (static_cast<int64_t>(W.row) * p.n_splits + W.split) * kHeads + st;
-                    p.part_ml[2 * slot] = m_s[st];
-                    p.part_ml[2 * slot + 1] = l_s[st];
+                if (p.part_o) {
+                    named_bar(kSoftBar, kSoftThreads);
+                    if (st < 64) {
+                        const int64_t slot = (static_cast<int64_t>(W.row) * p.n_splits + W.split) * kHeads + st;
+                        p.part_ml[2 * slot] = m_s[st];
+                        p.part_ml[2 * slot + 1] = l_s[st];
+                    }
                 }
+                tc::tc_fence_before();
+                tc::mbar_arrive(o_empty);
             }
-            tc::tc_fence_before();
-            tc::mbar_arrive(o_empty);
         }
+        asm volatile("cp.async.wait_all;" ::: "memory");
     }
     tc::tc_fence_before();
     __syncthreads();
