@@ -271,11 +271,43 @@ def run_gpu(args, rank, world):
         "setup_s": round(setup_s, 1),
     }
     result["clocks"] = clocks.summary()
+    if G >= 2 and not args.no_overlap:
+        result["overlap"] = measure_overlap(cfg, ind, idx, ws, stream)
 
     # --- end to end through the C ABI with host buffers ---------------------------------
     if not args.no_e2e:
         result["e2e"] = run_e2e(args, cfg, ind, lay, idx, outs, ws, stream, world)
     return result
+
+
+def measure_overlap(cfg, ind, idx, ws, stream, reps=5):
+    """Cross-layer top-k overlap of the Full layers of groups 0 and 1 (tsi_topk_overlap),
+    outside the timed step: its kernel time and the mean overlap rate of the rows."""
+    import torch
+
+    import top_selection_indexer_gb300 as tsi
+
+    idx_b = torch.empty_like(idx)
+    for g, out in ((0, idx), (1, idx_b)):
+        qI, kI, w = ind[g]
+        tsi.indexer_topk(qI, kI, w, cfg.topk, idx=out, workspace=ws, stream=stream)
+    rows = cfg.B * cfg.T
+    inter = torch.empty(rows, dtype=torch.int32, device=idx.device)
+    card = torch.empty_like(inter)
+    tsi.topk_overlap(idx, idx_b, inter, card, stream=stream)  # warm-up
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(reps):
+        tsi.topk_overlap(idx, idx_b, inter, card, stream=stream)
+    b.record(stream)
+    tsi.device_status(stream)
+    ms = a.elapsed_time(b) / reps
+    nbytes = 2 * rows * cfg.topk * 4 + 2 * rows * 4  # both index buffers in, counts out
+    rate = (inter.double() / card.clamp(min=1).double())[card > 0].mean().item()
+    return {"layers": "Full layers of groups 0 and 1", "rows": rows, "ms_per_launch": round(ms, 4),
+            "achieved_gbs": round(nbytes / (ms / 1e3) / 1e9, 1),
+            "algorithmic_bytes_per_launch": nbytes, "mean_overlap_rate": round(rate, 5)}
 
 
 def run_e2e(args, cfg, ind, lay, idx, outs, ws, stream, world):
@@ -419,6 +451,8 @@ def main():
     ap.add_argument("--config", type=int, default=4)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-overlap", action="store_true",
+                    help="skip the cross-layer top-k overlap measurement after the timed steps")
     ap.add_argument("--tail-rows", type=int, default=0,
                     help="profiling: only the last R query rows of the prefill")
     ap.add_argument("--groups", type=int, default=0, help="profiling: only the first G groups")

@@ -156,6 +156,44 @@ tsi_status tsi_sparse_attn_group(int n_layers, const void* const* q, const void*
                                  size_t workspace_bytes, void* stream);
 
 /*
+ * Layer schedule of an IndexShare stack ("GLM 5.2: Built for Long Horizon Tasks" §5.2:
+ * the model config's index_topk_freq, index_skip_topk_offset and index_topk_pattern, with
+ * periodic full, shared, shared, shared layer types after the offset; "GLM-5.2
+ * 技术报告速览" §IndexShare: a Full layer runs its indexer, a Shared layer reuses the index
+ * rows of the nearest Full layer before it).
+ *
+ *   pattern  NULL, or a string of exactly n_layers characters 'F' (Full) / 'S' (Shared)
+ *            that overrides freq and skip_offset.  When NULL, layers l < skip_offset are
+ *            Full, and from skip_offset on the types repeat with period freq, the first of
+ *            each period Full (freq = 4, skip_offset = 3: F F F F S S S F S S S ...).
+ *   anchor   [n_layers] int32, HOST (out): the layer whose indexer gives layer l its index
+ *            rows; anchor[l] == l exactly for the Full layers.
+ *
+ * Layer 0 must be Full.  TSI_ERR_INVALID_ARG for n_layers < 0, freq < 1, skip_offset < 0,
+ * a pattern of the wrong length or with other characters, a Shared layer 0, or a NULL
+ * anchor with n_layers > 0.  Host only: launches nothing.
+ */
+tsi_status tsi_index_share_layers(int n_layers, int freq, int skip_offset, const char* pattern,
+                                  int32_t* anchor);
+
+/*
+ * Cross-layer top-k overlap ("GLM-5.2 技术报告速览" §IndexShare: the pairwise overlap of
+ * the per-layer top-k index sets that makes reuse across layers possible, 0.7-1.0 between
+ * adjacent layers).  For every row r of two index buffers:
+ *
+ *   idx_a, idx_b  [rows, topk] int32 device: index rows (entries < 0 are padding, the rest
+ *                 distinct positions within a row, as tsi_indexer_topk writes them)
+ *   inter         [rows] int32 device (out): |S_a(r) ∩ S_b(r)|
+ *   card_a        [rows] int32 device (out): |S_a(r)|, the entries >= 0 of row r of idx_a
+ *
+ * The overlap rate of a row is inter / card_a (rows with card_a = 0 have none).  A repeated
+ * position within a row of idx_a sets the device error word (tsi_device_status then returns
+ * TSI_ERR_DEVICE_ASSERT).  1 <= topk <= TSI_MAX_TOPK; pointers 16-byte aligned.
+ */
+tsi_status tsi_topk_overlap(const int32_t* idx_a, const int32_t* idx_b, int rows, int topk,
+                            int32_t* inter, int32_t* card_a, void* stream);
+
+/*
  * Waits for `stream`, then reads and clears the device error word of the current
  * device.  Returns TSI_OK, TSI_ERR_TIMEOUT (a bounded wait ran out),
  * TSI_ERR_DEVICE_ASSERT (a device check failed) or TSI_ERR_CUDA.

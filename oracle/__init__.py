@@ -240,3 +240,53 @@ def dsa_group(indexer_inputs, layers, topk, scale, Dv=None, kv_len=None, share=T
                                 kv_len=kv_len, n_threads=n_threads))
         idxs.append(idx)
     return idxs, outs
+
+
+def index_share_layers(n_layers, freq=4, skip_offset=0, pattern=None):
+    """Anchor layer of every layer of an IndexShare stack.
+
+    "GLM 5.2: Built for Long Horizon Tasks" §5.2: the model config sets index_topk_freq,
+    index_skip_topk_offset and index_topk_pattern, and after the offset the layer types
+    repeat full, shared, shared, shared.  "GLM-5.2 技术报告速览" §IndexShare: a Shared
+    layer inherits the index set of the nearest Full layer before it.  Reading (the pages
+    do not spell out the layers before the offset): they keep their own indexer (Full).
+    An explicit pattern ('F' / 'S' per layer) replaces freq and offset.
+    """
+    if pattern is not None:
+        if len(pattern) != n_layers or any(c not in "FS" for c in pattern):
+            raise ValueError("pattern must have one 'F' or 'S' per layer")
+        kinds = list(pattern)
+    else:
+        kinds = []
+        for layer in range(n_layers):
+            if layer < skip_offset:
+                kinds.append("F")
+            else:
+                kinds.append("F" if (layer - skip_offset) % freq == 0 else "S")
+    anchors = []
+    for layer, kind in enumerate(kinds):
+        if kind == "F":
+            anchors.append(layer)
+        elif not anchors:
+            raise ValueError("layer 0 must be a Full layer")
+        else:
+            anchors.append(anchors[-1])
+    return anchors
+
+
+def topk_overlap(idx_a, idx_b):
+    """Per-row |S_a ∩ S_b| and |S_a| of two [rows, k] index arrays (entries < 0 are padding).
+
+    "GLM-5.2 技术报告速览" §IndexShare: the pairwise overlap of the per-layer top-k index
+    sets.  Written as plain set intersection, one row at a time.
+    """
+    a = np.asarray(idx_a).reshape(-1, np.asarray(idx_a).shape[-1])
+    b = np.asarray(idx_b).reshape(a.shape)
+    inter = np.zeros(a.shape[0], dtype=np.int64)
+    card = np.zeros(a.shape[0], dtype=np.int64)
+    for r in range(a.shape[0]):
+        sa = {int(x) for x in a[r] if x >= 0}
+        sb = {int(x) for x in b[r] if x >= 0}
+        inter[r] = len(sa & sb)
+        card[r] = len(sa)
+    return inter, card

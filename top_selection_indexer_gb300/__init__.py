@@ -24,7 +24,8 @@ MAX_TOPK = 2048
 EXPORTS = ("tsi_indexer_topk_workspace", "tsi_indexer_topk", "tsi_sparse_attn_workspace",
            "tsi_sparse_attn_group", "tsi_device_status", "tsi_last_error", "tsi_version",
            "tsi_launch_count", "tsi_indexer_topk_noalloc", "tsi_indexer_topk_noalloc_limit",
-           "tsi_indexer_topk_path", "tsi_sparse_attn_path")
+           "tsi_indexer_topk_path", "tsi_sparse_attn_path", "tsi_index_share_layers",
+           "tsi_topk_overlap")
 
 
 class TSIError(RuntimeError):
@@ -70,6 +71,10 @@ def load():
             lib.tsi_sparse_attn_path.restype = i32
             lib.tsi_indexer_topk_noalloc_limit.argtypes = []
             lib.tsi_indexer_topk_noalloc_limit.restype = sz
+            lib.tsi_index_share_layers.argtypes = [i32, i32, i32, ctypes.c_char_p, vp]
+            lib.tsi_index_share_layers.restype = i32
+            lib.tsi_topk_overlap.argtypes = [vp, vp, i32, i32, vp, vp, vp]
+            lib.tsi_topk_overlap.restype = i32
             _lib = lib
     return _lib
 
@@ -207,3 +212,32 @@ def sparse_attn_group(qs, ks, vs, idx, scale, kv_len=None, outs=None, workspace=
 def device_status(stream=None):
     """Synchronize and read / clear the device error word (raises on a set flag)."""
     _check(load().tsi_device_status(_stream_handle(stream)))
+
+
+def index_share_layers(n_layers, freq=4, skip_offset=0, pattern=None):
+    """Anchor layer per layer of an IndexShare stack (tsi_index_share_layers): the layer
+    whose indexer gives layer l its index rows, l itself for a Full layer."""
+    out = (ctypes.c_int32 * max(n_layers, 1))()
+    pat = None if pattern is None else pattern.encode()
+    _check(load().tsi_index_share_layers(n_layers, freq, skip_offset, pat,
+                                         ctypes.cast(out, ctypes.c_void_p)))
+    return [int(out[i]) for i in range(n_layers)]
+
+
+def topk_overlap(idx_a, idx_b, inter=None, card_a=None, stream=None):
+    """Per-row |S_a ∩ S_b| and |S_a| of two [rows, topk] int32 index buffers
+    (tsi_topk_overlap).  Returns (inter, card_a), int32 tensors of length rows."""
+    import torch
+
+    if idx_a.shape != idx_b.shape or idx_a.dtype != torch.int32 or idx_b.dtype != torch.int32:
+        raise ValueError("idx_a and idx_b must be int32 tensors of one shape")
+    topk = idx_a.shape[-1]
+    rows = idx_a.numel() // topk if topk else 0
+    if inter is None:
+        inter = torch.empty(rows, dtype=torch.int32, device=idx_a.device)
+    if card_a is None:
+        card_a = torch.empty(rows, dtype=torch.int32, device=idx_a.device)
+    _check(load().tsi_topk_overlap(_dev(idx_a, "idx_a"), _dev(idx_b, "idx_b"), rows, topk,
+                                   _dev(inter, "inter"), _dev(card_a, "card_a"),
+                                   _stream_handle(stream)))
+    return inter, card_a

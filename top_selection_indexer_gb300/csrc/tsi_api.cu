@@ -8,6 +8,7 @@
 #include "attn_generic.cuh"
 #include "indexer_generic.cuh"
 #include "kernels_tc.cuh"
+#include "overlap.cuh"
 #include "tsi_common.cuh"
 
 namespace tsi {
@@ -197,6 +198,52 @@ tsi_status tsi_sparse_attn_group(int n_layers, const void* const* q, const void*
         if (e != cudaSuccess)
             return fail(TSI_ERR_CUDA, "attention launch (layer %d): %s", l, cudaGetErrorString(e));
     }
+    return ok();
+}
+
+tsi_status tsi_index_share_layers(int n_layers, int freq, int skip_offset, const char* pattern,
+                                  int32_t* anchor) {
+    if (n_layers < 0) return fail(TSI_ERR_INVALID_ARG, "n_layers=%d", n_layers);
+    if (n_layers == 0) return ok();
+    if (!anchor) return fail(TSI_ERR_INVALID_ARG, "NULL anchor array");
+    if (pattern) {
+        for (int l = 0; l < n_layers; ++l) {
+            const char c = pattern[l];
+            if (c != 'F' && c != 'S')
+                return fail(TSI_ERR_INVALID_ARG, "pattern[%d] is not 'F' or 'S' (or the pattern "
+                            "is shorter than %d layers)", l, n_layers);
+        }
+        if (pattern[n_layers] != '\0')
+            return fail(TSI_ERR_INVALID_ARG, "pattern is longer than %d layers", n_layers);
+    } else if (freq < 1 || skip_offset < 0) {
+        return fail(TSI_ERR_INVALID_ARG, "freq=%d skip_offset=%d", freq, skip_offset);
+    }
+    int last_full = -1;
+    for (int l = 0; l < n_layers; ++l) {
+        const bool full = pattern ? pattern[l] == 'F'
+                                  : (l < skip_offset || (l - skip_offset) % freq == 0);
+        if (full) last_full = l;
+        if (last_full < 0) return fail(TSI_ERR_INVALID_ARG, "layer 0 must be a Full layer");
+        anchor[l] = last_full;
+    }
+    return ok();
+}
+
+tsi_status tsi_topk_overlap(const int32_t* idx_a, const int32_t* idx_b, int rows, int topk,
+                            int32_t* inter, int32_t* card_a, void* stream) {
+    if (rows < 0) return fail(TSI_ERR_INVALID_ARG, "rows=%d", rows);
+    if (topk < 1 || topk > TSI_MAX_TOPK)
+        return fail(TSI_ERR_UNSUPPORTED, "topk=%d outside [1, %d]", topk, TSI_MAX_TOPK);
+    if (rows == 0) return ok();
+    if (!idx_a || !idx_b || !inter || !card_a) return fail(TSI_ERR_INVALID_ARG, "NULL pointer");
+    if (!aligned16(idx_a) || !aligned16(idx_b) || !aligned16(inter) || !aligned16(card_a))
+        return fail(TSI_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+    unsigned* err = nullptr;
+    tsi_status st = device_error_word(&err);
+    if (st != TSI_OK) return st;
+    cudaError_t e = tsi::launch_topk_overlap(idx_a, idx_b, rows, topk, inter, card_a, err,
+                                             static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(TSI_ERR_CUDA, "overlap launch: %s", cudaGetErrorString(e));
     return ok();
 }
 
