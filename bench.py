@@ -271,6 +271,14 @@ def run_gpu(args, rank, world):
         "setup_s": round(setup_s, 1),
     }
     result["clocks"] = clocks.summary()
+    if cfg.T == 1:
+        # MTP draft steps of a decode (index_share_for_mtp_iteration): the first step runs
+        # the indexer, the later ones reuse its rows; from the measured stage times
+        n = 4
+        result["mtp"] = {"draft_steps": n, "ms_first_step": round(ms_idx + ms_attn, 4),
+                         "ms_later_step": round(ms_attn, 4),
+                         "ms_draft_reusing_indices": round(ms_idx + n * ms_attn, 4),
+                         "ms_draft_recomputing_indices": round(n * (ms_idx + ms_attn), 4)}
     if G >= 2 and not args.no_overlap:
         result["overlap"] = measure_overlap(cfg, ind, idx, ws, stream)
 

@@ -25,6 +25,8 @@ __device__ __forceinline__ uint32_t slot_of(int32_t pos) {
 }
 static_assert(kSlots == 4096, "slot_of takes the top 12 bits of the product");
 
+constexpr int kPer = TSI_MAX_TOPK / kOvThreads;  // positions per thread and row
+
 __global__ void __launch_bounds__(kOvThreads) topk_overlap_kernel(const int32_t* idx_a,
                                                                    const int32_t* idx_b,
                                                                    int topk, int32_t* inter,
@@ -35,11 +37,20 @@ __global__ void __launch_bounds__(kOvThreads) topk_overlap_kernel(const int32_t*
     const int row = blockIdx.x;
     const int32_t* a = idx_a + static_cast<int64_t>(row) * topk;
     const int32_t* b = idx_b + static_cast<int64_t>(row) * topk;
+    // both rows' entries of this thread first, so that their load latencies overlap
+    int32_t pa[kPer], pb[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+        const int i = threadIdx.x + j * kOvThreads;
+        pa[j] = i < topk ? a[i] : kEmpty;
+        pb[j] = i < topk ? b[i] : kEmpty;
+    }
     for (int i = threadIdx.x; i < kSlots; i += kOvThreads) table[i] = kEmpty;
     if (threadIdx.x < 2) counts[threadIdx.x] = 0;
     __syncthreads();
-    for (int i = threadIdx.x; i < topk; i += kOvThreads) {
-        const int32_t pos = b[i];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+        const int32_t pos = pb[j];
         if (pos < 0) continue;
         uint32_t h = slot_of(pos);
         for (int probe = 0; probe < kSlots; ++probe, h = (h + 1) & (kSlots - 1)) {
@@ -49,8 +60,9 @@ __global__ void __launch_bounds__(kOvThreads) topk_overlap_kernel(const int32_t*
     }
     __syncthreads();
     int hit = 0, mine = 0;
-    for (int i = threadIdx.x; i < topk; i += kOvThreads) {
-        const int32_t pos = a[i];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+        const int32_t pos = pa[j];
         if (pos < 0) continue;
         ++mine;
         uint32_t h = slot_of(pos);
