@@ -387,10 +387,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     held > (p.topk + C::kCap - 2 * L::kGroupThreads) / 2)
                     sel.compact(p.topk, held, false, (C::kCap - 2 * L::kGroupThreads - p.topk) / 4);
                 const uint64_t thr = *reinterpret_cast<volatile uint64_t*>(sel.thr);
-#pragma unroll
-                for (int j = 0; j < 2; ++j)
-                    sel.offer_thr(has[j] && row_ok && key[j] < limit,
-                                  make_key(sc[j], static_cast<uint32_t>(key[j])), thr);
+                sel.offer2_thr(has[0] && row_ok && key[0] < limit,
+                               make_key(sc[0], static_cast<uint32_t>(key[0])),
+                               has[1] && row_ok && key[1] < limit,
+                               make_key(sc[1], static_cast<uint32_t>(key[1])), thr);
             }
             acc_base += U.ntiles;
             if (row_ok) {

@@ -153,6 +153,39 @@ struct TopKSelector {
         }
     }
 
+    // Warp-collective: offer_thr of two keys per thread with one shared-memory reservation
+    // for the warp (one atomic round trip instead of two).
+    __device__ __forceinline__ void offer2_thr(bool has0, uint64_t key0, bool has1, uint64_t key1,
+                                               uint64_t threshold) {
+        const int lane = threadIdx.x & 31;
+        const bool t0 = has0 && key0 >= threshold;
+        const bool t1 = has1 && key1 >= threshold;
+        const unsigned m0 = __ballot_sync(kFull, t0);
+        const unsigned m1 = __ballot_sync(kFull, t1);
+        const int n0 = __popc(m0);
+        const int n = n0 + __popc(m1);
+        if (n) {
+            int base = 0;
+            if (lane == 0) base = atomicAdd(&ctl[0], n);
+            base = __shfl_sync(kFull, base, 0);
+            const unsigned below = (1u << lane) - 1u;
+            const int p0 = base + __popc(m0 & below);
+            const int p1 = base + n0 + __popc(m1 & below);
+            if (t0) {
+                if (p0 < CAP)
+                    buf[p0] = key0;
+                else
+                    atomicOr(err, kErrAssert);
+            }
+            if (t1) {
+                if (p1 < CAP)
+                    buf[p1] = key1;
+                else
+                    atomicOr(err, kErrAssert);
+            }
+        }
+    }
+
     // Collective: drop held keys that cannot be among the k largest (no-op when n <= k).
     // `n` must be a settled_count() result (the same value in every thread).
     //
