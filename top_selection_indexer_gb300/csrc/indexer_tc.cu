@@ -380,12 +380,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // the same accumulators anyway): when some row is about to fill, every row
                 // past half full compacts in the same stall of the MMA pipeline instead of
                 // each stalling it on its own.
-                named_bar(kAllBar, 32 * kEpiWarps);  // every offer of the last round landed
-                const int held = sel.count();
-                const bool full = held > C::kCap - 2 * L::kGroupThreads;
-                if (tc::bar_red_or(kAllBar, 32 * kEpiWarps, full) &&
-                    held > (p.topk + C::kCap - 2 * L::kGroupThreads) / 2)
-                    sel.compact(p.topk, held, false, (C::kCap - 2 * L::kGroupThreads - p.topk) / 4);
+                // One barrier: each thread's count may miss the other warps' offers of the
+                // last round (at most 2 NT keys), and this round adds at most 2 NT more, so
+                // the trigger leaves 4 NT of room.  The rows then settle their exact counts.
+                constexpr int kTrigger = C::kCap - 4 * L::kGroupThreads;
+                if (tc::bar_red_or(kAllBar, 32 * kEpiWarps, sel.count() > kTrigger)) {
+                    const int held = sel.settled_count();
+                    if (held > (p.topk + kTrigger) / 2)
+                        sel.compact(p.topk, held, false, (kTrigger - p.topk) / 4);
+                }
                 const uint64_t thr = *reinterpret_cast<volatile uint64_t*>(sel.thr);
                 sel.offer2_thr(has[0] && row_ok && key[0] < limit,
                                make_key(sc[0], static_cast<uint32_t>(key[0])),
