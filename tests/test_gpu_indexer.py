@@ -58,6 +58,14 @@ def test_prefill_chunk_positions(cuda_lib):
                    exact=True, kv_len=[1000, 900])
 
 
+@pytest.mark.parametrize("T", [301, 3])
+def test_prefill_chunk_positions_e4m3(cuda_lib, T):
+    # four query rows per tensor-core unit: T not a multiple of 4 leaves a partial first
+    # unit; rows sit at kv_len - T + t (T = 3: a multi-query decode step)
+    _run_and_check(cuda_lib, 2, T, 1000, 64, 128, 256, "e4m3", "bf16", "int8", "pow2", 43 + T,
+                   exact=True, kv_len=[1000, 905])
+
+
 def test_decode_ragged_kv_len_integer_exact(cuda_lib):
     # one query per sequence at position kv_len-1; empty, tiny and long caches
     _run_and_check(cuda_lib, 6, 1, 40000, 64, 128, 2048, "e4m3", "bf16", "int8", "pow2", 51,
