@@ -79,29 +79,6 @@ __global__ void __launch_bounds__(kNT) indexer_generic_kernel(IndexerArgs a, int
     }
 }
 
-__global__ void __launch_bounds__(kNT) topk_merge_kernel(int topk, int n_splits,
-                                                         const uint64_t* cand,
-                                                         const int* cand_cnt, int32_t* idx,
-                                                         float* score, unsigned* err) {
-    extern __shared__ __align__(16) uint8_t smem[];
-    TopKSelector<kNT, kCAP> sel;
-    sel.bind(smem, threadIdx.x, 0, err);
-    sel.reset();
-    const int row = blockIdx.x;
-    for (int sp = 0; sp < n_splits; ++sp) {
-        const int64_t slot = static_cast<int64_t>(row) * n_splits + sp;
-        const int cnt = cand_cnt[slot];
-        const uint64_t* c = cand + slot * topk;
-        for (int base = 0; base < cnt; base += kNT) {
-            sel.make_room(topk);
-            const int i = base + threadIdx.x;
-            sel.offer(i < cnt, i < cnt ? c[i] : 0ull);
-        }
-    }
-    sel.finalize(topk, idx + static_cast<int64_t>(row) * topk,
-                 score ? score + static_cast<int64_t>(row) * topk : nullptr);
-}
-
 int generic_smem_bytes(int H_I, int d_I) {
     int off = (selector_smem_bytes<kCAP>() + 15) & ~15;
     return off + (H_I * (d_I + 1) + ((H_I + 3) & ~3) + kTK * (d_I + 1)) * 4;
@@ -155,13 +132,7 @@ cudaError_t launch_indexer_generic(const IndexerArgs& a, void* workspace, cudaSt
     note_launches(1);
     e = cudaGetLastError();
     if (e != cudaSuccess || ns == 1) return e;
-    const int msmem = selector_smem_bytes<kCAP>();
-    e = cudaFuncSetAttribute(topk_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             msmem);
-    if (e != cudaSuccess) return e;
-    topk_merge_kernel<<<rows, kNT, msmem, st>>>(a.topk, ns, cand, cnt, a.idx, a.score, a.err);
-    note_launches(1);
-    return cudaGetLastError();
+    return launch_topk_merge(rows, a.topk, ns, cand, cnt, a.idx, a.score, a.err, st);
 }
 
 }  // namespace tsi
@@ -193,27 +164,15 @@ __device__ __forceinline__ void in_thread_stage(uint64_t (&x)[kRankPer], int t, 
         if ((j & D) == 0) cas(x[j], x[j | D], ((kRankPer * t + j) & size) == 0);
 }
 
-// One block per row: the row's n <= topk distinct keys (unordered) become idx / score in
-// rank order, -1 / -inf after the n-th.  A bitonic sorting network over 2048 slots
-// (empty slots hold key 0, below every real key) sorts descending.  Thread t holds slots
+// Rank n <= topk distinct keys held in xs[0 .. kRankN) (empty slots hold key 0, below
+// every real key) and write idx / score rows in rank order, -1 / -inf after the n-th.  A
+// bitonic sorting network over the 2048 slots sorts descending; threads t = 0 .. 255 of
+// the block take part (their only barrier is named barrier `bar`).  Thread t holds slots
 // 8t .. 8t+7 in registers: exchanges at distance < 8 stay in the thread, distances 8..255
 // go through warp shuffles, and only the six stages at distance >= 256 go through shared
 // memory.
-__global__ void __launch_bounds__(kRankThreads) topk_rank_kernel(int topk, const uint64_t* cand,
-                                                                  const int* cand_cnt,
-                                                                  int32_t* idx, float* score,
-                                                                  unsigned* err) {
-    __shared__ __align__(16) uint64_t xs[kRankN];
-    const int row = blockIdx.x;
-    const int t = threadIdx.x;
-    int n = cand_cnt[row];
-    if (n < 0 || n > topk) {
-        if (t == 0) atomicOr(err, kErrAssert);
-        n = n < 0 ? 0 : topk;
-    }
-    const uint64_t* c = cand + static_cast<int64_t>(row) * topk;
-    for (int i = t; i < kRankN; i += kRankThreads) xs[i] = i < n ? c[i] : 0ull;
-    __syncthreads();
+__device__ void rank_sort_write(uint64_t* xs, int n, int topk, int32_t* io, float* so, int t,
+                                int bar) {
     uint64_t x[kRankPer];
 #pragma unroll
     for (int j = 0; j < kRankPer; ++j) x[j] = xs[kRankPer * t + j];
@@ -243,10 +202,10 @@ __global__ void __launch_bounds__(kRankThreads) topk_rank_kernel(int topk, const
                 const bool upper = (t & tm) != 0;
                 const bool desc = ((kRankPer * t) & size) == 0;
                 const bool keep_max = desc != upper;
-                __syncthreads();  // the previous exchange has been read
+                named_bar(bar, kRankThreads);  // the previous exchange has been read
 #pragma unroll
                 for (int j = 0; j < kRankPer; ++j) xs[kRankPer * t + j] = x[j];
-                __syncthreads();
+                named_bar(bar, kRankThreads);
 #pragma unroll
                 for (int j = 0; j < kRankPer; ++j) {
                     const uint64_t y = xs[kRankPer * (t ^ tm) + j];
@@ -255,8 +214,6 @@ __global__ void __launch_bounds__(kRankThreads) topk_rank_kernel(int topk, const
             }
         }
     }
-    int32_t* io = idx + static_cast<int64_t>(row) * topk;
-    float* so = score ? score + static_cast<int64_t>(row) * topk : nullptr;
 #pragma unroll
     for (int j = 0; j < kRankPer; ++j) {
         const int r = kRankPer * t + j;
@@ -266,6 +223,200 @@ __global__ void __launch_bounds__(kRankThreads) topk_rank_kernel(int topk, const
             if (so) so[r] = real ? key_score(x[j]) : -__int_as_float(0x7f800000);
         }
     }
+}
+
+// One block per row: the row's n <= topk distinct keys (unordered) become idx / score in
+// rank order.
+__global__ void __launch_bounds__(kRankThreads) topk_rank_kernel(int topk, const uint64_t* cand,
+                                                                  const int* cand_cnt,
+                                                                  int32_t* idx, float* score,
+                                                                  unsigned* err) {
+    __shared__ __align__(16) uint64_t xs[kRankN];
+    const int row = blockIdx.x;
+    const int t = threadIdx.x;
+    int n = cand_cnt[row];
+    if (n < 0 || n > topk) {
+        if (t == 0) atomicOr(err, kErrAssert);
+        n = n < 0 ? 0 : topk;
+    }
+    const uint64_t* c = cand + static_cast<int64_t>(row) * topk;
+    for (int i = t; i < kRankN; i += kRankThreads) xs[i] = i < n ? c[i] : 0ull;
+    __syncthreads();
+    rank_sort_write(xs, n, topk, idx + static_cast<int64_t>(row) * topk,
+                    score ? score + static_cast<int64_t>(row) * topk : nullptr, t, 1);
+}
+
+// ------------------------------------------------------------------- split merge
+
+constexpr int kMergeThreads = 1024;
+constexpr int kMaxSplits = 1024;  // candidate lists per row the merge accepts
+
+// One block per row: the row's n_splits candidate lists (each the exact top-k of one key
+// range, unordered) -> the row's top k in rank order.  An MSD radix select runs directly
+// over the lists in global memory: the bits above the highest bit in which the smallest
+// and the largest candidate differ are skipped, then 8-bit digits narrow down the bin of
+// the k-th key until exactly k keys are at or above the prefix (keys are distinct).  The
+// k survivors are gathered into shared memory and ranked by rank_sort_write.
+__global__ void __launch_bounds__(kMergeThreads) topk_split_merge_kernel(
+    int topk, int n_splits, const uint64_t* cand, const int* cand_cnt, int32_t* idx,
+    float* score, unsigned* err) {
+    __shared__ __align__(16) uint64_t xs[kRankN];
+    __shared__ unsigned hist[256];
+    __shared__ unsigned long long range[2];
+    __shared__ int ctl[4];  // 0 digit, 1 above, 2 in-bin, 3 write cursor
+    __shared__ int cnt_s[kMaxSplits];
+    __shared__ int total_s;
+    const int row = blockIdx.x;
+    const int tid = threadIdx.x;
+    const uint64_t* rc = cand + static_cast<int64_t>(row) * n_splits * topk;
+    const int* cc = cand_cnt + static_cast<int64_t>(row) * n_splits;
+    if (tid == 0) total_s = 0;
+    __syncthreads();
+    for (int sp = tid; sp < n_splits; sp += kMergeThreads) {
+        int c = cc[sp];
+        if (c < 0 || c > topk) {
+            atomicOr(err, kErrAssert);
+            c = 0;
+        }
+        cnt_s[sp] = c;
+        atomicAdd(&total_s, c);
+    }
+    __syncthreads();
+    const int total = total_s;
+    // every candidate slot of the row: `f(key, valid)` in every lane (warp-uniform calls,
+    // so f may use warp collectives).  The lists sit back to back, topk slots each; a pass
+    // walks the slots four per thread at a time so that a thread's loads are independent.
+    const int n_slots = n_splits * topk;
+    auto for_each = [&](auto f) {
+        constexpr int U = 4;
+        for (int base = 0; base < n_slots; base += U * kMergeThreads) {
+            uint64_t x[U];
+            bool ok[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int slot = base + u * kMergeThreads + tid;
+                const int sp = slot / topk;
+                ok[u] = slot < n_slots && slot - sp * topk < cnt_s[sp < n_splits ? sp : 0];
+                x[u] = ok[u] ? rc[slot] : 0ull;
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) f(x[u], ok[u]);
+        }
+    };
+    const int lane = tid & 31;
+    for (int i = tid; i < 256; i += kMergeThreads) hist[i] = 0u;
+    if (tid == 0) {
+        range[0] = ~0ull;
+        range[1] = 0ull;
+        ctl[3] = 0;
+    }
+    __syncthreads();
+    uint64_t prefix = 0ull;  // keys >= prefix are kept
+    const int n = total < topk ? total : topk;
+    if (total > topk) {
+        uint64_t lo = ~0ull, hi = 0ull;
+        for_each([&](uint64_t x, bool ok) {
+            if (ok) {
+                lo = x < lo ? x : lo;
+                hi = x > hi ? x : hi;
+            }
+        });
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const uint64_t l2 = __shfl_xor_sync(0xFFFFFFFFu, lo, o);
+            const uint64_t h2 = __shfl_xor_sync(0xFFFFFFFFu, hi, o);
+            lo = l2 < lo ? l2 : lo;
+            hi = h2 > hi ? h2 : hi;
+        }
+        if ((tid & 31) == 0) {
+            atomicMin(&range[0], static_cast<unsigned long long>(lo));
+            atomicMax(&range[1], static_cast<unsigned long long>(hi));
+        }
+        __syncthreads();
+        lo = range[0];
+        hi = range[1];
+        const int top = lo == hi ? 0 : 63 - __clzll(static_cast<long long>(lo ^ hi));
+        prefix = top == 63 ? 0ull : (hi & ~((2ull << top) - 1ull));
+        int width = top + 1 < 8 ? top + 1 : 8;
+        int shift = top + 1 - width;
+        int need = topk;
+        while (true) {
+            const int end = shift + width;
+            const uint64_t hmask = end >= 64 ? 0ull : ~((1ull << end) - 1ull);
+            const unsigned dmask = (1u << width) - 1u;
+            for_each([&](uint64_t x, bool ok) {
+                if (ok && (x & hmask) == prefix)
+                    atomicAdd(&hist[static_cast<unsigned>(x >> shift) & dmask], 1u);
+            });
+            __syncthreads();
+            if (tid < 32) {
+                // lane l scans bins 255-8l .. 248-8l (descending key order), then clears them
+                unsigned c[8];
+                unsigned sum = 0;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    c[j] = hist[255 - (tid * 8 + j)];
+                    sum += c[j];
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) hist[255 - (tid * 8 + j)] = 0u;
+                if (tid == 0) ctl[0] = -1;
+                __syncwarp();
+                unsigned incl = sum;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const unsigned v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+                    if (tid >= o) incl += v;
+                }
+                const unsigned excl = incl - sum;
+                if (excl < static_cast<unsigned>(need) && static_cast<unsigned>(need) <= incl) {
+                    unsigned above = excl;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        if (above + c[j] >= static_cast<unsigned>(need)) {
+                            ctl[0] = 255 - (tid * 8 + j);
+                            ctl[1] = static_cast<int>(above);
+                            ctl[2] = static_cast<int>(c[j]);
+                            break;
+                        }
+                        above += c[j];
+                    }
+                }
+            }
+            __syncthreads();
+            const int d = ctl[0];
+            if (d < 0) {  // no bin holds the k-th key: counts are inconsistent
+                if (tid == 0) atomicOr(err, kErrAssert);
+                break;
+            }
+            prefix |= static_cast<uint64_t>(d) << shift;
+            need -= ctl[1];
+            const bool done = ctl[2] == need || shift == 0;
+            __syncthreads();  // every thread has read ctl before the next scan writes it
+            if (done) break;
+            width = shift < 8 ? shift : 8;
+            shift -= width;
+        }
+    }
+    // the survivors (all candidates when there are at most k of them) into shared memory
+    for (int i = tid; i < kRankN; i += kMergeThreads) xs[i] = 0ull;
+    __syncthreads();
+    for_each([&](uint64_t x, bool ok) {
+        const bool keep = ok && x >= prefix;
+        const unsigned m = __ballot_sync(0xFFFFFFFFu, keep);
+        if (m) {
+            int at = 0;
+            if (lane == 0) at = atomicAdd(&ctl[3], __popc(m));
+            at = __shfl_sync(0xFFFFFFFFu, at, 0);
+            const int pos = at + __popc(m & ((1u << lane) - 1u));
+            if (keep && pos < kRankN) xs[pos] = x;
+        }
+    });
+    __syncthreads();
+    if (tid == 0 && ctl[3] != n) atomicOr(err, kErrAssert);
+    if (tid < kRankThreads)
+        rank_sort_write(xs, n, topk, idx + static_cast<int64_t>(row) * topk,
+                        score ? score + static_cast<int64_t>(row) * topk : nullptr, tid, 1);
 }
 
 }  // namespace
@@ -281,11 +432,10 @@ cudaError_t launch_topk_rank(int rows, int topk, const uint64_t* cand, const int
 cudaError_t launch_topk_merge(int rows, int topk, int n_splits, const uint64_t* cand,
                               const int* cand_cnt, int32_t* idx, float* score, unsigned* err,
                               cudaStream_t st) {
-    const int msmem = selector_smem_bytes<kCAP>();
-    cudaError_t e = cudaFuncSetAttribute(topk_merge_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, msmem);
-    if (e != cudaSuccess) return e;
-    topk_merge_kernel<<<rows, kNT, msmem, st>>>(topk, n_splits, cand, cand_cnt, idx, score, err);
+    if (rows == 0) return cudaSuccess;
+    if (n_splits < 1 || n_splits > kMaxSplits) return cudaErrorInvalidValue;
+    topk_split_merge_kernel<<<rows, kMergeThreads, 0, st>>>(topk, n_splits, cand, cand_cnt, idx,
+                                                            score, err);
     note_launches(1);
     return cudaGetLastError();
 }
