@@ -253,7 +253,7 @@ def run_gpu(args, rank, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": f"{cfg.qk_dtype}+bf16", "data": "synthetic",
-        "config": {"workload": f"prefill L={L}, {cfg.n_layers} layers = {G} IndexShare groups "
+        "config": {"workload": f"{_phase(cfg)}, {cfg.n_layers} layers = {G} IndexShare groups "
                                f"(1 Full + {cfg.group - 1} Shared), indexer H_I={cfg.H_I} "
                                f"d_I={cfg.d_I} {cfg.qk_dtype}, k={cfg.topk}, MQA {cfg.H} heads "
                                f"over a {cfg.Dqk}-d bf16 latent (value = first {cfg.Dv})",
@@ -286,6 +286,15 @@ def run_gpu(args, rank, world):
     if not args.no_e2e:
         result["e2e"] = run_e2e(args, cfg, ind, lay, idx, outs, ws, stream, world)
     return result
+
+
+def _phase(cfg):
+    """Name of the workload's phase: a whole prefill, the last rows of one, or a decode."""
+    if cfg.T == cfg.S:
+        return f"prefill L={cfg.S}"
+    if cfg.T == 1:
+        return f"decode B={cfg.B} over L={cfg.S}"
+    return f"chunked prefill: last {cfg.T} rows of L={cfg.S}"
 
 
 def measure_overlap(cfg, ind, idx, ws, stream, reps=5):
