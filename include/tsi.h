@@ -156,6 +156,52 @@ tsi_status tsi_sparse_attn_group(int n_layers, const void* const* q, const void*
                                  size_t workspace_bytes, void* stream);
 
 /*
+ * One key shard of a context-parallel indexer ("GLM 5.2: Built for Long Horizon Tasks",
+ * discussion §4: context parallelism (CP / DCP) for single very long requests, the context
+ * split over ranks; the score and top-k are those of tsi_indexer_topk).  A rank holding keys key_offset ..
+ * key_offset + S_shard - 1 of a cache of S_total keys finds, for every query row, the top k
+ * of its shard; merging the shards' lists (tsi_topk_merge) gives exactly the rows that
+ * tsi_indexer_topk computes over the whole cache.
+ *
+ *   qI, w     as tsi_indexer_topk (all B x T query rows)
+ *   kI        [B, S_shard, d_I] qk_dtype: the shard's keys
+ *   kv_len    [B] int32 or NULL: cached length per sequence in the WHOLE cache (NULL:
+ *             S_total); query row t sits at position kv_len[b] - T + t, as always
+ *   cand      [B*T, topk] uint64 (out): per row the shard's best keys as rank keys
+ *             (order(score) << 32 | (0xFFFFFFFF - position), positions of the whole cache),
+ *             unordered; entries past the count are left as they were
+ *   cand_cnt  [B*T] int32 (out): how many keys of the row the shard holds, at most topk
+ *
+ * Requires 0 <= key_offset, key_offset + S_shard <= S_total, and
+ * workspace_bytes >= tsi_indexer_topk_shard_workspace(...) (0 unless rows are few enough
+ * that keys are split across thread blocks).  Other rules as tsi_indexer_topk.
+ */
+size_t tsi_indexer_topk_shard_workspace(int B, int T, int S_shard, int H_I, int d_I, int topk,
+                                        int qk_dtype);
+tsi_status tsi_indexer_topk_shard(const void* qI, const void* kI, const void* w, int qk_dtype,
+                                  int w_dtype, int B, int T, int S_total, int64_t key_offset,
+                                  int S_shard, int H_I, int d_I, int topk, const int32_t* kv_len,
+                                  uint64_t* cand, int32_t* cand_cnt, void* workspace,
+                                  size_t workspace_bytes, void* stream);
+
+/*
+ * Merge of candidate lists (the exchange step of the context-parallel indexer: every
+ * rank's tsi_indexer_topk_shard output, gathered): for each row, the top k of the union
+ * of its n_lists lists, written as tsi_indexer_topk writes them (rank order, -1 / -inf
+ * padding).  Rank keys are distinct within a row, so the result does not depend on the
+ * order of the lists.
+ *
+ *   cand      [n_lists, rows, topk] uint64 device, list-major (the layout of an
+ *             all-gather of the ranks' cand buffers)
+ *   cand_cnt  [n_lists, rows] int32 device: valid entries of each list, each <= topk
+ *   idx       [rows, topk] int32 device (out); score [rows, topk] float (out, may be NULL)
+ *
+ * 1 <= n_lists <= 1024, 1 <= topk <= TSI_MAX_TOPK; pointers 16-byte aligned.
+ */
+tsi_status tsi_topk_merge(const uint64_t* cand, const int32_t* cand_cnt, int n_lists, int rows,
+                          int topk, int32_t* idx, float* score, void* stream);
+
+/*
  * Layer schedule of an IndexShare stack ("GLM 5.2: Built for Long Horizon Tasks" §5.2:
  * the model config's index_topk_freq, index_skip_topk_offset and index_topk_pattern, with
  * periodic full, shared, shared, shared layer types after the offset; "GLM-5.2

@@ -290,3 +290,31 @@ def topk_overlap(idx_a, idx_b):
         inter[r] = len(sa & sb)
         card[r] = len(sa)
     return inter, card
+
+
+def shard_topk(q_row, k_shard, w_row, p, key_offset, topk):
+    """Top-k of one query row over one key shard, as (scores, positions) in rank order.
+
+    The shard holds keys key_offset .. key_offset + len(k_shard) - 1 of the whole cache;
+    the row at position p keeps the keys s <= p among them ("GLM 5.2: Built for Long
+    Horizon Tasks", discussion §4: the context split over ranks).  Rank order is score
+    descending, position ascending; positions are those of the whole cache.
+    """
+    n_local = min(len(k_shard), int(p) + 1 - int(key_offset))
+    if n_local <= 0:
+        return np.zeros(0), np.zeros(0, dtype=np.int64)
+    sc = indexer_scores(q_row, k_shard[:n_local], w_row, n_local - 1)
+    pos = np.arange(n_local, dtype=np.int64) + int(key_offset)
+    order = np.lexsort((pos, -sc))[:topk]
+    return sc[order], pos[order]
+
+
+def merge_topk(lists, topk):
+    """Top-k of the union of candidate lists [(scores, positions), ...], rank order: the
+    plain definition (concatenate, order by score descending then position ascending)."""
+    if not lists:
+        return np.zeros(0), np.zeros(0, dtype=np.int64)
+    sc = np.concatenate([np.asarray(l[0], dtype=np.float64) for l in lists])
+    pos = np.concatenate([np.asarray(l[1], dtype=np.int64) for l in lists])
+    order = np.lexsort((pos, -sc))[:topk]
+    return sc[order], pos[order]

@@ -25,7 +25,8 @@ EXPORTS = ("tsi_indexer_topk_workspace", "tsi_indexer_topk", "tsi_sparse_attn_wo
            "tsi_sparse_attn_group", "tsi_device_status", "tsi_last_error", "tsi_version",
            "tsi_launch_count", "tsi_indexer_topk_noalloc", "tsi_indexer_topk_noalloc_limit",
            "tsi_indexer_topk_path", "tsi_sparse_attn_path", "tsi_index_share_layers",
-           "tsi_topk_overlap")
+           "tsi_topk_overlap", "tsi_indexer_topk_shard_workspace", "tsi_indexer_topk_shard",
+           "tsi_topk_merge")
 
 
 class TSIError(RuntimeError):
@@ -75,6 +76,14 @@ def load():
             lib.tsi_index_share_layers.restype = i32
             lib.tsi_topk_overlap.argtypes = [vp, vp, i32, i32, vp, vp, vp]
             lib.tsi_topk_overlap.restype = i32
+            lib.tsi_indexer_topk_shard_workspace.argtypes = [i32] * 7
+            lib.tsi_indexer_topk_shard_workspace.restype = sz
+            lib.tsi_indexer_topk_shard.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32,
+                                                   ctypes.c_int64, i32, i32, i32, i32, vp, vp,
+                                                   vp, vp, sz, vp]
+            lib.tsi_indexer_topk_shard.restype = i32
+            lib.tsi_topk_merge.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp]
+            lib.tsi_topk_merge.restype = i32
             _lib = lib
     return _lib
 
@@ -241,3 +250,75 @@ def topk_overlap(idx_a, idx_b, inter=None, card_a=None, stream=None):
                                    _dev(inter, "inter"), _dev(card_a, "card_a"),
                                    _stream_handle(stream)))
     return inter, card_a
+
+
+def indexer_topk_shard(qI, kI, w, topk, S_total, key_offset, kv_len=None, cand=None,
+                       cand_cnt=None, workspace=None, stream=None):
+    """One key shard of a context-parallel indexer (``tsi_indexer_topk_shard``).
+
+    kI [B, S_shard, d_I] holds keys key_offset .. key_offset+S_shard-1 of a cache of
+    S_total keys.  Returns (cand [B*T, topk] uint64 rank keys, unordered, with positions of
+    the whole cache; cand_cnt [B*T] int32).
+    """
+    import torch
+
+    B, T, H_I, d_I = qI.shape
+    S = kI.shape[1]
+    rows = B * T
+    if cand is None:
+        cand = torch.empty((rows, topk), dtype=torch.int64, device=qI.device)
+    if cand_cnt is None:
+        cand_cnt = torch.empty(rows, dtype=torch.int32, device=qI.device)
+    code = _dtype_code(qI)
+    if _dtype_code(kI) != code:
+        raise TypeError("qI and kI must share a dtype")
+    need = load().tsi_indexer_topk_shard_workspace(B, T, S, H_I, d_I, topk, code)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=qI.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().tsi_indexer_topk_shard(
+        _dev(qI, "qI"), _dev(kI, "kI"), _dev(w, "w"), code, _dtype_code(w), B, T, S_total,
+        key_offset, S, H_I, d_I, topk, _dev(kv_len, "kv_len"), _dev(cand, "cand"),
+        _dev(cand_cnt, "cand_cnt"), _dev(workspace, "workspace"), ws_bytes,
+        _stream_handle(stream)))
+    return cand, cand_cnt
+
+
+def topk_merge(cand, cand_cnt, idx=None, score=None, want_score=False, stream=None):
+    """Top-k rows from candidate lists (``tsi_topk_merge``): cand [n_lists, rows, topk]
+    uint64 rank keys, cand_cnt [n_lists, rows] int32.  Returns idx [rows, topk] int32 (and
+    the scores with ``want_score``)."""
+    import torch
+
+    n_lists, rows, topk = cand.shape
+    if idx is None:
+        idx = torch.empty((rows, topk), dtype=torch.int32, device=cand.device)
+    if score is None and want_score:
+        score = torch.empty((rows, topk), dtype=torch.float32, device=cand.device)
+    _check(load().tsi_topk_merge(_dev(cand, "cand"), _dev(cand_cnt, "cand_cnt"), n_lists, rows,
+                                 topk, _dev(idx, "idx"), _dev(score, "score"),
+                                 _stream_handle(stream)))
+    return (idx, score) if score is not None else idx
+
+
+def gather_candidates(cand, cand_cnt, group=None):
+    """The exchange step of the context-parallel indexer: all-gather every rank's candidate
+    lists into [world, rows, topk] / [world, rows] (torch.distributed: NCCL between GPUs)."""
+    import torch
+    import torch.distributed as dist
+
+    world = dist.get_world_size(group)
+    parts_c = [torch.empty_like(cand) for _ in range(world)]
+    parts_n = [torch.empty_like(cand_cnt) for _ in range(world)]
+    dist.all_gather(parts_c, cand.contiguous(), group=group)
+    dist.all_gather(parts_n, cand_cnt.contiguous(), group=group)
+    return torch.stack(parts_c), torch.stack(parts_n)
+
+
+def cp_indexer_topk(qI, kI_shard, w, topk, S_total, key_offset, kv_len=None, group=None,
+                    want_score=False):
+    """Context-parallel indexer + top-k: this rank's shard, the all-gather of every rank's
+    lists, the merge.  Every rank gets the rows of tsi_indexer_topk over the whole cache."""
+    cand, cnt = indexer_topk_shard(qI, kI_shard, w, topk, S_total, key_offset, kv_len=kv_len)
+    all_c, all_n = gather_candidates(cand, cnt, group)
+    return topk_merge(all_c, all_n, want_score=want_score)

@@ -33,8 +33,10 @@ __global__ void __launch_bounds__(kNT) indexer_generic_kernel(IndexerArgs a, int
     const int split = blockIdx.y;
     const int b = row / a.T;
     const int t = row % a.T;
-    const int64_t p = query_position(a.kv_len, b, a.T, a.S, t);
-    const int64_t n_keys = p + 1 > 0 ? p + 1 : 0;
+    // position relative to the first key of this call: keys 0 .. p of kI are causal
+    const int64_t p = query_position(a.kv_len, b, a.T, a.S_total, t) - a.key_offset;
+    int64_t n_keys = p + 1 > 0 ? p + 1 : 0;
+    if (n_keys > a.S) n_keys = a.S;
     const int64_t key_lo = static_cast<int64_t>(split) * chunk;
     const int64_t key_hi = key_lo + chunk < n_keys ? key_lo + chunk : n_keys;
 
@@ -67,10 +69,11 @@ __global__ void __launch_bounds__(kNT) indexer_generic_kernel(IndexerArgs a, int
         acc += __shfl_xor_sync(kFull, acc, 1);
         acc += __shfl_xor_sync(kFull, acc, 2);
         sel.make_room(a.topk);
-        sel.offer(kk < nt && part == 0, make_key(acc, static_cast<uint32_t>(tile + kk)));
+        sel.offer(kk < nt && part == 0,
+                  make_key(acc, static_cast<uint32_t>(tile + kk + a.key_offset)));
         __syncthreads();
     }
-    if (n_splits == 1) {
+    if (n_splits == 1 && !cand) {
         sel.finalize(a.topk, a.idx + static_cast<int64_t>(row) * a.topk,
                      a.score ? a.score + static_cast<int64_t>(row) * a.topk : nullptr);
     } else {
@@ -114,7 +117,9 @@ bool generic_supported(int H_I, int d_I) {
     return H_I >= 1 && d_I >= 1 && d_I <= 256 && H_I <= 128 && H_I * d_I <= 8192;
 }
 
-cudaError_t launch_indexer_generic(const IndexerArgs& a, void* workspace, cudaStream_t st) {
+cudaError_t launch_indexer_generic(const IndexerArgs& args, void* workspace, cudaStream_t st) {
+    IndexerArgs a = args;
+    if (a.S_total == 0) a.S_total = a.S;
     const int rows = a.B * a.T;
     int ns, ch;
     generic_split_plan(rows, a.S, &ns, &ch);
@@ -127,12 +132,17 @@ cudaError_t launch_indexer_generic(const IndexerArgs& a, void* workspace, cudaSt
     if (ns > 1) {
         cand = static_cast<uint64_t*>(workspace);
         cnt = reinterpret_cast<int*>(cand + static_cast<size_t>(rows) * ns * a.topk);
+    } else if (a.out_cand) {  // one list per row: the candidates are the output
+        cand = a.out_cand;
+        cnt = a.out_cnt;
     }
     indexer_generic_kernel<<<dim3(rows, ns), kNT, smem, st>>>(a, ns, ch, cand, cnt);
     note_launches(1);
     e = cudaGetLastError();
     if (e != cudaSuccess || ns == 1) return e;
-    return launch_topk_merge(rows, a.topk, ns, cand, cnt, a.idx, a.score, a.err, st);
+    return launch_topk_merge_strided(rows, a.topk, ns, cand, static_cast<int64_t>(ns) * a.topk,
+                                     a.topk, cnt, ns, 1, a.idx, a.score, a.out_cand, a.out_cnt,
+                                     a.err, st);
 }
 
 }  // namespace tsi
@@ -252,14 +262,17 @@ constexpr int kMergeThreads = 1024;
 constexpr int kMaxSplits = 1024;  // candidate lists per row the merge accepts
 
 // One block per row: the row's n_splits candidate lists (each the exact top-k of one key
-// range, unordered) -> the row's top k in rank order.  An MSD radix select runs directly
+// range, unordered) -> the row's top k in rank order (or, with out_keys, as unordered keys
+// and a count).  List l of row r: cand_cnt[r * cnt_row + l * cnt_list] keys at
+// cand + r * row_stride + l * list_stride.  An MSD radix select runs directly
 // over the lists in global memory: the bits above the highest bit in which the smallest
 // and the largest candidate differ are skipped, then 8-bit digits narrow down the bin of
 // the k-th key until exactly k keys are at or above the prefix (keys are distinct).  The
 // k survivors are gathered into shared memory and ranked by rank_sort_write.
 __global__ void __launch_bounds__(kMergeThreads) topk_split_merge_kernel(
-    int topk, int n_splits, const uint64_t* cand, const int* cand_cnt, int32_t* idx,
-    float* score, unsigned* err) {
+    int topk, int n_splits, const uint64_t* cand, int64_t row_stride, int64_t list_stride,
+    const int* cand_cnt, int64_t cnt_row, int64_t cnt_list, int32_t* idx, float* score,
+    uint64_t* out_keys, int* out_cnt, unsigned* err) {
     __shared__ __align__(16) uint64_t xs[kRankN];
     __shared__ unsigned hist[256];
     __shared__ unsigned long long range[2];
@@ -268,12 +281,12 @@ __global__ void __launch_bounds__(kMergeThreads) topk_split_merge_kernel(
     __shared__ int total_s;
     const int row = blockIdx.x;
     const int tid = threadIdx.x;
-    const uint64_t* rc = cand + static_cast<int64_t>(row) * n_splits * topk;
-    const int* cc = cand_cnt + static_cast<int64_t>(row) * n_splits;
+    const uint64_t* rc = cand + static_cast<int64_t>(row) * row_stride;
+    const int* cc = cand_cnt + static_cast<int64_t>(row) * cnt_row;
     if (tid == 0) total_s = 0;
     __syncthreads();
     for (int sp = tid; sp < n_splits; sp += kMergeThreads) {
-        int c = cc[sp];
+        int c = cc[static_cast<int64_t>(sp) * cnt_list];
         if (c < 0 || c > topk) {
             atomicOr(err, kErrAssert);
             c = 0;
@@ -284,7 +297,7 @@ __global__ void __launch_bounds__(kMergeThreads) topk_split_merge_kernel(
     __syncthreads();
     const int total = total_s;
     // every candidate slot of the row: `f(key, valid)` in every lane (warp-uniform calls,
-    // so f may use warp collectives).  The lists sit back to back, topk slots each; a pass
+    // so f may use warp collectives).  Slot s is entry s % topk of list s / topk; a pass
     // walks the slots four per thread at a time so that a thread's loads are independent.
     const int n_slots = n_splits * topk;
     auto for_each = [&](auto f) {
@@ -296,8 +309,9 @@ __global__ void __launch_bounds__(kMergeThreads) topk_split_merge_kernel(
             for (int u = 0; u < U; ++u) {
                 const int slot = base + u * kMergeThreads + tid;
                 const int sp = slot / topk;
-                ok[u] = slot < n_slots && slot - sp * topk < cnt_s[sp < n_splits ? sp : 0];
-                x[u] = ok[u] ? rc[slot] : 0ull;
+                const int j = slot - sp * topk;
+                ok[u] = slot < n_slots && j < cnt_s[sp < n_splits ? sp : 0];
+                x[u] = ok[u] ? rc[static_cast<int64_t>(sp) * list_stride + j] : 0ull;
             }
 #pragma unroll
             for (int u = 0; u < U; ++u) f(x[u], ok[u]);
@@ -414,6 +428,12 @@ __global__ void __launch_bounds__(kMergeThreads) topk_split_merge_kernel(
     });
     __syncthreads();
     if (tid == 0 && ctl[3] != n) atomicOr(err, kErrAssert);
+    if (out_keys) {  // the survivors themselves, unordered
+        for (int i = tid; i < n; i += kMergeThreads)
+            out_keys[static_cast<int64_t>(row) * topk + i] = xs[i];
+        if (tid == 0) out_cnt[row] = n;
+        return;
+    }
     if (tid < kRankThreads)
         rank_sort_write(xs, n, topk, idx + static_cast<int64_t>(row) * topk,
                         score ? score + static_cast<int64_t>(row) * topk : nullptr, tid, 1);
@@ -432,10 +452,21 @@ cudaError_t launch_topk_rank(int rows, int topk, const uint64_t* cand, const int
 cudaError_t launch_topk_merge(int rows, int topk, int n_splits, const uint64_t* cand,
                               const int* cand_cnt, int32_t* idx, float* score, unsigned* err,
                               cudaStream_t st) {
+    return launch_topk_merge_strided(rows, topk, n_splits, cand,
+                                     static_cast<int64_t>(n_splits) * topk, topk, cand_cnt,
+                                     n_splits, 1, idx, score, nullptr, nullptr, err, st);
+}
+
+cudaError_t launch_topk_merge_strided(int rows, int topk, int n_lists, const uint64_t* cand,
+                                      int64_t row_stride, int64_t list_stride,
+                                      const int* cand_cnt, int64_t cnt_row, int64_t cnt_list,
+                                      int32_t* idx, float* score, uint64_t* out_keys,
+                                      int* out_cnt, unsigned* err, cudaStream_t st) {
     if (rows == 0) return cudaSuccess;
-    if (n_splits < 1 || n_splits > kMaxSplits) return cudaErrorInvalidValue;
-    topk_split_merge_kernel<<<rows, kMergeThreads, 0, st>>>(topk, n_splits, cand, cand_cnt, idx,
-                                                            score, err);
+    if (n_lists < 1 || n_lists > kMaxSplits) return cudaErrorInvalidValue;
+    topk_split_merge_kernel<<<rows, kMergeThreads, 0, st>>>(
+        topk, n_lists, cand, row_stride, list_stride, cand_cnt, cnt_row, cnt_list, idx, score,
+        out_keys, out_cnt, err);
     note_launches(1);
     return cudaGetLastError();
 }

@@ -16,6 +16,15 @@ struct IndexerArgs {
     int32_t* idx;
     float* score;
     unsigned* err;  // device error word
+    // Key shards (context parallelism): the keys kI[b, 0 .. S) sit at positions
+    // key_offset .. key_offset + S - 1 of a cache of S_total keys (0 = S); query positions
+    // and the positions in the results are those of the whole cache.
+    int64_t key_offset = 0;
+    int S_total = 0;
+    // Non-null: each row's top-k leaves as unordered 64-bit rank keys [B*T][topk] with
+    // counts [B*T] instead of rank-ordered idx / score.
+    uint64_t* out_cand = nullptr;
+    int* out_cnt = nullptr;
 };
 
 // CUDA-core path (any supported shape).
@@ -29,6 +38,15 @@ cudaError_t launch_indexer_generic(const IndexerArgs& a, void* workspace, cudaSt
 cudaError_t launch_topk_merge(int rows, int topk, int n_splits, const uint64_t* cand,
                               const int* cand_cnt, int32_t* idx, float* score, unsigned* err,
                               cudaStream_t st);
+
+// General merge: list l of row r holds cand_cnt[r * cnt_row + l * cnt_list] keys at
+// cand + r * row_stride + l * list_stride.  Writes rank-ordered idx / score, or (out_keys
+// non-null) each row's top-k as unordered keys [rows][topk] with counts [rows].
+cudaError_t launch_topk_merge_strided(int rows, int topk, int n_lists, const uint64_t* cand,
+                                      int64_t row_stride, int64_t list_stride,
+                                      const int* cand_cnt, int64_t cnt_row, int64_t cnt_list,
+                                      int32_t* idx, float* score, uint64_t* out_keys,
+                                      int* out_cnt, unsigned* err, cudaStream_t st);
 
 // Rank one unordered list of at most topk distinct keys per row ([rows][topk] keys +
 // counts) into rank-ordered idx / score rows.

@@ -90,6 +90,8 @@ struct TcParams {
     const void* w;
     int w_dtype;
     int B, T, S, topk;
+    int S_total;  // length of the whole cache (the keys here are a shard of it)
+    int64_t key_offset;  // position of key 0 of kI in the whole cache
     const int32_t* kv_len;
     int32_t* idx;
     float* score;
@@ -115,8 +117,10 @@ __device__ __forceinline__ Unit unit_of(const TcParams& p, int u) {
     const int j = pu / p.B;
     U.b = pu % p.B;
     U.t_hi = p.T - 1 - R * j;
-    const int64_t p_hi = query_position(p.kv_len, U.b, p.T, p.S, U.t_hi);
-    const int64_t end = p_hi + 1 > 0 ? p_hi + 1 : 0;
+    // positions relative to key 0 of this call; keys beyond the shard are not here
+    const int64_t p_hi = query_position(p.kv_len, U.b, p.T, p.S_total, U.t_hi) - p.key_offset;
+    int64_t end = p_hi + 1 > 0 ? p_hi + 1 : 0;
+    if (end > p.S) end = p.S;
     U.key_lo = static_cast<int64_t>(U.chunk) * p.chunk_keys;
     U.key_hi = U.key_lo + p.chunk_keys < end ? U.key_lo + p.chunk_keys : end;
     if (U.key_hi < U.key_lo) U.key_hi = U.key_lo;
@@ -345,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int m = 0; m < 8; ++m) w2[m] = make_float2(0.f, 0.f);
             if (row_ok) {
-                const int64_t pr = query_position(p.kv_len, U.b, p.T, p.S, t);
+                const int64_t pr = query_position(p.kv_len, U.b, p.T, p.S_total, t) - p.key_offset;
                 limit = pr + 1 < U.key_hi ? pr + 1 : U.key_hi;
                 const int64_t wrow = (static_cast<int64_t>(U.b) * p.T + t) * 64;
                 // this thread's 16 gate weights (see tile_score)
@@ -391,9 +395,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const uint64_t thr = *reinterpret_cast<volatile uint64_t*>(sel.thr);
                 sel.offer2_thr(has[0] && row_ok && key[0] < limit,
-                               make_key(sc[0], static_cast<uint32_t>(key[0])),
+                               make_key(sc[0], static_cast<uint32_t>(key[0] + p.key_offset)),
                                has[1] && row_ok && key[1] < limit,
-                               make_key(sc[1], static_cast<uint32_t>(key[1])), thr);
+                               make_key(sc[1], static_cast<uint32_t>(key[1] + p.key_offset)), thr);
             }
             acc_base += U.ntiles;
             if (row_ok) {
@@ -491,6 +495,8 @@ cudaError_t launch_qk(const IndexerArgs& a, void* workspace, cudaStream_t st) {
     p.T = a.T;
     p.S = a.S;
     p.topk = a.topk;
+    p.S_total = a.S_total ? a.S_total : a.S;
+    p.key_offset = a.key_offset;
     p.kv_len = a.kv_len;
     p.idx = a.idx;
     p.score = a.score;
@@ -500,8 +506,14 @@ cudaError_t launch_qk(const IndexerArgs& a, void* workspace, cudaStream_t st) {
     const int64_t groups = static_cast<int64_t>(a.B) * ((a.T + R - 1) / R);
     p.n_units = static_cast<int>(groups * p.n_chunks);
     const int rows = a.B * a.T;
-    p.cand = static_cast<uint64_t*>(workspace);
-    p.cand_cnt = reinterpret_cast<int*>(p.cand + static_cast<size_t>(rows) * p.n_chunks * a.topk);
+    if (p.n_chunks == 1 && a.out_cand) {  // one list per row: the candidates are the output
+        p.cand = a.out_cand;
+        p.cand_cnt = a.out_cnt;
+    } else {
+        p.cand = static_cast<uint64_t*>(workspace);
+        p.cand_cnt =
+            reinterpret_cast<int*>(p.cand + static_cast<size_t>(rows) * p.n_chunks * a.topk);
+    }
     constexpr int smem = Lay<QK>::kSmem;
     cudaError_t e = cudaFuncSetAttribute(tsi_indexer_tc_kernel<QK>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -512,9 +524,13 @@ cudaError_t launch_qk(const IndexerArgs& a, void* workspace, cudaStream_t st) {
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (p.n_chunks == 1)
-        return launch_topk_rank(rows, a.topk, p.cand, p.cand_cnt, a.idx, a.score, a.err, st);
-    return launch_topk_merge(rows, a.topk, p.n_chunks, p.cand, p.cand_cnt, a.idx, a.score, a.err,
-                             st);
+        return a.out_cand ? e
+                          : launch_topk_rank(rows, a.topk, p.cand, p.cand_cnt, a.idx, a.score,
+                                             a.err, st);
+    return launch_topk_merge_strided(rows, a.topk, p.n_chunks, p.cand,
+                                     static_cast<int64_t>(p.n_chunks) * a.topk, a.topk,
+                                     p.cand_cnt, p.n_chunks, 1, a.idx, a.score, a.out_cand,
+                                     a.out_cnt, a.err, st);
 }
 
 }  // namespace
@@ -528,6 +544,12 @@ size_t tc_indexer_workspace_bytes(int qk_dtype, int B, int T, int S, int topk) {
     tc_plan(qk_dtype, B, T, S, &nc, &ck);
     const size_t slots = static_cast<size_t>(B) * T * nc;
     return slots * topk * sizeof(uint64_t) + ((slots * sizeof(int) + 255) & ~size_t(255));
+}
+
+size_t tc_indexer_split_workspace_bytes(int qk_dtype, int B, int T, int S, int topk) {
+    int nc, ck;
+    tc_plan(qk_dtype, B, T, S, &nc, &ck);
+    return nc <= 1 ? 0 : tc_indexer_workspace_bytes(qk_dtype, B, T, S, topk);
 }
 
 cudaError_t launch_indexer_tc(const IndexerArgs& a, void* workspace, cudaStream_t st) {

@@ -138,6 +138,86 @@ tsi_status tsi_indexer_topk(const void* qI, const void* kI, const void* w, int q
     return ok();
 }
 
+size_t tsi_indexer_topk_shard_workspace(int B, int T, int S_shard, int H_I, int d_I, int topk,
+                                        int qk_dtype) {
+    if (B <= 0 || T <= 0 || S_shard < 0 || topk < 1) return 0;
+    if (use_tc_indexer(qk_dtype, H_I, d_I))
+        return tsi::tc_indexer_split_workspace_bytes(qk_dtype, B, T, S_shard, topk);
+    return tsi::generic_workspace_bytes(B, T, S_shard, topk);
+}
+
+tsi_status tsi_indexer_topk_shard(const void* qI, const void* kI, const void* w, int qk_dtype,
+                                  int w_dtype, int B, int T, int S_total, int64_t key_offset,
+                                  int S_shard, int H_I, int d_I, int topk, const int32_t* kv_len,
+                                  uint64_t* cand, int32_t* cand_cnt, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+    if (!qk_dtype_ok(qk_dtype)) return fail(TSI_ERR_INVALID_ARG, "qk_dtype %d unknown", qk_dtype);
+    if (!w_dtype_ok(w_dtype)) return fail(TSI_ERR_INVALID_ARG, "w_dtype %d unknown", w_dtype);
+    if (B < 0 || T < 0 || S_shard < 0 || S_total < 0)
+        return fail(TSI_ERR_INVALID_ARG, "negative size (B=%d T=%d S_total=%d S_shard=%d)", B, T,
+                    S_total, S_shard);
+    if (key_offset < 0 || key_offset + S_shard > S_total)
+        return fail(TSI_ERR_INVALID_ARG, "shard [%lld, %lld) outside the cache of %d keys",
+                    static_cast<long long>(key_offset),
+                    static_cast<long long>(key_offset + S_shard), S_total);
+    if (topk < 1 || topk > TSI_MAX_TOPK)
+        return fail(TSI_ERR_UNSUPPORTED, "topk=%d outside [1, %d]", topk, TSI_MAX_TOPK);
+    if (H_I < 1 || d_I < 1) return fail(TSI_ERR_INVALID_ARG, "H_I=%d d_I=%d", H_I, d_I);
+    const bool tc = use_tc_indexer(qk_dtype, H_I, d_I);
+    if (!tc && !tsi::generic_supported(H_I, d_I))
+        return fail(TSI_ERR_UNSUPPORTED, "H_I=%d d_I=%d unsupported (d_I<=256, H_I<=128, "
+                    "H_I*d_I<=8192)", H_I, d_I);
+    if (static_cast<int64_t>(B) * T > (1ll << 31) - 1 ||
+        static_cast<int64_t>(B) * S_total > (1ll << 31) - 1)
+        return fail(TSI_ERR_UNSUPPORTED, "B*T or B*S_total exceeds 2^31-1");
+    if (B == 0 || T == 0) return ok();
+    if (!qI || !w || !cand || !cand_cnt || (S_shard > 0 && !kI))
+        return fail(TSI_ERR_INVALID_ARG, "NULL tensor pointer");
+    if (!aligned16(qI) || !aligned16(kI) || !aligned16(w) || !aligned16(cand) ||
+        !aligned16(cand_cnt) || !aligned16(kv_len))
+        return fail(TSI_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+    const size_t need = tsi_indexer_topk_shard_workspace(B, T, S_shard, H_I, d_I, topk, qk_dtype);
+    if (workspace_bytes < need || (need > 0 && !workspace))
+        return fail(TSI_ERR_WORKSPACE, "workspace %zu bytes, need %zu", workspace_bytes, need);
+    if (need > 0 && !aligned16(workspace))
+        return fail(TSI_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+    unsigned* err = nullptr;
+    tsi_status st = device_error_word(&err);
+    if (st != TSI_OK) return st;
+    tsi::IndexerArgs a{qI, kI, w, qk_dtype, w_dtype, B, T, S_shard, H_I, d_I, topk, kv_len,
+                       nullptr, nullptr, err};
+    a.key_offset = key_offset;
+    a.S_total = S_total;
+    a.out_cand = cand;
+    a.out_cnt = cand_cnt;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = tc ? tsi::launch_indexer_tc(a, workspace, s)
+                       : tsi::launch_indexer_generic(a, workspace, s);
+    if (e != cudaSuccess) return fail(TSI_ERR_CUDA, "indexer launch: %s", cudaGetErrorString(e));
+    return ok();
+}
+
+tsi_status tsi_topk_merge(const uint64_t* cand, const int32_t* cand_cnt, int n_lists, int rows,
+                          int topk, int32_t* idx, float* score, void* stream) {
+    if (rows < 0 || n_lists < 0) return fail(TSI_ERR_INVALID_ARG, "rows=%d n_lists=%d", rows, n_lists);
+    if (topk < 1 || topk > TSI_MAX_TOPK)
+        return fail(TSI_ERR_UNSUPPORTED, "topk=%d outside [1, %d]", topk, TSI_MAX_TOPK);
+    if (n_lists > 1024) return fail(TSI_ERR_UNSUPPORTED, "n_lists=%d above 1024", n_lists);
+    if (rows == 0) return ok();
+    if (n_lists == 0) return fail(TSI_ERR_INVALID_ARG, "no candidate lists");
+    if (!cand || !cand_cnt || !idx) return fail(TSI_ERR_INVALID_ARG, "NULL pointer");
+    if (!aligned16(cand) || !aligned16(cand_cnt) || !aligned16(idx) || !aligned16(score))
+        return fail(TSI_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+    unsigned* err = nullptr;
+    tsi_status st = device_error_word(&err);
+    if (st != TSI_OK) return st;
+    cudaError_t e = tsi::launch_topk_merge_strided(
+        rows, topk, n_lists, cand, topk, static_cast<int64_t>(rows) * topk, cand_cnt, 1, rows,
+        idx, score, nullptr, nullptr, err, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(TSI_ERR_CUDA, "merge launch: %s", cudaGetErrorString(e));
+    return ok();
+}
+
 size_t tsi_sparse_attn_workspace(int B, int T, int S, int H, int Hkv, int Dqk, int Dv,
                                  int topk) {
     if (B <= 0 || T <= 0 || topk < 1 || H < 1) return 0;
