@@ -281,6 +281,8 @@ def run_gpu(args, rank, world):
                          "ms_draft_recomputing_indices": round(n * (ms_idx + ms_attn), 4)}
     if G >= 2 and not args.no_overlap:
         result["overlap"] = measure_overlap(cfg, ind, idx, ws, stream)
+    if not args.no_cp:
+        result["context_parallel"] = measure_cp(cfg, ind, idx, stream)
 
     # --- end to end through the C ABI with host buffers ---------------------------------
     if not args.no_e2e:
@@ -295,6 +297,71 @@ def _phase(cfg):
     if cfg.T == 1:
         return f"decode B={cfg.B} over L={cfg.S}"
     return f"chunked prefill: last {cfg.T} rows of L={cfg.S}"
+
+
+def _balanced_edges(cfg, shards, align=128):
+    """Key-shard edges that give every shard the same number of causal pairs (a prefill's
+    early keys are seen by more rows than its late keys), rounded to `align` keys."""
+    import numpy as np
+
+    p = np.arange(cfg.T, dtype=np.int64) + (cfg.S - cfg.T)  # row positions, kv_len = S
+
+    def pairs_below(e):
+        return int(np.minimum(p + 1, e).clip(min=0).sum())
+
+    total = pairs_below(cfg.S)
+    edges = [0]
+    for i in range(1, shards):
+        lo, hi = edges[-1], cfg.S
+        while lo < hi:  # smallest e with pairs_below(e) >= i / shards of the total
+            mid = (lo + hi) // 2
+            if pairs_below(mid) * shards >= i * total:
+                hi = mid
+            else:
+                lo = mid + 1
+        edges.append(min(cfg.S, max(edges[-1], (lo + align // 2) // align * align)))
+    edges.append(cfg.S)
+    return edges
+
+
+def measure_cp(cfg, ind, idx, stream, shards=2, reps=3):
+    """Context-parallel indexer of group 0 with its keys in `shards` shards of equal causal
+    work, run one after another on this GPU (each standing in for a rank): per-shard kernel
+    time, the merge of the gathered lists, and whether the result equals the unsharded rows."""
+    import torch
+
+    import top_selection_indexer_gb300 as tsi
+
+    qI, kI, w = ind[0]
+    S = cfg.S
+    edges = _balanced_edges(cfg, shards)
+    kparts = [kI[:, lo:hi].contiguous() for lo, hi in zip(edges[:-1], edges[1:])]
+    rows = cfg.B * cfg.T
+    cand = torch.empty((shards, rows, cfg.topk), dtype=torch.int64, device=idx.device)
+    cnt = torch.empty((shards, rows), dtype=torch.int32, device=idx.device)
+    out = torch.empty((rows, cfg.topk), dtype=torch.int32, device=idx.device)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(shards + 2)] for _ in range(reps)]
+    for r in range(reps + 1):  # the first pass warms up
+        rec = ev[r - 1] if r else None
+        for i, (lo, kp) in enumerate(zip(edges[:-1], kparts)):
+            if rec:
+                rec[i].record(stream)
+            tsi.indexer_topk_shard(qI, kp, w, cfg.topk, S, lo, cand=cand[i], cand_cnt=cnt[i],
+                                   stream=stream)
+        if rec:
+            rec[shards].record(stream)
+        tsi.topk_merge(cand, cnt, idx=out, stream=stream)
+        if rec:
+            rec[shards + 1].record(stream)
+    tsi.device_status(stream)
+    shard_ms = [statistics.mean(e[i].elapsed_time(e[i + 1]) for e in ev) for i in range(shards)]
+    merge_ms = statistics.mean(e[shards].elapsed_time(e[shards + 1]) for e in ev)
+    tsi.indexer_topk(qI, kI, w, cfg.topk, idx=idx, stream=stream)
+    same = bool(torch.equal(out, idx.view(rows, cfg.topk)))
+    return {"shards": shards, "key_edges": edges, "ms_per_shard": [round(x, 3) for x in shard_ms],
+            "ms_merge": round(merge_ms, 3), "equals_unsharded": same,
+            "note": "shards run one after another on this GPU, each standing in for a rank; "
+                    "the exchange between ranks (all-gather of the lists) is not timed"}
 
 
 def measure_overlap(cfg, ind, idx, ws, stream, reps=5):
@@ -530,6 +597,8 @@ def main():
     ap.add_argument("--config", type=int, default=4)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-cp", action="store_true",
+                    help="skip the context-parallel indexer measurement after the timed steps")
     ap.add_argument("--no-overlap", action="store_true",
                     help="skip the cross-layer top-k overlap measurement after the timed steps")
     ap.add_argument("--tail-rows", type=int, default=0,

@@ -258,7 +258,6 @@ __global__ void __launch_bounds__(kRankThreads) topk_rank_kernel(int topk, const
 
 // ------------------------------------------------------------------- split merge
 
-constexpr int kMergeThreads = 1024;
 constexpr int kMaxSplits = 1024;  // candidate lists per row the merge accepts
 
 // One block per row: the row's n_splits candidate lists (each the exact top-k of one key
@@ -269,6 +268,7 @@ constexpr int kMaxSplits = 1024;  // candidate lists per row the merge accepts
 // and the largest candidate differ are skipped, then 8-bit digits narrow down the bin of
 // the k-th key until exactly k keys are at or above the prefix (keys are distinct).  The
 // k survivors are gathered into shared memory and ranked by rank_sort_write.
+template <int kMergeThreads>
 __global__ void __launch_bounds__(kMergeThreads) topk_split_merge_kernel(
     int topk, int n_splits, const uint64_t* cand, int64_t row_stride, int64_t list_stride,
     const int* cand_cnt, int64_t cnt_row, int64_t cnt_list, int32_t* idx, float* score,
@@ -464,9 +464,15 @@ cudaError_t launch_topk_merge_strided(int rows, int topk, int n_lists, const uin
                                       int* out_cnt, unsigned* err, cudaStream_t st) {
     if (rows == 0) return cudaSuccess;
     if (n_lists < 1 || n_lists > kMaxSplits) return cudaErrorInvalidValue;
-    topk_split_merge_kernel<<<rows, kMergeThreads, 0, st>>>(
-        topk, n_lists, cand, row_stride, list_stride, cand_cnt, cnt_row, cnt_list, idx, score,
-        out_keys, out_cnt, err);
+    // few rows (decode): wide blocks; many rows: several narrower blocks per SM
+    if (rows < 4 * 152)
+        topk_split_merge_kernel<1024><<<rows, 1024, 0, st>>>(
+            topk, n_lists, cand, row_stride, list_stride, cand_cnt, cnt_row, cnt_list, idx,
+            score, out_keys, out_cnt, err);
+    else
+        topk_split_merge_kernel<kRankThreads><<<rows, kRankThreads, 0, st>>>(
+            topk, n_lists, cand, row_stride, list_stride, cand_cnt, cnt_row, cnt_list, idx,
+            score, out_keys, out_cnt, err);
     note_launches(1);
     return cudaGetLastError();
 }
