@@ -156,6 +156,57 @@ tsi_status tsi_sparse_attn_group(int n_layers, const void* const* q, const void*
                                  size_t workspace_bytes, void* stream);
 
 /*
+ * tsi_sparse_attn_group that also returns each layer's per-head log-partition
+ *
+ *   lse[l]  [B, T, H] fp32 (out) or lse == NULL: ln sum_{s in S} exp(scale * Q_l[b,t,h,:] .
+ *           K_l[b,s,g,:]) over the same keys S as the output; -inf for a row with no key.
+ *
+ * The sum is the one that normalises the output (the tensor-core path sums the bf16
+ * probabilities that multiply V).  It is what tsi_index_kl needs to turn recomputed logits
+ * back into the layer's attention probabilities.  Other arguments and rules as
+ * tsi_sparse_attn_group; lse[l] must be 16-byte aligned.
+ */
+tsi_status tsi_sparse_attn_group_lse(int n_layers, const void* const* q, const void* const* k,
+                                     const void* const* v, int B, int T, int S, int H, int Hkv,
+                                     int Dqk, int Dv, float scale, const int32_t* idx, int topk,
+                                     const int32_t* kv_len, void* const* out, float* const* lse,
+                                     void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Group-centroid KL target of the Full layer's indexer ("GLM-5.2 技术报告速览"
+ * §IndexShare, "少数层挑，其余层复用": the indexer that serves a group of m + 1 layers is
+ * fitted, by KL, to pbar_t = 1/(m+1) sum_j p^(l+j)_t, the mean of the group's
+ * head-averaged attention distributions).  For every query row t of the group (one Full
+ * layer then its Shared layers, n_layers = m + 1) and its selected keys S_t (the entries
+ * of idx[b,t,:] inside [0, kv_len[b])):
+ *
+ *   p_l[t,s]  = 1/H sum_h exp(scale * Q_l[b,t,h,:] . K_l[b,s,:] - lse_l[b,t,h])
+ *   pbar[t,s] = 1/n_layers sum_l p_l[t,s]
+ *   q[t,s]    = exp(I[t,s]) / sum_{s' in S_t} exp(I[t,s'])      (I = score)
+ *   loss[t]   = sum_{s in S_t, pbar > 0} pbar[t,s] (ln pbar[t,s] - ln q[t,s])
+ *   grad[t,s] = q[t,s] - pbar[t,s]          (d loss[t] / d I[t,s]; pbar sums to one)
+ *
+ *   q[l]      [B, T, 64, 576] bf16: layer l's attention queries (H = 64)
+ *   k[l]      [B, S, 576] bf16: layer l's latent key cache (one KV head)
+ *   lse[l]    [B, T, 64] fp32: layer l's log-partition, from tsi_sparse_attn_group_lse with
+ *             the same idx, kv_len and scale
+ *   idx       [B, T, topk] int32: the group's shared index rows
+ *   score     [B, T, topk] fp32: the indexer scores of those entries, I[t, idx[t,i]] (the
+ *             score output of tsi_indexer_topk); read only where the entry is a key
+ *   loss      [B, T] fp32 (out): 0 for a row with no key
+ *   grad      [B, T, topk] fp32 (out) or NULL: in idx order, 0 where the entry is no key
+ *   pbar      [B, T, topk] fp32 (out) or NULL: the centroid in idx order, 0 where no key
+ *
+ * Logits come from bf16 products summed in fp32 on the tensor core, probabilities in fp32;
+ * the loss uses fp32 exp / log.  1 <= n_layers <= 8, 1 <= topk <= TSI_MAX_TOPK; H = 64 and
+ * Dqk = 576 only (TSI_ERR_UNSUPPORTED otherwise).  Pointers must be 16-byte aligned.
+ */
+tsi_status tsi_index_kl(int n_layers, const void* const* q, const void* const* k,
+                        const float* const* lse, int B, int T, int S, int H, int Dqk, float scale,
+                        const int32_t* idx, const float* score, int topk, const int32_t* kv_len,
+                        float* loss, float* grad, float* pbar, void* stream);
+
+/*
  * One key shard of a context-parallel indexer ("GLM 5.2: Built for Long Horizon Tasks",
  * discussion §4: context parallelism (CP / DCP) for single very long requests, the context
  * split over ranks; the score and top-k are those of tsi_indexer_topk).  A rank holding keys key_offset ..

@@ -41,6 +41,8 @@ def _load():
             vp, i32, i64, dbl = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_double
             lib.tsio_decode.argtypes = [vp, i64, i32]
             lib.tsio_decode.restype = dbl
+            lib.tsio_decode_n.argtypes = [vp, i64, i32, vp]
+            lib.tsio_decode_n.restype = None
             lib.tsio_indexer_topk.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32,
                                               vp, i64, vp, vp, vp, vp, i32]
             lib.tsio_indexer_topk.restype = i32
@@ -82,10 +84,10 @@ def n_threads_default() -> int:
 def decode(x) -> np.ndarray:
     """Decode every stored element of ``x`` to float64 (oracle's own decoder)."""
     arr, dt = _as_bytes_array(x)
-    lib = _load()
-    flat = arr.reshape(-1)
-    return np.array([lib.tsio_decode(_ptr(flat), i, DTYPE_CODE[dt]) for i in range(flat.size)],
-                    dtype=np.float64).reshape(arr.shape)
+    flat = np.ascontiguousarray(arr.reshape(-1))
+    out = np.empty(flat.size, dtype=np.float64)
+    _load().tsio_decode_n(_ptr(flat), flat.size, DTYPE_CODE[dt], _ptr(out))
+    return out.reshape(arr.shape)
 
 
 def _rows_arrays(B, T, rows):
@@ -318,3 +320,105 @@ def merge_topk(lists, topk):
     pos = np.concatenate([np.asarray(l[1], dtype=np.int64) for l in lists])
     order = np.lexsort((pos, -sc))[:topk]
     return sc[order], pos[order]
+
+
+def _logsumexp(x, axis=-1):
+    """ln sum exp(x) along ``axis`` in float64 (-inf for an empty or all -inf slice)."""
+    x = np.asarray(x, dtype=np.float64)
+    if x.shape[axis] == 0:
+        return np.full(np.delete(x.shape, axis), -np.inf)
+    m = np.max(x, axis=axis, keepdims=True)
+    m_safe = np.where(np.isfinite(m), m, 0.0)
+    with np.errstate(divide="ignore"):
+        out = np.log(np.sum(np.exp(x - m_safe), axis=axis, keepdims=True)) + m_safe
+    return np.squeeze(out, axis=axis)
+
+
+def index_kl(q_layers, k_layers, idx_rows, score_rows, scale, T, rows, kv_len=None, lse=None):
+    """Group-centroid KL target of a Full layer's indexer, per query row.
+
+    "GLM-5.2 技术报告速览" §IndexShare, subsection "少数层挑，其余层复用": the Full
+    layer's indexer is fitted, by KL, to the centroid of the head-averaged main-attention
+    distributions of the layers it serves,
+
+        pbar_t = 1/(m+1) * sum_{j=0..m} p^(l+j)_t,
+
+    p^(l+j)_t being layer l+j's attention distribution of query t averaged over heads and
+    m the number of Shared layers.  Reading taken here (the page leaves the key set and the
+    KL direction to the sparse-attention setting it builds on): every distribution lives on
+    the row's selected keys S_t (the entries of idx inside [0, kv_len[b])), the only keys
+    the main attention of the group sees, and the loss is KL(pbar_t || q_t) with
+    q_t = softmax over S_t of the indexer scores I[t, s].
+
+    q_layers   list of [n, H, Dqk] query rows of each layer of the group (compacted to
+               ``rows``, flattened b*T + t), Full layer first
+    k_layers   list of [B, S, Dqk] (or [B, S, 1, Dqk]) key caches of the same layers
+    idx_rows   [n, topk] the group's shared index rows; score_rows [n, topk] the indexer
+               scores I[t, idx[t, i]] in the same order
+    lse        optional [G, n, H]: log-partitions to normalise with instead of the exact
+               ones (to check a kernel that is handed another implementation's values)
+    Returns a dict of float64 arrays:
+        lse   [G, n, H]  ln sum_{s in S_t} exp(scale * Q[t,h] . K[s])  (-inf: no key)
+        p     [G, n, topk] head-averaged attention of each layer, 0 at padding
+        pbar  [n, topk]   the centroid
+        q     [n, topk]   the indexer distribution
+        loss  [n]         KL(pbar_t || q_t), 0 for a row with no key
+        grad  [n, topk]   d loss_t / d I[t, idx[t, i]] = q - pbar (pbar sums to one), 0 at
+                          padding
+    Library steps: float64 matmul for the logits; everything else is written out.
+    """
+    import torch
+
+    G = len(q_layers)
+    assert G >= 1 and len(k_layers) == G
+    idx = np.asarray(torch.as_tensor(idx_rows).to("cpu", torch.int64).numpy())
+    n, topk = idx.shape
+    sc = np.asarray(torch.as_tensor(score_rows).to("cpu", torch.float64).numpy()).reshape(n, topk)
+    k_shapes = [tuple(k.shape) for k in k_layers]
+    B, S = k_shapes[0][0], k_shapes[0][1]
+    rb, _ = _rows_arrays(B, T, rows)
+    kv = None if kv_len is None else np.asarray(torch.as_tensor(kv_len).to("cpu").numpy())
+    # decode each layer's queries once; keys once per layer when small, else per row
+    qd = [decode(q).reshape(n, q.shape[-2], q.shape[-1]) for q in q_layers]
+    H = qd[0].shape[1]
+    small = all(int(np.prod(s)) <= (1 << 24) for s in k_shapes)
+    kd = [decode(k).reshape(B, S, -1) for k in k_layers] if small else None
+    out = {
+        "lse": np.full((G, n, H), -np.inf),
+        "p": np.zeros((G, n, topk)),
+        "pbar": np.zeros((n, topk)),
+        "q": np.zeros((n, topk)),
+        "loss": np.zeros(n),
+        "grad": np.zeros((n, topk)),
+    }
+    for r in range(n):
+        b = int(rb[r])
+        length = S if kv is None else int(kv[b])
+        valid = (idx[r] >= 0) & (idx[r] < length)
+        if not valid.any():
+            continue
+        sel = idx[r][valid]
+        for l in range(G):
+            if kd is not None:
+                keys = kd[l][b, sel]
+            else:
+                kl = k_layers[l].reshape(B, S, -1)
+                keys = decode(_take_rows(kl[b], torch.as_tensor(sel)))
+            logits = scale * (qd[l][r] @ keys.T)  # [H, |S_t|]
+            lse_l = _logsumexp(logits, axis=1)  # [H]
+            lse_given = None if lse is None else np.asarray(lse[l][r], dtype=np.float64)
+            lse_use = lse_l if lse_given is None else lse_given
+            probs = np.exp(logits - lse_use[:, None])  # softmax of every head over S_t
+            out["lse"][l, r] = lse_l
+            out["p"][l, r, valid] = probs.mean(axis=0)  # average over the H heads
+        pbar = out["p"][:, r, :].sum(axis=0) / G  # centroid of the group's layers
+        out["pbar"][r] = pbar
+        i_valid = sc[r][valid]
+        log_q = i_valid - _logsumexp(i_valid)
+        q = np.exp(log_q)
+        out["q"][r, valid] = q
+        pv = pbar[valid]
+        pos = pv > 0
+        out["loss"][r] = np.sum(pv[pos] * (np.log(pv[pos]) - log_q[pos]))
+        out["grad"][r, valid] = q - pv
+    return out

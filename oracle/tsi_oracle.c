@@ -78,6 +78,11 @@ double tsio_decode(const void* base, int64_t i, int dtype) {
     }
 }
 
+/* Every stored element of a buffer of n elements, decoded to double. */
+void tsio_decode_n(const void* base, int64_t n, int dtype, double* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = tsio_decode(base, i, dtype);
+}
+
 static int dtype_ok(int dt) { return dt == TSIO_F32 || dt == TSIO_BF16 || dt == TSIO_E4M3; }
 
 /* Position of query row t of sequence b: the T query rows are the last T of the

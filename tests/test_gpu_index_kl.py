@@ -1,0 +1,184 @@
+"""GPU parity of the group-centroid KL kernel (tsi_index_kl) and of the attention
+log-partitions it is fed (tsi_sparse_attn_group_lse), against the oracle.
+
+Tolerances, from the arithmetic: the kernel's logits are bf16 products summed in fp32 on
+the tensor core (relative error ~1e-6 of |logit| <~ 10), its exponentials ex2.approx
+(~2^-22), its head / layer sums fp32: pbar within 2e-4 relative.  The attention's
+log-partition sums the bf16-rounded probabilities that multiply V (each within 2^-9),
+so it sits within 2e-3 of the exact one, and pbar computed from it within 5e-3."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from workloads.gen import draw
+
+pytestmark = pytest.mark.gpu
+
+H, D = 64, 576
+
+
+def _index_rows(B, T, S, topk, kv, seed, dev, interleave=True):
+    """Per row, min(topk, p+1) distinct random positions <= p (p the row's position) and
+    -1 for the rest, in random order when ``interleave`` (any entry may be padding)."""
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    idx = torch.full((B, T, topk), -1, dtype=torch.int32)
+    for b in range(B):
+        L = S if kv is None else kv[b]
+        for t in range(T):
+            p = L - T + t
+            n = max(0, min(topk, p + 1))
+            if n:
+                row = torch.randperm(p + 1, generator=g)[:n].to(torch.int32)
+                idx[b, t, :n] = row
+            if interleave:
+                idx[b, t] = idx[b, t, torch.randperm(topk, generator=g)]
+    return idx.to(dev)
+
+
+def _scores(idx, seed, dev):
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    sc = (torch.randn(idx.shape, generator=g) * 2).to(dev)
+    return torch.where(idx >= 0, sc, torch.full_like(sc, float("-inf")))
+
+
+def _inputs(B, T, S, G, seed, dev):
+    qs = [draw((B, T, H, D), "normal", "bf16", seed + 10 * l, dev) for l in range(G)]
+    ks = [draw((B, S, D), "normal", "bf16", seed + 10 * l + 1, dev) for l in range(G)]
+    return qs, ks
+
+
+def _oracle(qs, ks, idx, sc, scale, kv, rows=None, lse=None):
+    B, T = idx.shape[0], idx.shape[1]
+    rows = np.arange(B * T) if rows is None else np.asarray(rows)
+    q_rows = [q.reshape(B * T, H, D)[torch.as_tensor(rows, device=q.device)].cpu() for q in qs]
+    k_cpu = [k.cpu() for k in ks]
+    idx_r = idx.reshape(B * T, -1)[torch.as_tensor(rows, device=idx.device)].cpu()
+    sc_r = sc.reshape(B * T, -1)[torch.as_tensor(rows, device=sc.device)].cpu()
+    return oracle.index_kl(q_rows, k_cpu, idx_r, sc_r, scale, T, rows,
+                           kv_len=None if kv is None else torch.tensor(kv), lse=lse)
+
+
+def _check(loss, grad, pbar, ref, rows, p_rtol, loss_tol):
+    topk = ref["pbar"].shape[1]
+    pb = pbar.reshape(-1, topk).cpu().double().numpy()[rows]
+    gr = grad.reshape(-1, topk).cpu().double().numpy()[rows]
+    ls = loss.reshape(-1).cpu().double().numpy()[rows]
+    np.testing.assert_allclose(pb, ref["pbar"], rtol=p_rtol, atol=1e-9)
+    np.testing.assert_allclose(gr, ref["grad"], rtol=0,
+                               atol=1e-9 + p_rtol * (np.abs(ref["q"]) + np.abs(ref["pbar"])).max())
+    assert np.all(np.abs(ls - ref["loss"]) <= loss_tol * np.maximum(1.0, np.abs(ref["loss"]))), \
+        np.abs(ls - ref["loss"]).max()
+    assert np.all(pb[ref["pbar"] == 0] == 0)  # entries that are no key stay exactly 0
+
+
+CASES = [
+    # B, T, S, topk, G, kv_len
+    (2, 150, 3000, 2048, 4, [3000, 2100]),  # full tiles, short rows padded
+    (1, 97, 500, 300, 2, None),  # ragged last tile
+    (3, 40, 1000, 129, 1, [1000, 0, 57]),  # one sequence without keys, one shorter than k
+    (1, 20, 4000, 2048, 8, None),  # the largest group
+    (1, 30, 100, 1, 3, None),  # k = 1
+]
+
+
+@pytest.mark.parametrize("B,T,S,topk,G,kv", CASES)
+def test_kl_kernel_matches_oracle(cuda_lib, B, T, S, topk, G, kv):
+    dev = "cuda"
+    seed = 900 + S + T + G
+    qs, ks = _inputs(B, T, S, G, seed, dev)
+    idx = _index_rows(B, T, S, topk, kv, seed + 5, dev)
+    sc = _scores(idx, seed + 6, dev)
+    scale = 1.0 / D ** 0.5
+    ref = _oracle(qs, ks, idx, sc, scale, kv)
+    # the kernel gets the exact log-partitions (rounded to fp32): this checks the kernel alone
+    lses = [torch.from_numpy(ref["lse"][l]).float().reshape(B, T, H).to(dev) for l in range(G)]
+    kv_t = None if kv is None else torch.tensor(kv, dtype=torch.int32, device=dev)
+    loss, grad, pbar = cuda_lib.index_kl(qs, ks, lses, idx, sc, scale, kv_len=kv_t,
+                                         want_grad=True, want_pbar=True)
+    cuda_lib.device_status()
+    _check(loss, grad, pbar, ref, np.arange(B * T), 2e-4, 5e-4)
+
+
+def test_kl_from_the_attention_log_partitions(cuda_lib):
+    # the training-time chain: each layer's sparse attention returns its lse, the KL kernel
+    # recomputes the probabilities from it
+    B, T, S, topk, G, kv = 2, 150, 3000, 2048, 4, [3000, 2100]
+    dev = "cuda"
+    qs, ks = _inputs(B, T, S, G, 4321, dev)
+    idx = _index_rows(B, T, S, topk, kv, 4326, dev, interleave=False)
+    sc = _scores(idx, 4327, dev)
+    scale = 1.0 / D ** 0.5
+    kv_t = torch.tensor(kv, dtype=torch.int32, device=dev)
+    _, lses = cuda_lib.sparse_attn_group(qs, [k.view(B, S, 1, D) for k in ks], None, idx, scale,
+                                         kv_len=kv_t, Dv=512, want_lse=True)
+    loss, grad, pbar = cuda_lib.index_kl(qs, ks, lses, idx, sc, scale, kv_len=kv_t,
+                                         want_grad=True, want_pbar=True)
+    cuda_lib.device_status()
+    ref = _oracle(qs, ks, idx, sc, scale, kv)
+    got_lse = np.stack([l.reshape(B * T, H).cpu().double().numpy() for l in lses])
+    np.testing.assert_allclose(got_lse, ref["lse"], rtol=0, atol=2e-3)
+    _check(loss, grad, pbar, ref, np.arange(B * T), 5e-3, 1e-2)
+    # and against the oracle handed the same log-partitions: the kernel's own error only
+    ref2 = _oracle(qs, ks, idx, sc, scale, kv, lse=got_lse)
+    np.testing.assert_allclose(pbar.reshape(B * T, topk).cpu().double().numpy(), ref2["pbar"],
+                               rtol=2e-4, atol=1e-9)
+
+
+@pytest.mark.parametrize("B,T,S,Hh,Dqk,Dv,topk", [
+    (4, 1, 5000, 64, 576, 512, 2048),  # decode: keys split over CTAs, lse from the combine
+    (1, 200, 800, 64, 576, 512, 333),  # tensor-core kernel, unsplit rows
+    (2, 64, 300, 4, 64, 64, 64),  # CUDA-core kernel
+    (2, 1, 3000, 4, 64, 64, 1024),  # CUDA-core kernel, split rows
+])
+def test_attention_lse_on_every_path(cuda_lib, B, T, S, Hh, Dqk, Dv, topk):
+    dev = "cuda"
+    kv = [S] + [S // 2] * (B - 1)
+    Q = draw((B, T, Hh, Dqk), "normal", "bf16", 77 + S, dev)
+    K = draw((B, S, 1, Dqk), "normal", "bf16", 78 + S, dev)
+    idx = _index_rows(B, T, S, topk, kv, 79 + S, dev)
+    scale = 1.0 / Dqk ** 0.5
+    kv_t = torch.tensor(kv, dtype=torch.int32, device=dev)
+    _, lses = cuda_lib.sparse_attn_group([Q], [K], None, idx, scale, kv_len=kv_t, Dv=Dv,
+                                         want_lse=True)
+    cuda_lib.device_status()
+    ref = oracle.index_kl([Q.reshape(B * T, Hh, Dqk).cpu()], [K.cpu()],
+                          idx.reshape(B * T, topk).cpu(), torch.zeros(B * T, topk), scale, T,
+                          np.arange(B * T), kv_len=torch.tensor(kv))
+    got = lses[0].reshape(B * T, Hh).cpu().double().numpy()
+    finite = np.isfinite(ref["lse"][0])
+    assert np.array_equal(np.isfinite(got), finite)
+    np.testing.assert_allclose(got[finite], ref["lse"][0][finite], rtol=0, atol=2e-3)
+
+
+def test_full_size_sampled_rows(cuda_lib):
+    # full sizes in the benchmark's launch configuration (152 persistent CTAs, one group of
+    # 4 layers, k = 2048 over a 131072-key cache), here the last 4096 query rows of the
+    # prefill; the oracle on sampled rows
+    B, T, S, topk, G = 1, 4096, 131072, 2048, 4
+    dev = "cuda"
+    qs, ks = _inputs(B, T, S, G, 5150, dev)
+    g = torch.Generator(device=dev).manual_seed(5151)
+    idx = torch.empty((B, T, topk), dtype=torch.int32, device=dev)
+    pos = torch.arange(S, device=dev)
+    for r0 in range(0, T, 512):  # distinct causal positions: top-k of random keys
+        r1 = min(T, r0 + 512)
+        p = (S - T + torch.arange(r0, r1, device=dev))[:, None]
+        u = torch.rand((r1 - r0, S), generator=g, device=dev).masked_fill(pos[None] > p, -1.0)
+        idx[0, r0:r1] = u.topk(topk, dim=1).indices.to(torch.int32)
+    sc = _scores(idx, 5152, dev)
+    scale = 1.0 / D ** 0.5
+    _, lses = cuda_lib.sparse_attn_group(qs, [k.view(B, S, 1, D) for k in ks], None, idx, scale,
+                                         Dv=512, want_lse=True)
+    loss, grad, pbar = cuda_lib.index_kl(qs, ks, lses, idx, sc, scale, want_grad=True,
+                                         want_pbar=True)
+    cuda_lib.device_status()
+    rows = np.array([0, 1, 1000, 2047, 3001, 4095])
+    lse_rows = np.stack([l.reshape(T, H).cpu().double().numpy()[rows] for l in lses])
+    ref = _oracle(qs, ks, idx, sc, scale, None, rows=rows, lse=lse_rows)
+    _check(loss, grad, pbar, ref, rows, 2e-4, 5e-4)
+    np.testing.assert_allclose(lse_rows, ref["lse"], rtol=0, atol=2e-3)
+    # properties at every row: pbar sums to one (up to the attention's lse), loss >= 0
+    sums = pbar.reshape(T, topk).double().sum(1).cpu().numpy()
+    assert np.all(np.abs(sums - 1) < 5e-3)
+    assert float(loss.min()) >= -1e-4

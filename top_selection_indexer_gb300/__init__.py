@@ -26,7 +26,7 @@ EXPORTS = ("tsi_indexer_topk_workspace", "tsi_indexer_topk", "tsi_sparse_attn_wo
            "tsi_launch_count", "tsi_indexer_topk_noalloc", "tsi_indexer_topk_noalloc_limit",
            "tsi_indexer_topk_path", "tsi_sparse_attn_path", "tsi_index_share_layers",
            "tsi_topk_overlap", "tsi_indexer_topk_shard_workspace", "tsi_indexer_topk_shard",
-           "tsi_topk_merge")
+           "tsi_topk_merge", "tsi_sparse_attn_group_lse", "tsi_index_kl")
 
 
 class TSIError(RuntimeError):
@@ -84,6 +84,13 @@ def load():
             lib.tsi_indexer_topk_shard.restype = i32
             lib.tsi_topk_merge.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp]
             lib.tsi_topk_merge.restype = i32
+            lib.tsi_sparse_attn_group_lse.argtypes = [i32, vp, vp, vp, i32, i32, i32, i32, i32,
+                                                      i32, i32, f32, vp, i32, vp, vp, vp, vp, sz,
+                                                      vp]
+            lib.tsi_sparse_attn_group_lse.restype = i32
+            lib.tsi_index_kl.argtypes = [i32, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp, vp,
+                                         i32, vp, vp, vp, vp, vp]
+            lib.tsi_index_kl.restype = i32
             _lib = lib
     return _lib
 
@@ -178,12 +185,13 @@ def sparse_attn_workspace(B, T, S, H, Hkv, Dqk, Dv, topk) -> int:
 
 
 def sparse_attn_group(qs, ks, vs, idx, scale, kv_len=None, outs=None, workspace=None,
-                      stream=None, Dv=None):
+                      stream=None, Dv=None, want_lse=False, lses=None):
     """Sparse attention of every layer of one IndexShare group over the shared ``idx``.
 
     qs: list of Q [B,T,H,Dqk] bf16; ks: list of K [B,S,Hkv,Dqk] bf16; vs: list of
     V [B,S,Hkv,Dv] bf16, or None (value = first ``Dv`` dims of K).  Returns the
-    list of O [B,T,H,Dv] bf16.
+    list of O [B,T,H,Dv] bf16; with ``want_lse`` (or ``lses`` given) also the list of
+    per-head log-partitions [B,T,H] fp32 (tsi_sparse_attn_group_lse).
     """
     import torch
 
@@ -211,11 +219,73 @@ def sparse_attn_group(qs, ks, vs, idx, scale, kv_len=None, outs=None, workspace=
     kp = P(*[_dev(t, "k") for t in ks])
     vp = P(*[_dev(t, "v") for t in vs]) if vs is not None else None
     op = P(*[_dev(t, "out") for t in outs])
+    if want_lse or lses is not None:
+        if lses is None:
+            lses = [torch.empty((B, T, H), dtype=torch.float32, device=qs[0].device)
+                    for _ in range(n)]
+        for t in lses:
+            if t.dtype != torch.float32:
+                raise TypeError("lse tensors must be float32")
+        lp = P(*[_dev(t, "lse") for t in lses])
+        _check(load().tsi_sparse_attn_group_lse(
+            n, qp, kp, vp, B, T, S, H, Hkv, Dqk, Dv, float(scale), _dev(idx, "idx"), topk,
+            _dev(kv_len, "kv_len"), op, lp, _dev(workspace, "workspace"), ws_bytes,
+            _stream_handle(stream)))
+        return outs, lses
     _check(load().tsi_sparse_attn_group(
         n, qp, kp, vp, B, T, S, H, Hkv, Dqk, Dv, float(scale), _dev(idx, "idx"), topk,
         _dev(kv_len, "kv_len"), op, _dev(workspace, "workspace"), ws_bytes,
         _stream_handle(stream)))
     return outs
+
+
+def index_kl(qs, ks, lses, idx, score, scale, kv_len=None, want_grad=False, want_pbar=False,
+             loss=None, grad=None, pbar=None, stream=None):
+    """Group-centroid KL target of the Full layer's indexer over the group's layers
+    (tsi_index_kl).
+
+    qs: list of Q [B,T,64,576] bf16 (Full layer first); ks: list of latent caches
+    [B,S,576] or [B,S,1,576] bf16; lses: the layers' [B,T,64] fp32 log-partitions
+    (``sparse_attn_group(..., want_lse=True)``); idx [B,T,topk] int32 the shared index
+    rows; score [B,T,topk] fp32 the indexer scores of those entries.  Returns loss [B,T]
+    fp32, followed by grad and / or pbar [B,T,topk] fp32 when asked for.
+    """
+    import torch
+
+    n = len(qs)
+    B, T, H, Dqk = qs[0].shape
+    S = ks[0].shape[1]
+    topk = idx.shape[-1]
+    dev = qs[0].device
+    for name, lst, dt in (("q", qs, torch.bfloat16), ("k", ks, torch.bfloat16),
+                          ("lse", lses, torch.float32)):
+        if len(lst) != n:
+            raise ValueError(f"{name}: {len(lst)} tensors for {n} layers")
+        for t in lst:
+            if t.dtype != dt:
+                raise TypeError(f"{name} tensors must be {dt}")
+    if score.dtype != torch.float32:
+        raise TypeError("score must be float32")
+    if loss is None:
+        loss = torch.empty((B, T), dtype=torch.float32, device=dev)
+    if want_grad and grad is None:
+        grad = torch.empty((B, T, topk), dtype=torch.float32, device=dev)
+    if want_pbar and pbar is None:
+        pbar = torch.empty((B, T, topk), dtype=torch.float32, device=dev)
+    P = ctypes.c_void_p * n
+    qp = P(*[_dev(t, "q") for t in qs])
+    kp = P(*[_dev(t, "k") for t in ks])
+    lp = P(*[_dev(t, "lse") for t in lses])
+    _check(load().tsi_index_kl(
+        n, qp, kp, lp, B, T, S, H, Dqk, float(scale), _dev(idx, "idx"), _dev(score, "score"),
+        topk, _dev(kv_len, "kv_len"), _dev(loss, "loss"), _dev(grad, "grad"),
+        _dev(pbar, "pbar"), _stream_handle(stream)))
+    out = (loss,)
+    if want_grad or grad is not None:
+        out += (grad,)
+    if want_pbar or pbar is not None:
+        out += (pbar,)
+    return out[0] if len(out) == 1 else out
 
 
 def device_status(stream=None):

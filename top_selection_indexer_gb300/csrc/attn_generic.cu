@@ -85,6 +85,8 @@ __global__ void __launch_bounds__(kWarps * 32) attn_generic_kernel(AttnArgs a, i
             const int d = lane + 32 * i;
             if (d < a.Dv) o[d] = __float2bfloat16_rn(acc[i] * inv);
         }
+        if (a.lse && lane == 0)
+            a.lse[static_cast<int64_t>(row) * a.H + h] = lse_of(m, l);
     } else {
         const int64_t slot = (static_cast<int64_t>(row) * n_splits + split) * a.H + h;
         float* po = part_o + slot * a.Dv;
@@ -117,6 +119,7 @@ __global__ void attn_combine_kernel(AttnArgs a, int n_splits, const float* part_
         if (l > 0.f) L += l * exp2f(part_ml[2 * slot] - M);
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
+    if (a.lse && threadIdx.x == 0) a.lse[static_cast<int64_t>(row) * a.H + h] = lse_of(M, L);
     __nv_bfloat16* o = static_cast<__nv_bfloat16*>(a.out) +
                        (static_cast<int64_t>(row) * a.H + h) * a.Dv;
     for (int d = threadIdx.x; d < a.Dv; d += blockDim.x) {

@@ -17,6 +17,7 @@ struct AttnArgs {
     const int32_t* kv_len;
     void* out;  // [B,T,H,Dv] bf16
     unsigned* err;
+    float* lse = nullptr;  // [B,T,H] fp32 or nullptr: ln sum_s exp(scale * Q.K) (-inf: no key)
 };
 
 bool attn_generic_supported(int H, int Hkv, int Dqk, int Dv, bool v_from_k);

@@ -38,6 +38,7 @@
 #include <cudaTypedefs.h>
 
 #include "kernels_tc.cuh"
+#include "latent_gather.cuh"
 #include "tc_common.cuh"
 #include "topk_select.cuh"
 
@@ -50,6 +51,9 @@ constexpr int kDqk = 576;
 constexpr int kDv = 512;
 constexpr int kChunks = kDqk / 64;  // 9 chunks of 64 dims (128 bytes) per latent row
 constexpr int kKVChunkBytes = kKeys * 128;
+static_assert(kKeys == latent::kKeys && kChunks == latent::kChunks &&
+                  kKVChunkBytes == latent::kChunkBytes && kDqk == latent::kDqk,
+              "the gather helper fills the tiles this kernel multiplies");
 constexpr int kQChunkBytes = kHeads * 128;
 constexpr int kPSlot = 8;  // the RoPE chunk's slot holds P^T once S^T is done
 // 16 warps: warp 4 issues the MMAs; the other 15 gather.  Warps 0..3 and 8..11 also run
@@ -85,6 +89,7 @@ struct AttnTcParams {
     int tiles_per_row, n_splits, tiles_per_split, n_units;
     float scale_log2;
     unsigned* err;
+    float* lse;  // [B*T, 64] or nullptr (unsplit rows; split rows get it from the combine)
 };
 
 struct Work {
@@ -114,39 +119,15 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     return lo | (hi << 16);
 }
 
-// This thread's share of the gather of key tile t of work item W: a chunk is 128 keys x 8
-// pieces of 16 bytes, and gather thread g copies pieces g, g + kGather, g + 2 kGather of
-// every chunk, each chunk as soon as the MMA has released its slot (ring phase it).
+// This thread's share of the gather of key tile t of work item W (the latent rows of the
+// row's selected keys, zero-filled past kv_len and past topk).
 __device__ __forceinline__ void gather_tile(const AttnTcParams& p, const Work& W, int t, int it,
                                             int g, uint32_t kv_addr, uint64_t* kv_empty,
                                             uint64_t* kv_full, volatile int* abort) {
-    const int64_t len = seq_len(p.kv_len, W.b, p.S);
-    const int32_t* irow = p.idx + static_cast<int64_t>(W.row) * p.topk;
-    const uint16_t* src[3];
-    uint32_t nbytes[3];
-    uint32_t dst0[3];
-#pragma unroll
-    for (int j = 0; j < 3; ++j) {
-        const int piece = g + kGather * j;
-        const int k = (piece >> 3) & (kKeys - 1);
-        const int sub = piece & 7;
-        const int e = t * kKeys + k;
-        const int s = (piece < kKeys * 8 && e < p.topk) ? irow[e] : -1;
-        const bool ok = s >= 0 && s < len;
-        src[j] = ok ? p.k + (static_cast<int64_t>(W.b) * p.S + s) * kDqk + sub * 8 : p.k;
-        nbytes[j] = ok ? 16u : 0u;
-        dst0[j] = kv_addr + (k >> 3) * 1024 + (k & 7) * 128 + ((sub ^ (k & 7)) << 4);
-    }
-    for (int c = 0; c < kChunks; ++c) {
-        tc::mbar_wait(&kv_empty[c], (it & 1) ^ 1, abort, p.err);
-#pragma unroll
-        for (int j = 0; j < 3; ++j) {
-            if (g + kGather * j < kKeys * 8)
-                tc::cp_async16(dst0[j] + c * kKVChunkBytes, src[j] + (nbytes[j] ? c * 64 : 0),
-                               nbytes[j]);
-        }
-        tc::cp_async_arrive_noinc(&kv_full[c]);
-    }
+    latent::gather_tile<kGather>(p.k + static_cast<int64_t>(W.b) * p.S * kDqk,
+                                 seq_len(p.kv_len, W.b, p.S),
+                                 p.idx + static_cast<int64_t>(W.row) * p.topk, p.topk, t, it, g,
+                                 kv_addr, kv_empty, kv_full, abort, p.err);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -417,6 +398,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         p.part_ml[2 * slot] = m_s[st];
                         p.part_ml[2 * slot + 1] = l_s[st];
                     }
+                } else if (p.lse) {
+                    named_bar(kSoftBar, kSoftThreads);
+                    if (st < 64) p.lse[static_cast<int64_t>(W.row) * kHeads + st] = lse_of(m_s[st], l_s[st]);
                 }
                 tc::tc_fence_before();
                 tc::mbar_arrive(o_empty);
@@ -517,6 +501,7 @@ cudaError_t launch_attn_tc(const AttnArgs& a, void* workspace, cudaStream_t st) 
     p.n_units = rows * p.n_splits;
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.err = a.err;
+    p.lse = a.lse;
     if (p.n_splits > 1) {
         p.part_o = static_cast<float*>(workspace);
         p.part_ml = p.part_o + static_cast<size_t>(rows) * p.n_splits * kHeads * kDv;

@@ -21,4 +21,26 @@ bool tc_attn_supported(int H, int Hkv, int Dqk, int Dv, bool v_from_k);
 size_t tc_attn_workspace_bytes(int B, int T, int H, int Dv, int topk);
 cudaError_t launch_attn_tc(const AttnArgs& a, void* workspace, cudaStream_t st);
 
+// Group-centroid KL target of a Full layer's indexer over the group's layers (H = 64,
+// Dqk = 576 latent keys), from the layers' queries, keys and attention log-partitions.
+constexpr int kMaxIndexKlLayers = 8;
+struct IndexKlArgs {
+    int n_layers;
+    const void* const* q;  // [n_layers] of [B,T,64,576] bf16
+    const void* const* k;  // [n_layers] of [B,S,576] bf16
+    const float* const* lse;  // [n_layers] of [B,T,64] fp32
+    int B, T, S;
+    float scale;
+    const int32_t* idx;  // [B,T,topk]
+    const float* score;  // [B,T,topk]
+    int topk;
+    const int32_t* kv_len;
+    float* loss;  // [B,T]
+    float* grad;  // [B,T,topk] or nullptr
+    float* pbar;  // [B,T,topk] or nullptr
+    unsigned* err;
+};
+bool tc_index_kl_supported(int H, int Dqk);
+cudaError_t launch_index_kl_tc(const IndexKlArgs& a, cudaStream_t st);
+
 }  // namespace tsi

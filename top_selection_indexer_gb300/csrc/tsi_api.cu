@@ -233,6 +233,16 @@ tsi_status tsi_sparse_attn_group(int n_layers, const void* const* q, const void*
                                  int Dqk, int Dv, float scale, const int32_t* idx, int topk,
                                  const int32_t* kv_len, void* const* out, void* workspace,
                                  size_t workspace_bytes, void* stream) {
+    return tsi_sparse_attn_group_lse(n_layers, q, k, v, B, T, S, H, Hkv, Dqk, Dv, scale, idx,
+                                     topk, kv_len, out, nullptr, workspace, workspace_bytes,
+                                     stream);
+}
+
+tsi_status tsi_sparse_attn_group_lse(int n_layers, const void* const* q, const void* const* k,
+                                     const void* const* v, int B, int T, int S, int H, int Hkv,
+                                     int Dqk, int Dv, float scale, const int32_t* idx, int topk,
+                                     const int32_t* kv_len, void* const* out, float* const* lse,
+                                     void* workspace, size_t workspace_bytes, void* stream) {
     if (n_layers < 0) return fail(TSI_ERR_INVALID_ARG, "n_layers=%d", n_layers);
     if (B < 0 || T < 0 || S < 0)
         return fail(TSI_ERR_INVALID_ARG, "negative size (B=%d T=%d S=%d)", B, T, S);
@@ -255,6 +265,8 @@ tsi_status tsi_sparse_attn_group(int n_layers, const void* const* q, const void*
             return fail(TSI_ERR_INVALID_ARG, "layer %d: NULL tensor pointer", l);
         if (!aligned16(q[l]) || !aligned16(k[l]) || !aligned16(vl) || !aligned16(out[l]))
             return fail(TSI_ERR_INVALID_ARG, "layer %d: pointers must be 16-byte aligned", l);
+        if (lse && !aligned16(lse[l]))
+            return fail(TSI_ERR_INVALID_ARG, "layer %d: lse must be 16-byte aligned", l);
         if (!use_tc_attn(H, Hkv, Dqk, Dv, vk) && !tsi::attn_generic_supported(H, Hkv, Dqk, Dv, vk))
             return fail(TSI_ERR_UNSUPPORTED, "H=%d Hkv=%d Dqk=%d Dv=%d%s unsupported (Dqk<=576, "
                         "Dv<=512)", H, Hkv, Dqk, Dv, vk ? " (value from key)" : "");
@@ -271,13 +283,52 @@ tsi_status tsi_sparse_attn_group(int n_layers, const void* const* q, const void*
     for (int l = 0; l < n_layers; ++l) {
         const void* vl = v ? v[l] : nullptr;
         tsi::AttnArgs a{q[l], k[l], vl, B, T, S, H, Hkv, Dqk, Dv, scale, idx, topk, kv_len,
-                        out[l], err};
+                        out[l], err, lse ? lse[l] : nullptr};
         cudaError_t e = use_tc_attn(H, Hkv, Dqk, Dv, vl == nullptr)
                             ? tsi::launch_attn_tc(a, workspace, s)
                             : tsi::launch_attn_generic(a, workspace, s);
         if (e != cudaSuccess)
             return fail(TSI_ERR_CUDA, "attention launch (layer %d): %s", l, cudaGetErrorString(e));
     }
+    return ok();
+}
+
+tsi_status tsi_index_kl(int n_layers, const void* const* q, const void* const* k,
+                        const float* const* lse, int B, int T, int S, int H, int Dqk, float scale,
+                        const int32_t* idx, const float* score, int topk, const int32_t* kv_len,
+                        float* loss, float* grad, float* pbar, void* stream) {
+    if (n_layers < 1 || n_layers > tsi::kMaxIndexKlLayers)
+        return fail(TSI_ERR_INVALID_ARG, "n_layers=%d outside [1, %d]", n_layers,
+                    tsi::kMaxIndexKlLayers);
+    if (B < 0 || T < 0 || S < 0)
+        return fail(TSI_ERR_INVALID_ARG, "negative size (B=%d T=%d S=%d)", B, T, S);
+    if (topk < 1 || topk > TSI_MAX_TOPK)
+        return fail(TSI_ERR_UNSUPPORTED, "topk=%d outside [1, %d]", topk, TSI_MAX_TOPK);
+    if (!tsi::tc_index_kl_supported(H, Dqk))
+        return fail(TSI_ERR_UNSUPPORTED, "H=%d Dqk=%d unsupported (64 heads over the 576-d latent)",
+                    H, Dqk);
+    if (!std::isfinite(scale)) return fail(TSI_ERR_INVALID_ARG, "scale is not finite");
+    if (static_cast<int64_t>(B) * T * H > (1ll << 31) - 1 || static_cast<int64_t>(B) * S > (1ll << 31) - 1)
+        return fail(TSI_ERR_UNSUPPORTED, "B*T*H or B*S exceeds 2^31-1");
+    if (B == 0 || T == 0) return ok();
+    if (!q || !k || !lse || !idx || !score || !loss)
+        return fail(TSI_ERR_INVALID_ARG, "NULL pointer (q, k, lse, idx, score and loss are required)");
+    if (!aligned16(idx) || !aligned16(score) || !aligned16(kv_len) || !aligned16(loss) ||
+        !aligned16(grad) || !aligned16(pbar))
+        return fail(TSI_ERR_INVALID_ARG, "idx / score / kv_len / loss / grad / pbar must be 16-byte aligned");
+    for (int l = 0; l < n_layers; ++l) {
+        if (!q[l] || !lse[l] || (S > 0 && !k[l]))
+            return fail(TSI_ERR_INVALID_ARG, "layer %d: NULL tensor pointer", l);
+        if (!aligned16(q[l]) || !aligned16(k[l]) || !aligned16(lse[l]))
+            return fail(TSI_ERR_INVALID_ARG, "layer %d: pointers must be 16-byte aligned", l);
+    }
+    unsigned* err = nullptr;
+    tsi_status st = device_error_word(&err);
+    if (st != TSI_OK) return st;
+    tsi::IndexKlArgs a{n_layers, q, k, lse, B, T, S, scale, idx, score, topk, kv_len,
+                       loss, grad, pbar, err};
+    cudaError_t e = tsi::launch_index_kl_tc(a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(TSI_ERR_CUDA, "index KL launch: %s", cudaGetErrorString(e));
     return ok();
 }
 

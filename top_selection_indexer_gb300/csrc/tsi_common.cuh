@@ -44,6 +44,12 @@ __device__ __forceinline__ int64_t seq_len(const int32_t* kv_len, int b, int S) 
     return len < 0 ? 0 : (len > S ? S : len);
 }
 
+// ln sum_s exp(x_s) from the base-2 running maximum m (of x_s * log2(e)) and the sum
+// l = sum_s 2^(x_s log2(e) - m) of an online softmax; -inf when nothing was summed.
+__device__ __forceinline__ float lse_of(float m, float l) {
+    return l > 0.f ? (m + log2f(l)) * 0.69314718055994531f : -__int_as_float(0x7f800000);
+}
+
 // Counts kernel launches made by the library (reported by tsi_launch_count).
 void note_launches(int n);
 
