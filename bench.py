@@ -283,6 +283,8 @@ def run_gpu(args, rank, world):
         result["overlap"] = measure_overlap(cfg, ind, idx, ws, stream)
     if not args.no_cp:
         result["context_parallel"] = measure_cp(cfg, ind, idx, stream)
+    if not args.no_kl and tsi.attn_path(cfg.H, cfg.Hkv, cfg.Dqk, cfg.Dv, cfg.v_from_k) == 1:
+        result["index_kl"] = measure_index_kl(cfg, ind, lay, idx, outs, ws, stream)
 
     # --- end to end through the C ABI with host buffers ---------------------------------
     if not args.no_e2e:
@@ -392,6 +394,59 @@ def measure_overlap(cfg, ind, idx, ws, stream, reps=5):
     return {"layers": "Full layers of groups 0 and 1", "rows": rows, "ms_per_launch": round(ms, 4),
             "achieved_gbs": round(nbytes / (ms / 1e3) / 1e9, 1),
             "algorithmic_bytes_per_launch": nbytes, "mean_overlap_rate": round(rate, 5)}
+
+
+def measure_index_kl(cfg, ind, lay, idx, outs, ws, stream, reps=2):
+    """Group-centroid KL target of group 0's Full-layer indexer over every query row: the
+    indexer's scores and each layer's attention with its log-partition are computed first
+    (untimed), then tsi_index_kl (loss and gradient) is timed on its own."""
+    import torch
+
+    import top_selection_indexer_gb300 as tsi
+    from top_selection_indexer_gb300 import accounting
+
+    qI, kI, w = ind[0]
+    dev = idx.device
+    score = torch.empty(idx.shape, dtype=torch.float32, device=dev)
+    tsi.indexer_topk(qI, kI, w, cfg.topk, idx=idx, score=score, workspace=ws, stream=stream)
+    layers = lay[:cfg.group]
+    qs = [Q for Q, _, _ in layers]
+    ks = [K for _, K, _ in layers]
+    lses = [torch.empty((cfg.B, cfg.T, cfg.H), dtype=torch.float32, device=dev)
+            for _ in layers]
+    tsi.sparse_attn_group(qs, ks, None, idx, cfg.scale, outs=outs[:len(layers)], workspace=ws,
+                          stream=stream, Dv=cfg.Dv, lses=lses)
+    loss = torch.empty((cfg.B, cfg.T), dtype=torch.float32, device=dev)
+    grad = torch.empty(idx.shape, dtype=torch.float32, device=dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(reps)]
+    for r in range(reps + 1):  # the first call warms up
+        if r:
+            ev[r - 1][0].record(stream)
+        tsi.index_kl(qs, ks, lses, idx, score, cfg.scale, loss=loss, grad=grad, stream=stream)
+        if r:
+            ev[r - 1][1].record(stream)
+    tsi.device_status(stream)
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    rows = cfg.B * cfg.T
+    valid_k = accounting.selected_pairs(cfg.B, cfg.T, cfg.S, cfg.topk)
+    nbytes = accounting.index_kl_bytes(valid_k, rows, len(layers), cfg.H, cfg.Dqk, cfg.topk)
+    flops = accounting.index_kl_flops(valid_k, len(layers), cfg.H, cfg.Dqk)
+    peaks = _peaks()
+    achieved = nbytes / (ms / 1e3) / 1e9
+    kernel = "tsi_index_kl_tc_kernel"
+    return {"layers": f"group 0: 1 Full + {len(layers) - 1} Shared", "rows": rows,
+            "outputs": "loss and gradient per row", "ms_per_launch": round(ms, 3),
+            "rows_per_s": round(rows / (ms / 1e3), 1),
+            "mean_loss": round(float(loss.double().mean().item()), 6),
+            "roofline": {"kernel": kernel, "bound": "hbm", "achieved": round(achieved, 1),
+                         "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(achieved / peaks["hbm_gbs"], 4),
+                         "traffic": _profiled_traffic(kernel, ["index_kl_tc.cu",
+                                                               "latent_gather.cuh"]),
+                         "algorithmic_bytes_per_launch": nbytes,
+                         "tc_tflops": round(flops / (ms / 1e3) / 1e12, 1),
+                         "peak_source": f"{peaks['source']} hbm_gbs"}}
 
 
 def run_e2e(args, cfg, ind, lay, idx, outs, ws, stream, world):
@@ -599,6 +654,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-cp", action="store_true",
                     help="skip the context-parallel indexer measurement after the timed steps")
+    ap.add_argument("--no-kl", action="store_true",
+                    help="skip the group-centroid KL measurement")
     ap.add_argument("--no-overlap", action="store_true",
                     help="skip the cross-layer top-k overlap measurement after the timed steps")
     ap.add_argument("--tail-rows", type=int, default=0,

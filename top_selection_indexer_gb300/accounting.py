@@ -86,3 +86,22 @@ def cost_dsa(N: int, L: int, k: int, C_I: float, C_A: float) -> float:
 def cost_indexshare(N: int, L: int, k: int, C_I: float, C_A: float, r: float) -> float:
     """Prefill cost model with IndexShare (Full-layer ratio r): r N C_I L^2 + N C_A L k."""
     return r * N * C_I * L * L + N * C_A * L * k
+
+
+def index_kl_bytes(valid_k: int, rows: int, n_layers: int, H: int, Dqk: int, topk: int,
+                   grad: bool = True, pbar: bool = False, elem: int = 2) -> int:
+    """Algorithmic bytes of the group-centroid KL target over one group of n_layers layers
+    ("GLM-5.2 技术报告速览" §IndexShare: pbar_t = 1/(m+1) sum_j p^(l+j)_t).
+
+    Per layer every selected key row (Dqk elements) is gathered once per query row and the
+    row's queries (H x Dqk) and log-partitions (H fp32) are read once; the index row and its
+    scores are read once, the loss (and the gradient / centroid rows) written once.
+    """
+    per_layer = valid_k * Dqk * elem + rows * H * Dqk * elem + rows * H * 4
+    outs = rows * 4 + (rows * topk * 4 if grad else 0) + (rows * topk * 4 if pbar else 0)
+    return n_layers * per_layer + rows * topk * 8 + outs
+
+
+def index_kl_flops(valid_k: int, n_layers: int, H: int, Dqk: int) -> int:
+    """Tensor-core FLOPs of the recomputed logits: 2 * Dqk per (selected key, head, layer)."""
+    return 2 * valid_k * H * Dqk * n_layers
