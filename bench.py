@@ -234,7 +234,8 @@ def run_gpu(args, rank, world):
     roof_attn = {"kernel": attn_kernel, "bound": "hbm", "achieved": round(attn_achieved, 1),
                  "peak": peaks["hbm_gbs"], "unit": "GB/s",
                  "frac": round(attn_achieved / peaks["hbm_gbs"], 4),
-                 "traffic": _profiled_traffic(attn_kernel, ["attn_tc.cu", "attn_generic.cu"]),
+                 "traffic": _profiled_traffic(attn_kernel, ["attn_tc.cu", "attn_generic.cu",
+                                                             "latent_gather.cuh"]),
                  "algorithmic_bytes_per_launch": attn_bytes, "ms_per_launch": round(ms_attn, 4),
                  "tc_tflops": round(attn_tc, 1),
                  "peak_source": f"{peaks['source']} hbm_gbs"}
