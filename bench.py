@@ -247,6 +247,17 @@ def run_gpu(args, rank, world):
                 "algorithmic_flops_per_launch": idx_flops, "ms_per_launch": round(ms_idx, 4),
                 "peak_source": f"{peaks['source']} bf16 sustained x {FP8_PER_BF16:g} (fp8)"
                                if cfg.qk_dtype == "e4m3" else f"{peaks['source']} bf16 sustained"}
+    if cfg.T == 1:
+        # decode: one query per sequence scans its whole key cache once -- HBM-bound
+        idx_bytes = accounting.indexer_bytes(rows, cfg.B * cfg.S, cfg.H_I, cfg.d_I, qk_bytes,
+                                             2 if cfg.w_dtype == "bf16" else 4, cfg.topk)
+        idx_gbs = idx_bytes / (ms_idx / 1e3) / 1e9
+        roof_idx = {"kernel": idx_kernel, "bound": "hbm", "achieved": round(idx_gbs, 1),
+                    "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": round(idx_gbs / peaks["hbm_gbs"], 4), "traffic": None,
+                    "algorithmic_bytes_per_launch": idx_bytes, "ms_per_launch": round(ms_idx, 4),
+                    "tc_tflops": round(idx_flops / (ms_idx / 1e3) / 1e12, 2),
+                    "peak_source": f"{peaks['source']} hbm_gbs"}
     dominant = roof_attn if ms_attn * cfg.n_layers >= ms_idx * G else roof_idx
 
     result = {
@@ -280,6 +291,8 @@ def run_gpu(args, rank, world):
                          "ms_later_step": round(ms_attn, 4),
                          "ms_draft_reusing_indices": round(ms_idx + n * ms_attn, 4),
                          "ms_draft_recomputing_indices": round(n * (ms_idx + ms_attn), 4)}
+    if cfg.T == 1:
+        result["decode_graph"] = measure_decode_graph(cfg, ind, lay, idx, outs, ws)
     if G >= 2 and not args.no_overlap:
         result["overlap"] = measure_overlap(cfg, ind, idx, ws, stream)
     if not args.no_cp:
@@ -395,6 +408,60 @@ def measure_overlap(cfg, ind, idx, ws, stream, reps=5):
     return {"layers": "Full layers of groups 0 and 1", "rows": rows, "ms_per_launch": round(ms, 4),
             "achieved_gbs": round(nbytes / (ms / 1e3) / 1e9, 1),
             "algorithmic_bytes_per_launch": nbytes, "mean_overlap_rate": round(rate, 5)}
+
+
+def measure_decode_graph(cfg, ind, lay, idx, outs, ws, reps=20):
+    """Latency of one IndexShare group of a decode step (the Full layer's indexer + top-k,
+    then the group's sparse attention layers) replayed from a CUDA graph, against the same
+    calls launched one by one."""
+    import torch
+
+    import top_selection_indexer_gb300 as tsi
+
+    qI, kI, w = ind[0]
+    layers = lay[:cfg.group]
+    qs = [Q for Q, _, _ in layers]
+    ks = [K for _, K, _ in layers]
+
+    def group_step(stream):
+        tsi.indexer_topk(qI, kI, w, cfg.topk, idx=idx, workspace=ws, stream=stream)
+        tsi.sparse_attn_group(qs, ks, None, idx, cfg.scale, outs=outs[:len(layers)],
+                              workspace=ws, stream=stream, Dv=cfg.Dv)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    n0 = tsi.launch_count()
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            group_step(side)
+    launches = (tsi.launch_count() - n0) // 3
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        group_step(side)
+    torch.cuda.synchronize()
+
+    def timed(fn):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(side):
+            for _ in range(3):
+                fn()
+            a.record(side)
+            for _ in range(reps):
+                fn()
+            b.record(side)
+        b.synchronize()
+        return a.elapsed_time(b) / reps * 1e3
+
+    us_graph = timed(graph.replay)
+    us_eager = timed(lambda: group_step(side))
+    tsi.device_status(side)
+    return {"what": f"one group of a decode step: indexer + top-k of the Full layer, then "
+                    f"{len(layers)} sparse-attention layers (B={cfg.B}, one query each)",
+            "kernel_launches": int(launches), "us_graph_replay": round(us_graph, 2),
+            "us_eager": round(us_eager, 2), "reps": reps}
 
 
 def measure_index_kl(cfg, ind, lay, idx, outs, ws, stream, reps=2):
