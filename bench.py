@@ -53,17 +53,26 @@ def _kernel_sources_sha(names):
     return h.hexdigest()[:16]
 
 
-def _profiled_traffic(kernel, src_files):
-    """DRAM bytes per launch from profiles/traffic.txt, if taken on the current source."""
+def _profiled_traffic(kernel, src_files, workload):
+    """DRAM bytes per launch from profiles/traffic.txt, if taken on the current source for
+    this workload (None otherwise)."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
-    if not os.path.exists(path):
+    if workload is None or not os.path.exists(path):
         return None
     sha = _kernel_sources_sha(src_files)
     for line in open(path):
         kv = dict(x.split("=", 1) for x in line.split() if "=" in x)
-        if kv.get("kernel") == kernel and kv.get("src_sha") == sha:
+        if kv.get("kernel") == kernel and kv.get("src_sha") == sha and \
+                kv.get("workload") == workload:
             return float(kv["bytes_per_launch"])
     return None
+
+
+def _traffic_workload(cfg, what):
+    """Name of a captured workload in profiles/traffic.txt: whole prefills of one sequence."""
+    if cfg.B != 1 or cfg.T != cfg.S:
+        return None
+    return f"prefill_L{cfg.S}_{what}"
 
 
 class ClockSampler:
@@ -235,7 +244,8 @@ def run_gpu(args, rank, world):
                  "peak": peaks["hbm_gbs"], "unit": "GB/s",
                  "frac": round(attn_achieved / peaks["hbm_gbs"], 4),
                  "traffic": _profiled_traffic(attn_kernel, ["attn_tc.cu", "attn_generic.cu",
-                                                             "latent_gather.cuh"]),
+                                                             "latent_gather.cuh"],
+                                              _traffic_workload(cfg, "layer")),
                  "algorithmic_bytes_per_launch": attn_bytes, "ms_per_launch": round(ms_attn, 4),
                  "tc_tflops": round(attn_tc, 1),
                  "peak_source": f"{peaks['source']} hbm_gbs"}
@@ -243,7 +253,8 @@ def run_gpu(args, rank, world):
                 "peak": round(tc_peak, 1), "unit": "TFLOP/s",
                 "frac": round(idx_achieved / tc_peak, 4),
                 "traffic": _profiled_traffic(idx_kernel, ["indexer_tc.cu", "indexer_generic.cu",
-                                                          "topk_select.cuh"]),
+                                                          "topk_select.cuh"],
+                                             _traffic_workload(cfg, "group")),
                 "algorithmic_flops_per_launch": idx_flops, "ms_per_launch": round(ms_idx, 4),
                 "peak_source": f"{peaks['source']} bf16 sustained x {FP8_PER_BF16:g} (fp8)"
                                if cfg.qk_dtype == "e4m3" else f"{peaks['source']} bf16 sustained"}
@@ -511,7 +522,8 @@ def measure_index_kl(cfg, ind, lay, idx, outs, ws, stream, reps=2):
                          "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": round(achieved / peaks["hbm_gbs"], 4),
                          "traffic": _profiled_traffic(kernel, ["index_kl_tc.cu",
-                                                               "latent_gather.cuh"]),
+                                                               "latent_gather.cuh"],
+                                                      _traffic_workload(cfg, "group_kl")),
                          "algorithmic_bytes_per_launch": nbytes,
                          "tc_tflops": round(flops / (ms / 1e3) / 1e12, 1),
                          "peak_source": f"{peaks['source']} hbm_gbs"}}

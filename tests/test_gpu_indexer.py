@@ -72,6 +72,14 @@ def test_decode_ragged_kv_len_integer_exact(cuda_lib):
                    exact=True, kv_len=[0, 1, 5, 2048, 2049, 40000])
 
 
+@pytest.mark.parametrize("B,kv", [(1, None), (2, [131072, 70001]), (8, None)])
+def test_decode_two_stage_merge_integer_exact(cuda_lib, B, kv):
+    # a long cache split into many key chunks (64 for one row, 19 per row for eight): the
+    # chunk lists are merged in groups of about sqrt(n) lists, then per row
+    _run_and_check(cuda_lib, B, 1, 131072, 64, 128, 2048, "e4m3", "bf16", "int8", "pow2",
+                   71 + B, exact=True, kv_len=kv)
+
+
 def test_decode_generic_heads_split_merge(cuda_lib):
     # few rows + long cache: keys split over blocks and merged (CUDA-core path)
     _run_and_check(cuda_lib, 4, 1, 30000, 4, 32, 512, "f32", "f32", "int4", "int03", 61,

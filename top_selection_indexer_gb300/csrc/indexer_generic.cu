@@ -259,6 +259,7 @@ __global__ void __launch_bounds__(kRankThreads) topk_rank_kernel(int topk, const
 // ------------------------------------------------------------------- split merge
 
 constexpr int kMaxSplits = 1024;  // candidate lists per row the merge accepts
+constexpr size_t kMaxStageBytes = 160 * 1024;  // candidates a merge block stages in smem
 
 // One block per row: the row's n_splits candidate lists (each the exact top-k of one key
 // range, unordered) -> the row's top k in rank order (or, with out_keys, as unordered keys
@@ -270,19 +271,31 @@ constexpr int kMaxSplits = 1024;  // candidate lists per row the merge accepts
 // k survivors are gathered into shared memory and ranked by rank_sort_write.
 template <int kMergeThreads>
 __global__ void __launch_bounds__(kMergeThreads) topk_split_merge_kernel(
-    int topk, int n_splits, const uint64_t* cand, int64_t row_stride, int64_t list_stride,
-    const int* cand_cnt, int64_t cnt_row, int64_t cnt_list, int32_t* idx, float* score,
-    uint64_t* out_keys, int* out_cnt, unsigned* err) {
+    int topk, int n_splits, int lists_per_group, const uint64_t* cand, int64_t row_stride,
+    int64_t list_stride, const int* cand_cnt, int64_t cnt_row, int64_t cnt_list, int32_t* idx,
+    float* score, uint64_t* out_keys, int* out_cnt, int staged, unsigned* err) {
+    // staged: the block's candidate slots are copied once into dynamic shared memory and
+    // every pass reads them there (empty slots hold 0, which no rank key equals: its low
+    // word is 0xFFFFFFFF - position)
+    extern __shared__ uint64_t stg[];
     __shared__ __align__(16) uint64_t xs[kRankN];
     __shared__ unsigned hist[256];
     __shared__ unsigned long long range[2];
     __shared__ int ctl[4];  // 0 digit, 1 above, 2 in-bin, 3 write cursor
     __shared__ int cnt_s[kMaxSplits];
     __shared__ int total_s;
-    const int row = blockIdx.x;
+    // output row v: lists first .. first + lists_per_group - 1 of input row `row` (a row's
+    // lists fall into ceil(n_splits / lists_per_group) groups, merged by separate blocks)
+    const int v = blockIdx.x;
+    const int n_groups = (n_splits + lists_per_group - 1) / lists_per_group;
+    const int row = v / n_groups;
+    const int first = (v - row * n_groups) * lists_per_group;
+    n_splits = n_splits - first < lists_per_group ? n_splits - first : lists_per_group;
     const int tid = threadIdx.x;
-    const uint64_t* rc = cand + static_cast<int64_t>(row) * row_stride;
-    const int* cc = cand_cnt + static_cast<int64_t>(row) * cnt_row;
+    const uint64_t* rc = cand + static_cast<int64_t>(row) * row_stride +
+                         static_cast<int64_t>(first) * list_stride;
+    const int* cc = cand_cnt + static_cast<int64_t>(row) * cnt_row +
+                    static_cast<int64_t>(first) * cnt_list;
     if (tid == 0) total_s = 0;
     __syncthreads();
     for (int sp = tid; sp < n_splits; sp += kMergeThreads) {
@@ -300,6 +313,14 @@ __global__ void __launch_bounds__(kMergeThreads) topk_split_merge_kernel(
     // so f may use warp collectives).  Slot s is entry s % topk of list s / topk; a pass
     // walks the slots four per thread at a time so that a thread's loads are independent.
     const int n_slots = n_splits * topk;
+    if (staged) {
+        for (int slot = tid; slot < n_slots; slot += kMergeThreads) {
+            const int sp = slot / topk;
+            const int j = slot - sp * topk;
+            stg[slot] = j < cnt_s[sp] ? rc[static_cast<int64_t>(sp) * list_stride + j] : 0ull;
+        }
+        __syncthreads();
+    }
     auto for_each = [&](auto f) {
         constexpr int U = 4;
         for (int base = 0; base < n_slots; base += U * kMergeThreads) {
@@ -308,10 +329,15 @@ __global__ void __launch_bounds__(kMergeThreads) topk_split_merge_kernel(
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int slot = base + u * kMergeThreads + tid;
-                const int sp = slot / topk;
-                const int j = slot - sp * topk;
-                ok[u] = slot < n_slots && j < cnt_s[sp < n_splits ? sp : 0];
-                x[u] = ok[u] ? rc[static_cast<int64_t>(sp) * list_stride + j] : 0ull;
+                if (staged) {
+                    x[u] = slot < n_slots ? stg[slot] : 0ull;
+                    ok[u] = x[u] != 0ull;
+                } else {
+                    const int sp = slot / topk;
+                    const int j = slot - sp * topk;
+                    ok[u] = slot < n_slots && j < cnt_s[sp < n_splits ? sp : 0];
+                    x[u] = ok[u] ? rc[static_cast<int64_t>(sp) * list_stride + j] : 0ull;
+                }
             }
 #pragma unroll
             for (int u = 0; u < U; ++u) f(x[u], ok[u]);
@@ -430,13 +456,13 @@ __global__ void __launch_bounds__(kMergeThreads) topk_split_merge_kernel(
     if (tid == 0 && ctl[3] != n) atomicOr(err, kErrAssert);
     if (out_keys) {  // the survivors themselves, unordered
         for (int i = tid; i < n; i += kMergeThreads)
-            out_keys[static_cast<int64_t>(row) * topk + i] = xs[i];
-        if (tid == 0) out_cnt[row] = n;
+            out_keys[static_cast<int64_t>(v) * topk + i] = xs[i];
+        if (tid == 0) out_cnt[v] = n;
         return;
     }
     if (tid < kRankThreads)
-        rank_sort_write(xs, n, topk, idx + static_cast<int64_t>(row) * topk,
-                        score ? score + static_cast<int64_t>(row) * topk : nullptr, tid, 1);
+        rank_sort_write(xs, n, topk, idx + static_cast<int64_t>(v) * topk,
+                        score ? score + static_cast<int64_t>(v) * topk : nullptr, tid, 1);
 }
 
 }  // namespace
@@ -462,19 +488,82 @@ cudaError_t launch_topk_merge_strided(int rows, int topk, int n_lists, const uin
                                       const int* cand_cnt, int64_t cnt_row, int64_t cnt_list,
                                       int32_t* idx, float* score, uint64_t* out_keys,
                                       int* out_cnt, unsigned* err, cudaStream_t st) {
+    return launch_topk_merge_grouped(rows, topk, n_lists, n_lists, cand, row_stride, list_stride,
+                                     cand_cnt, cnt_row, cnt_list, idx, score, out_keys, out_cnt,
+                                     err, st);
+}
+
+cudaError_t launch_topk_merge_grouped(int rows, int topk, int n_lists, int lists_per_group,
+                                      const uint64_t* cand, int64_t row_stride,
+                                      int64_t list_stride, const int* cand_cnt, int64_t cnt_row,
+                                      int64_t cnt_list, int32_t* idx, float* score,
+                                      uint64_t* out_keys, int* out_cnt, unsigned* err,
+                                      cudaStream_t st) {
     if (rows == 0) return cudaSuccess;
-    if (n_lists < 1 || n_lists > kMaxSplits) return cudaErrorInvalidValue;
-    // few rows (decode): wide blocks; many rows: several narrower blocks per SM
-    if (rows < 4 * 152)
-        topk_split_merge_kernel<1024><<<rows, 1024, 0, st>>>(
-            topk, n_lists, cand, row_stride, list_stride, cand_cnt, cnt_row, cnt_list, idx,
-            score, out_keys, out_cnt, err);
-    else
-        topk_split_merge_kernel<kRankThreads><<<rows, kRankThreads, 0, st>>>(
-            topk, n_lists, cand, row_stride, list_stride, cand_cnt, cnt_row, cnt_list, idx,
-            score, out_keys, out_cnt, err);
+    if (n_lists < 1 || n_lists > kMaxSplits || lists_per_group < 1) return cudaErrorInvalidValue;
+    const int groups = (n_lists + lists_per_group - 1) / lists_per_group;
+    if (groups > 1 && !out_keys) return cudaErrorInvalidValue;  // partial merges stay unordered
+    const int64_t blocks = static_cast<int64_t>(rows) * groups;
+    if (blocks > 0x7FFFFFFF) return cudaErrorInvalidValue;
+    // few blocks (decode): wide blocks, candidates staged in shared memory when they fit;
+    // many: several narrower blocks per SM reading the lists where they are
+    if (blocks < 4 * 152) {
+        const int per_block = (lists_per_group < n_lists ? lists_per_group : n_lists);
+        const size_t stage = static_cast<size_t>(per_block) * topk * sizeof(uint64_t);
+        const int staged = stage <= kMaxStageBytes ? 1 : 0;
+        if (staged) {
+            cudaError_t e = cudaFuncSetAttribute(topk_split_merge_kernel<1024>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 static_cast<int>(kMaxStageBytes));
+            if (e != cudaSuccess) return e;
+        }
+        topk_split_merge_kernel<1024><<<static_cast<int>(blocks), 1024, staged ? stage : 0, st>>>(
+            topk, n_lists, lists_per_group, cand, row_stride, list_stride, cand_cnt, cnt_row,
+            cnt_list, idx, score, out_keys, out_cnt, staged, err);
+    } else {
+        topk_split_merge_kernel<kRankThreads><<<static_cast<int>(blocks), kRankThreads, 0, st>>>(
+            topk, n_lists, lists_per_group, cand, row_stride, list_stride, cand_cnt, cnt_row,
+            cnt_list, idx, score, out_keys, out_cnt, 0, err);
+    }
     note_launches(1);
     return cudaGetLastError();
+}
+
+int topk_merge_group_size(int rows, int n_lists) {
+    if (n_lists < 8 || rows >= 152) return n_lists;  // one pass is parallel enough
+    int g = 1;
+    while (g * g < n_lists) ++g;  // about sqrt(n) lists per group, then about sqrt(n) groups
+    return g;
+}
+
+size_t topk_merge_stage_bytes(int rows, int topk, int n_lists) {
+    const int g = topk_merge_group_size(rows, n_lists);
+    if (g >= n_lists) return 0;
+    const size_t lists = static_cast<size_t>(rows) * ((n_lists + g - 1) / g);
+    return lists * topk * sizeof(uint64_t) + ((lists * sizeof(int) + 255) & ~size_t(255));
+}
+
+cudaError_t launch_topk_merge_two_stage(int rows, int topk, int n_lists, const uint64_t* cand,
+                                        int64_t row_stride, int64_t list_stride,
+                                        const int* cand_cnt, int64_t cnt_row, int64_t cnt_list,
+                                        void* stage, int32_t* idx, float* score,
+                                        uint64_t* out_keys, int* out_cnt, unsigned* err,
+                                        cudaStream_t st) {
+    const int g = topk_merge_group_size(rows, n_lists);
+    if (g >= n_lists || !stage)
+        return launch_topk_merge_strided(rows, topk, n_lists, cand, row_stride, list_stride,
+                                         cand_cnt, cnt_row, cnt_list, idx, score, out_keys,
+                                         out_cnt, err, st);
+    const int groups = (n_lists + g - 1) / g;
+    uint64_t* skeys = static_cast<uint64_t*>(stage);
+    int* scnt = reinterpret_cast<int*>(skeys + static_cast<size_t>(rows) * groups * topk);
+    cudaError_t e = launch_topk_merge_grouped(rows, topk, n_lists, g, cand, row_stride,
+                                              list_stride, cand_cnt, cnt_row, cnt_list, nullptr,
+                                              nullptr, skeys, scnt, err, st);
+    if (e != cudaSuccess) return e;
+    return launch_topk_merge_strided(rows, topk, groups, skeys,
+                                     static_cast<int64_t>(groups) * topk, topk, scnt, groups, 1,
+                                     idx, score, out_keys, out_cnt, err, st);
 }
 
 }  // namespace tsi

@@ -527,10 +527,13 @@ cudaError_t launch_qk(const IndexerArgs& a, void* workspace, cudaStream_t st) {
         return a.out_cand ? e
                           : launch_topk_rank(rows, a.topk, p.cand, p.cand_cnt, a.idx, a.score,
                                              a.err, st);
-    return launch_topk_merge_strided(rows, a.topk, p.n_chunks, p.cand,
-                                     static_cast<int64_t>(p.n_chunks) * a.topk, a.topk,
-                                     p.cand_cnt, p.n_chunks, 1, a.idx, a.score, a.out_cand,
-                                     a.out_cnt, a.err, st);
+    // decode: the chunk lists of few rows are merged in two stages (stage space after them)
+    void* stage = reinterpret_cast<uint8_t*>(p.cand_cnt) +
+                  ((static_cast<size_t>(rows) * p.n_chunks * sizeof(int) + 255) & ~size_t(255));
+    return launch_topk_merge_two_stage(rows, a.topk, p.n_chunks, p.cand,
+                                       static_cast<int64_t>(p.n_chunks) * a.topk, a.topk,
+                                       p.cand_cnt, p.n_chunks, 1, stage, a.idx, a.score,
+                                       a.out_cand, a.out_cnt, a.err, st);
 }
 
 }  // namespace
@@ -543,7 +546,8 @@ size_t tc_indexer_workspace_bytes(int qk_dtype, int B, int T, int S, int topk) {
     int nc, ck;
     tc_plan(qk_dtype, B, T, S, &nc, &ck);
     const size_t slots = static_cast<size_t>(B) * T * nc;
-    return slots * topk * sizeof(uint64_t) + ((slots * sizeof(int) + 255) & ~size_t(255));
+    return slots * topk * sizeof(uint64_t) + ((slots * sizeof(int) + 255) & ~size_t(255)) +
+           (nc > 1 ? topk_merge_stage_bytes(B * T, topk, nc) : 0);
 }
 
 size_t tc_indexer_split_workspace_bytes(int qk_dtype, int B, int T, int S, int topk) {
