@@ -7,76 +7,85 @@
 // layer's index set; "GLM 5.2: Built for Long Horizon Tasks" discussion §3: 576-d MLA
 // latent, 512 compressed + 64 RoPE dims, sparse attention over the indices).
 //
-// Both products are computed transposed so that the 128 gathered keys of a tile are the
-// MMA's M dimension and the 64 heads its N dimension:
-//   S^T[key, h] = K_tile . Q^T         (A = key rows, K-major; B = Q rows, K-major)
-//   O^T[d, h]  += V_tile^T . P^T       (A = the same key rows read MN-major as V^T,
-//                                       B = P^T written by the softmax threads)
-// O^T (512 x 64 fp32) lives in TMEM for the whole row; S^T takes 64 more columns.  One
-// softmax thread owns one key (one TMEM lane of S^T) and all 64 heads of it, so the
-// exponentials, the bf16 rounding of P and the running row sums need no cross-thread
-// traffic; the running max per head is refreshed only when a logit exceeds it by 2^16
-// (always on the first tile of a row), and then O^T is rescaled in place.
+// A row's keys are taken 64 at a time (a half-tile) through two 72 KB shared-memory
+// buffers, so the gather of the next half-tile runs while the current one is multiplied:
+//   S[h, key]   = Q . K_half^T          (M = 64 heads, N = 64 keys, K = 576; A = Q rows,
+//                                        B = the gathered key rows, both K-major)
+//   O^T[d, h]  += V_half^T . P^T        (M = 128 value dims x 4 blocks, N = 64 heads,
+//                                        K = 64 keys; A = the same key rows read MN-major
+//                                        as V^T, B = P^T written by the softmax threads)
+// O^T (512 x 64 fp32) lives in TMEM for the whole row; S takes 2 x 64 more columns (the
+// M = 64 accumulator puts head h on TMEM lane 32 (h / 16) + h % 16).  Four softmax threads
+// share a head (16 keys each), so the running max, the row sum of the bf16 probabilities
+// that multiply V and P^T's row need two shuffles and no shared memory.  The
+// running max is refreshed only when a logit exceeds it by 2^16 (always on a row's first
+// keys), and then O^T is rescaled in place.
 //
 // Roles of one persistent CTA (512 threads):
-//   warp 4        TMEM allocator + single-thread MMA issuer
-//   other warps   gather: 16-byte cp.async of the selected latent rows into nine 128-byte-
-//                 swizzled 64-dim chunk tiles (per-chunk mbarriers); warp 5 also loads Q
-//                 by TMA.  The gather rate of cp.async grows with the number of issuing
-//                 warps, so all 15 take part.
-//   warps 0..3,   softmax (writes P^T over the RoPE chunk once S^T is done) and the row
-//   8..11         epilogue (1/l normalisation, bf16 stores), heads 0..31 on warps 0..3 and
-//                 32..63 on warps 8..11: two warps per TMEM lane quadrant.  They gather
-//                 the next tile after writing P, when its chunks start to free up.
-// Row sums l[h] = sum_s P[h,s] come from the tensor core too: a fifth M=128 block
-// multiplies a 128-byte tile of ones (no-swizzle descriptor, zero strides: every core
-// matrix reads the same bytes) by P^T, so l sums exactly the bf16 P that multiplies V.
-// Few rows (decode): a row's key tiles are split over CTAs and the unnormalised partials
+//   warps 0..3    softmax (heads 16 w .. 16 w + 15, four threads per head, 16 keys each)
+//                 and the row epilogue (O^T's value dims); thread 0 also loads Q by TMA
+//   warp 4        TMEM allocator + issuer of the S products (one thread)
+//   warp 5        issuer of the P.V products (one thread): the two streams of tcgen05 work
+//                 wait on different inputs, so neither holds up the other
+//   warps 6..15   gather: 16-byte cp.async of the selected latent rows into the 128-byte-
+//                 swizzled chunks of a half-tile buffer, one mbarrier per buffer
+// Few rows (decode): a row's half-tiles are split over CTAs and the unnormalised partials
 // are merged by the combine kernel.
 #include <mutex>
 
 #include <cudaTypedefs.h>
 
 #include "kernels_tc.cuh"
-#include "latent_gather.cuh"
 #include "tc_common.cuh"
 #include "topk_select.cuh"
 
 namespace tsi {
 namespace {
 
-constexpr int kKeys = 128;  // keys per tile: MMA M of S^T, MMA K of O^T
-constexpr int kHeads = 64;  // MMA N
+constexpr int kHalf = 64;  // keys per half-tile: MMA N of S, MMA K of O^T
+constexpr int kHeads = 64;  // MMA M of S
 constexpr int kDqk = 576;
 constexpr int kDv = 512;
 constexpr int kChunks = kDqk / 64;  // 9 chunks of 64 dims (128 bytes) per latent row
-constexpr int kKVChunkBytes = kKeys * 128;
-static_assert(kKeys == latent::kKeys && kChunks == latent::kChunks &&
-                  kKVChunkBytes == latent::kChunkBytes && kDqk == latent::kDqk,
-              "the gather helper fills the tiles this kernel multiplies");
+constexpr int kChunkBytes = kHalf * 128;  // one chunk of a half-tile: 8 KB
+constexpr int kBufBytes = kChunks * kChunkBytes;  // one half-tile buffer: 72 KB
 constexpr int kQChunkBytes = kHeads * 128;
-constexpr int kPSlot = 8;  // the RoPE chunk's slot holds P^T once S^T is done
-// 16 warps: warp 4 issues the MMAs; the other 15 gather.  Warps 0..3 and 8..11 also run
-// the softmax and the row epilogue, warps 0..3 for heads 0..31 and 8..11 for heads
-// 32..63 of the keys in their TMEM lane quadrant (warp % 4).
+constexpr int kPSlot = 8;  // the RoPE chunk's slot holds P^T once S is done
 constexpr int kThreads = 512;
-constexpr int kMmaWarp = 4;
-constexpr int kGather = kThreads - 32;  // gathering threads (all but the MMA warp)
-constexpr int kGatherQ = 128;  // gather index of the thread that loads Q (warp 5, lane 0)
-constexpr int kSoftThreads = 256;
+constexpr int kSoftThreads = 128;  // warps 0..3
+constexpr int kMmaWarp = 4;  // issues S; also allocates TMEM
+constexpr int kPvWarp = 5;  // issues P.V
+constexpr int kGatherBase = 192;  // warp 6
+constexpr int kGather = kThreads - kGatherBase;  // 320
+constexpr int kPieces = kHalf * 8;  // 16-byte pieces per chunk of a half-tile
+constexpr int kGatherPer = (kPieces + kGather - 1) / kGather;  // 2
 constexpr int kSoftBar = 1;
-__device__ __forceinline__ bool is_softmax_warp(int w) { return (w & 4) == 0; }
 constexpr int kTmemCols = 512;
-constexpr int kColS = 0;
-constexpr int kColO = 64;  // O^T block m (d rows 128m..128m+127) at columns 64 + 64m
-constexpr int kColL = kColO + 256;  // row sums (every lane holds the same 64 values)
+constexpr int kColO = 0;  // O^T block m (value dims 128m .. 128m+127) at columns 64m
+constexpr int kColS = 256;  // S buffer b at columns 256 + 64b
 constexpr float kRescaleLog2 = 16.f;
-constexpr uint32_t kIdescS = tc::instr_desc(1, 128, 64, 0, 0);
-constexpr uint32_t kIdescO = tc::instr_desc(1, 128, 64, 1, 1);
-constexpr uint32_t kIdescL = tc::instr_desc(1, 128, 64, 0, 1);
+constexpr uint32_t kIdescS = tc::instr_desc(1, 64, 64, 0, 0);
+constexpr uint32_t kIdescO = tc::instr_desc(1, 128, 64, 1, 0);
 
-constexpr int kMiscBytes = 64 * 4 * 4 + 4 * 64 * 4 + 32 * 8 + 16;
-constexpr int kSmemBytes = 1024 + kChunks * kQChunkBytes + kChunks * kKVChunkBytes + kMiscBytes;
+struct Smem {
+    uint64_t full[2];  // half-tile buffer b gathered
+    uint64_t empty[2];  // half-tile buffer b released by its P.V
+    uint64_t q_full;
+    uint64_t s_full[2];
+    uint64_t s_empty[2];
+    uint64_t p_full[2];  // P^T of half-tile x written (x & 1: the softmax of x + 1 may
+                         // finish before the MMA issuer has seen x's phase)
+    uint64_t pv_done;
+    uint64_t o_full;
+    uint64_t o_empty;
+    uint64_t done[2];  // each MMA issuer's work complete
+    float alpha[kHeads];  // rescale factors of a running-max refresh
+    float linv[kHeads];  // 1 / row sum, for the epilogue
+    uint32_t tmem_slot;
+    int abort;
+};
+constexpr int kSmemBytes =
+    1024 + kChunks * kQChunkBytes + 2 * kBufBytes + static_cast<int>(sizeof(Smem));
 
 struct AttnTcParams {
     const uint16_t* k;  // latent [B, S, 576] bf16
@@ -86,14 +95,14 @@ struct AttnTcParams {
     float* part_o;  // split partials or nullptr
     float* part_ml;
     int B, T, S, topk;
-    int tiles_per_row, n_splits, tiles_per_split, n_units;
+    int halves_per_row, n_splits, halves_per_split, n_units;
     float scale_log2;
     unsigned* err;
     float* lse;  // [B*T, 64] or nullptr (unsplit rows; split rows get it from the combine)
 };
 
 struct Work {
-    int row, b, split, tile0, tile1;
+    int row, b, split, h0, h1;  // half-tiles h0 .. h1-1 of the row
 };
 
 __device__ __forceinline__ Work work_of(const AttnTcParams& p, int u) {
@@ -101,9 +110,9 @@ __device__ __forceinline__ Work work_of(const AttnTcParams& p, int u) {
     w.split = u % p.n_splits;
     w.row = u / p.n_splits;
     w.b = w.row / p.T;
-    w.tile0 = w.split * p.tiles_per_split;
-    w.tile1 = w.tile0 + p.tiles_per_split < p.tiles_per_row ? w.tile0 + p.tiles_per_split
-                                                             : p.tiles_per_row;
+    w.h0 = w.split * p.halves_per_split;
+    w.h1 = w.h0 + p.halves_per_split < p.halves_per_row ? w.h0 + p.halves_per_split
+                                                         : p.halves_per_row;
     return w;
 }
 
@@ -113,300 +122,364 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
-__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
-    const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(a));
-    const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(b));
-    return lo | (hi << 16);
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b, float& sum) {
+    const __nv_bfloat16 x = __float2bfloat16_rn(a);
+    const __nv_bfloat16 y = __float2bfloat16_rn(b);
+    sum += __bfloat162float(x) + __bfloat162float(y);
+    return static_cast<uint32_t>(__bfloat16_as_ushort(x)) |
+           (static_cast<uint32_t>(__bfloat16_as_ushort(y)) << 16);
 }
 
-// This thread's share of the gather of key tile t of work item W (the latent rows of the
-// row's selected keys, zero-filled past kv_len and past topk).
-__device__ __forceinline__ void gather_tile(const AttnTcParams& p, const Work& W, int t, int it,
-                                            int g, uint32_t kv_addr, uint64_t* kv_empty,
-                                            uint64_t* kv_full, volatile int* abort) {
-    latent::gather_tile<kGather>(p.k + static_cast<int64_t>(W.b) * p.S * kDqk,
-                                 seq_len(p.kv_len, W.b, p.S),
-                                 p.idx + static_cast<int64_t>(W.row) * p.topk, p.topk, t, it, g,
-                                 kv_addr, kv_empty, kv_full, abort, p.err);
+__device__ __forceinline__ void load_q(const CUtensorMap* map, uint8_t* qs, int row,
+                                       uint64_t* q_full) {
+    tc::mbar_expect_tx(q_full, kChunks * kQChunkBytes);
+    for (int c = 0; c < kChunks; ++c)
+        tc::tma_load_2d(qs + c * kQChunkBytes, map, c * 64, row * kHeads, q_full);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    tsi_attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const AttnTcParams p) {
+    tsi_attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
+                       const __grid_constant__ AttnTcParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t* qs = base;
     uint8_t* kv = qs + kChunks * kQChunkBytes;
-    float* m_s = reinterpret_cast<float*>(kv + kChunks * kKVChunkBytes);  // running max [64]
-    uint32_t* tmax_s = reinterpret_cast<uint32_t*>(m_s + 64);  // tile max (order bits) [64]
-    float* alpha_s = reinterpret_cast<float*>(tmax_s + 64);  // rescale factors [64]
-    float* l_s = alpha_s + 64;  // row sums of the unit [64]
-    uint16_t* ones = reinterpret_cast<uint16_t*>(l_s + 64);  // 64 x bf16 1.0 (128 bytes)
-    uint64_t* bars = reinterpret_cast<uint64_t*>(l_s + 64 + 4 * 64);
-    uint64_t* kv_full = bars;
-    uint64_t* kv_empty = bars + kChunks;
-    uint64_t* q_full = bars + 2 * kChunks;
-    uint64_t* q_empty = q_full + 1;
-    uint64_t* s_full = q_full + 2;
-    uint64_t* p_full = q_full + 3;
-    uint64_t* o_full = q_full + 4;
-    uint64_t* o_empty = q_full + 5;
-    uint64_t* done = q_full + 6;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_full + 7);
-    volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    Smem& sm = *reinterpret_cast<Smem*>(kv + 2 * kBufBytes);
+    volatile int* abort = &sm.abort;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-
-    if (threadIdx.x < 64) ones[threadIdx.x] = 0x3F80;  // bf16 1.0
-    tc::fence_proxy_async();  // read by the tensor core
     if (threadIdx.x == 0) {
-        for (int c = 0; c < kChunks; ++c) {
-            tc::mbar_init(&kv_full[c], kGather);
-            tc::mbar_init(&kv_empty[c], 1);
+        for (int b = 0; b < 2; ++b) {
+            tc::mbar_init(&sm.full[b], kGather);
+            tc::mbar_init(&sm.empty[b], 1);
+            tc::mbar_init(&sm.s_full[b], 1);
+            tc::mbar_init(&sm.s_empty[b], kSoftThreads);
+            tc::mbar_init(&sm.p_full[b], kSoftThreads);
         }
-        tc::mbar_init(q_full, 1);
-        tc::mbar_init(q_empty, 1);
-        tc::mbar_init(s_full, 1);
-        tc::mbar_init(p_full, kSoftThreads);
-        tc::mbar_init(o_full, 1);
-        tc::mbar_init(o_empty, kSoftThreads);
-        tc::mbar_init(done, 1);
-        *abort = 0;
+        tc::mbar_init(&sm.q_full, 1);
+        tc::mbar_init(&sm.pv_done, 1);
+        tc::mbar_init(&sm.o_full, 1);
+        tc::mbar_init(&sm.o_empty, kSoftThreads);
+        tc::mbar_init(&sm.done[0], 1);
+        tc::mbar_init(&sm.done[1], 1);
+        sm.abort = 0;
         tc::fence_barrier_init();
     }
     if (warp == kMmaWarp) {
-        tc::tmem_alloc(tmem_slot, kTmemCols);
+        tc::tmem_alloc(&sm.tmem_slot, kTmemCols);
         if (lane == 0) tc::prefetch_tmap(&tmap_q);
     }
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
+    const uint32_t tmem = sm.tmem_slot;
     const uint32_t q_addr = tc::smem_addr(qs);
     const uint32_t kv_addr = tc::smem_addr(kv);
 
-    if (warp == kMmaWarp) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            int it = 0, r_it = 0;
-            for (int u = blockIdx.x; u < p.n_units; u += gridDim.x, ++r_it) {
+    if (warp == kMmaWarp || warp == kPvWarp) {
+        // ------------------------------------------------------------ MMA issuers
+        // Two threads issue tcgen05 work: warp 4 the S products as key half-tiles land,
+        // warp 5 the P.V products as the softmax finishes them, so neither waits on the
+        // other's inputs (each commits only its own barriers).
+        if (lane == 0 && warp == kMmaWarp) {
+            int it = 0, un = 0;
+            for (int u = blockIdx.x; u < p.n_units; u += gridDim.x, ++un) {
                 const Work W = work_of(p, u);
-                tc::mbar_wait(q_full, r_it & 1, abort, p.err);
-                for (int t = W.tile0; t < W.tile1; ++t, ++it) {
-                    const bool first = t == W.tile0;
-                    for (int c = 0; c < kChunks; ++c) {
-                        tc::mbar_wait(&kv_full[c], it & 1, abort, p.err);
-                        tc::fence_proxy_async();  // cp.async landed via the generic proxy
-                        tc::tc_fence_after();
-                        if (!*abort) {
+                tc::mbar_wait(&sm.q_full, un & 1, abort, p.err);
+                for (int hh = W.h0; hh < W.h1; ++hh, ++it) {
+                    const int b = it & 1;
+                    tc::mbar_wait(&sm.full[b], (it >> 1) & 1, abort, p.err);
+                    tc::mbar_wait(&sm.s_empty[b], ((it >> 1) & 1) ^ 1, abort, p.err);
+                    tc::fence_proxy_async();  // cp.async landed via the generic proxy
+                    tc::tc_fence_after();
+                    if (!*abort) {
+                        // descriptors as base + byte offset / 16 (the start-address field
+                        // holds addr / 16; shared addresses stay below 2^18, no carry)
+                        const uint64_t da0 = tc::smem_desc(q_addr, 16, 1024);
+                        const uint64_t db0 = tc::smem_desc(kv_addr + b * kBufBytes, 16, 1024);
 #pragma unroll
-                            for (int kk = 0; kk < 4; ++kk) {
-                                const uint64_t da = tc::smem_desc(
-                                    kv_addr + c * kKVChunkBytes + kk * 32, 16, 1024);
-                                const uint64_t db = tc::smem_desc(
-                                    q_addr + c * kQChunkBytes + kk * 32, 16, 1024);
-                                tc::mma_bf16(tmem + kColS, da, db, kIdescS, (c | kk) ? 1u : 0u);
-                            }
+                        for (int c = 0; c < kChunks; ++c) {
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk)
+                                tc::mma_bf16(tmem + kColS + 64 * b,
+                                             da0 + ((c * kQChunkBytes + kk * 32) >> 4),
+                                             db0 + ((c * kChunkBytes + kk * 32) >> 4), kIdescS,
+                                             (c | kk) ? 1u : 0u);
                         }
                     }
-                    tc::mma_commit(s_full);
-                    if (t == W.tile1 - 1) tc::mma_commit(q_empty);
-                    tc::mbar_wait(p_full, it & 1, abort, p.err);
-                    if (first) tc::mbar_wait(o_empty, (r_it & 1) ^ 1, abort, p.err);
+                    tc::mma_commit(&sm.s_full[b]);
+                }
+            }
+            tc::mma_commit(&sm.done[0]);
+            tc::mbar_wait(&sm.done[0], 0, abort, p.err);
+        } else if (lane == 0) {
+            int it = 0, un = 0;
+            for (int u = blockIdx.x; u < p.n_units; u += gridDim.x, ++un) {
+                const Work W = work_of(p, u);
+                for (int hh = W.h0; hh < W.h1; ++hh, ++it) {
+                    const int b = it & 1;
+                    tc::mbar_wait(&sm.p_full[b], (it >> 1) & 1, abort, p.err);
+                    if (hh == W.h0) tc::mbar_wait(&sm.o_empty, (un & 1) ^ 1, abort, p.err);
                     tc::fence_proxy_async();  // P^T written with generic stores
                     tc::tc_fence_after();
-                    for (int m = 0; m < 4; ++m) {
-                        if (!*abort) {
-#pragma unroll
-                            for (int kk = 0; kk < 8; ++kk) {
-                                const uint64_t da = tc::smem_desc(
-                                    kv_addr + 2 * m * kKVChunkBytes + kk * 2048, kKVChunkBytes, 1024);
-                                const uint64_t db = tc::smem_desc(
-                                    kv_addr + kPSlot * kKVChunkBytes + kk * 2048, kKVChunkBytes, 1024);
-                                tc::mma_bf16(tmem + kColO + 64 * m, da, db, kIdescO,
-                                             (first && kk == 0) ? 0u : 1u);
-                            }
-                        }
-                        tc::mma_commit(&kv_empty[2 * m]);
-                        tc::mma_commit(&kv_empty[2 * m + 1]);
-                    }
-                    if (!*abort) {  // row sums: ones[128 x 16] . P^T per 16-key step
-                        const uint64_t da = tc::smem_desc(tc::smem_addr(ones), 0, 0, 0);
-#pragma unroll
-                        for (int kk = 0; kk < 8; ++kk) {
-                            const uint64_t db = tc::smem_desc(
-                                kv_addr + kPSlot * kKVChunkBytes + kk * 2048, kKVChunkBytes, 1024);
-                            tc::mma_bf16(tmem + kColL, da, db, kIdescL, (first && kk == 0) ? 0u : 1u);
-                        }
-                    }
-                    tc::mma_commit(&kv_empty[kPSlot]);
-                }
-                tc::mma_commit(o_full);
-            }
-            tc::mma_commit(done);
-            tc::mbar_wait(done, 0, abort, p.err);
-        }
-    } else {
-        // gather index: threads 0..127 and 160..511 (warp 4 issues the MMAs)
-        const int g = threadIdx.x < 128 ? static_cast<int>(threadIdx.x) : threadIdx.x - 32;
-        int it = 0, r_it = 0;
-        if (!is_softmax_warp(warp)) {
-            // -------------------------------------------------------- gather only
-            for (int u = blockIdx.x; u < p.n_units; u += gridDim.x, ++r_it) {
-                const Work W = work_of(p, u);
-                if (g == kGatherQ) {
-                    tc::mbar_wait(q_empty, (r_it & 1) ^ 1, abort, p.err);
                     if (!*abort) {
-                        tc::mbar_expect_tx(q_full, kChunks * kQChunkBytes);
-                        for (int c = 0; c < kChunks; ++c)
-                            tc::tma_load_2d(qs + c * kQChunkBytes, &tmap_q, c * 64,
-                                            W.row * kHeads, q_full);
+                        const uint32_t kb = kv_addr + b * kBufBytes;
+                        const uint64_t da0 = tc::smem_desc(kb, kChunkBytes, 1024);
+                        const uint64_t db0 = tc::smem_desc(kb + kPSlot * kChunkBytes, 16, 1024);
+                        const uint32_t first = hh == W.h0 ? 0u : 1u;
+#pragma unroll
+                        for (int m = 0; m < 4; ++m) {
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk)
+                                tc::mma_bf16(tmem + kColO + 64 * m,
+                                             da0 + ((2 * m * kChunkBytes + kk * 2048) >> 4),
+                                             db0 + ((kk * 32) >> 4), kIdescO,
+                                             kk == 0 ? first : 1u);
+                        }
                     }
+                    tc::mma_commit(&sm.empty[b]);
+                    tc::mma_commit(&sm.pv_done);
                 }
-                for (int t = W.tile0; t < W.tile1; ++t, ++it)
-                    gather_tile(p, W, t, it, g, kv_addr, kv_empty, kv_full, abort);
+                tc::mma_commit(&sm.o_full);
             }
-        } else {
-            // -------------------------------------------- gather, softmax + row epilogue
-            const int sw = warp < 4 ? warp : warp - 4;  // softmax warp 0..7
-            const int st = sw * 32 + lane;
-            const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31
-            const int h0 = 32 * (warp >> 3);  // this warp's heads h0 .. h0+31
-            const int k = quad * 32 + lane;  // key slot of the tile owned by this thread
-            const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-            const float neg_inf = -__int_as_float(0x7f800000);
-            uint8_t* prow = kv + kPSlot * kKVChunkBytes + (k >> 3) * 1024 + (k & 7) * 128;
-            for (int u = blockIdx.x; u < p.n_units; u += gridDim.x, ++r_it) {
-                const Work W = work_of(p, u);
-                const int64_t len = seq_len(p.kv_len, W.b, p.S);
-                const int32_t* irow = p.idx + static_cast<int64_t>(W.row) * p.topk;
-                if (st < 64) {
-                    m_s[st] = neg_inf;
-                    tmax_s[st] = 0u;
+            tc::mma_commit(&sm.done[1]);
+            tc::mbar_wait(&sm.done[1], 0, abort, p.err);
+        }
+    } else if (warp > kPvWarp) {
+        // ------------------------------------------------------------ gather
+        const int g = threadIdx.x - kGatherBase;
+        int it = 0;
+        for (int u = blockIdx.x; u < p.n_units; u += gridDim.x) {
+            const Work W = work_of(p, u);
+            const int64_t len = seq_len(p.kv_len, W.b, p.S);
+            const int32_t* irow = p.idx + static_cast<int64_t>(W.row) * p.topk;
+            const uint16_t* kseq = p.k + static_cast<int64_t>(W.b) * p.S * kDqk;
+            for (int hh = W.h0; hh < W.h1; ++hh, ++it) {
+                const int b = it & 1;
+                const uint16_t* src[kGatherPer];
+                uint32_t nbytes[kGatherPer];
+                uint32_t dst[kGatherPer];
+#pragma unroll
+                for (int j = 0; j < kGatherPer; ++j) {
+                    const int piece = g + kGather * j;
+                    const int k = (piece >> 3) & (kHalf - 1);
+                    const int sub = piece & 7;
+                    const int e = hh * kHalf + k;
+                    const int s = (piece < kPieces && e < p.topk) ? irow[e] : -1;
+                    const bool ok = s >= 0 && s < len;
+                    src[j] = ok ? kseq + static_cast<int64_t>(s) * kDqk + sub * 8 : kseq;
+                    nbytes[j] = ok ? 16u : 0u;
+                    dst[j] = kv_addr + b * kBufBytes + (k >> 3) * 1024 + (k & 7) * 128 +
+                             ((sub ^ (k & 7)) << 4);
                 }
-                named_bar(kSoftBar, kSoftThreads);
-                for (int t = W.tile0; t < W.tile1; ++t, ++it) {
-                    // the chunks of tile t free up as the MMA finishes tile t-1 with them,
-                    // and this warp has already written that tile's P
-                    gather_tile(p, W, t, it, g, kv_addr, kv_empty, kv_full, abort);
-                    const int e = t * kKeys + k;
-                    const int s = e < p.topk ? irow[e] : -1;
-                    const bool valid = s >= 0 && s < len;
-                    tc::mbar_wait(s_full, it & 1, abort, p.err);
-                    tc::tc_fence_after();
-                    const uint32_t s_addr = tmem + lane_base + kColS + h0;
-                    uint32_t z[32];  // logits of this key for heads h0 .. h0+31
-                    TSI_TMEM_LD32(s_addr, z);
-                    tc::tmem_wait_ld();
-                    // does any logit of the tile exceed the running max of its head by 2^16?
-                    bool over = false;
+                tc::mbar_wait(&sm.empty[b], ((it >> 1) & 1) ^ 1, abort, p.err);
+                for (int c = 0; c < kChunks; ++c) {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        over |= valid && (__uint_as_float(z[j]) * p.scale_log2 > m_s[h0 + j] + kRescaleLog2);
-                    if (tc::bar_red_or(kSoftBar, kSoftThreads, over)) {
-                        // exact tile max per head, new running max, rescale what O^T holds
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            const float zh = valid ? __uint_as_float(z[j]) * p.scale_log2 : neg_inf;
-                            const uint32_t v = __reduce_max_sync(kFull, score_order_bits(zh));
-                            if (lane == 0) atomicMax(&tmax_s[h0 + j], v);
-                        }
-                        named_bar(kSoftBar, kSoftThreads);
-                        if (st < 64) {
-                            const float mo = m_s[st];
-                            const float mn = fmaxf(mo, order_bits_score(tmax_s[st]));
-                            alpha_s[st] = mo == neg_inf ? 0.f : ex2(mo - mn);
-                            m_s[st] = mn;
-                            tmax_s[st] = 0u;
-                        }
-                        named_bar(kSoftBar, kSoftThreads);
-                        if (t != W.tile0) {
-                            for (int m = 0; m < 5; ++m) {  // the 4 O^T blocks and the row sums
-                                uint32_t o[32];
-                                const uint32_t ta = tmem + lane_base + kColO + 64 * m + h0;
-                                TSI_TMEM_LD32(ta, o);
-                                tc::tmem_wait_ld();
-#pragma unroll
-                                for (int j = 0; j < 32; ++j)
-                                    o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha_s[h0 + j]);
-                                TSI_TMEM_ST32(ta, o);
-                            }
-                            tc::tmem_wait_st();
-                        }
-                    }
-                    // P^T row of this key: heads h0 .. h0+31 as bf16, four 16-byte pieces of
-                    // the 128-byte-swizzled row (MN-major B operand)
-#pragma unroll
-                    for (int jj = 0; jj < 4; ++jj) {
-                        const int j = (h0 >> 3) + jj;
-                        float pv[8];
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            const int h = 8 * j + i;
-                            const float zh = __uint_as_float(z[8 * jj + i]) * p.scale_log2;
-                            pv[i] = valid ? ex2(zh - m_s[h]) : 0.f;
-                        }
-                        uint4 v;
-                        v.x = pack_bf16(pv[0], pv[1]);
-                        v.y = pack_bf16(pv[2], pv[3]);
-                        v.z = pack_bf16(pv[4], pv[5]);
-                        v.w = pack_bf16(pv[6], pv[7]);
-                        *reinterpret_cast<uint4*>(prow + ((j ^ (k & 7)) << 4)) = v;
-                    }
-                    tc::fence_proxy_async();
-                    tc::tc_fence_before();
-                    tc::mbar_arrive(p_full);
-                }
-                // ------------------------------------------------------ row epilogue
-                tc::mbar_wait(o_full, r_it & 1, abort, p.err);
-                tc::tc_fence_after();
-                uint32_t lv[32];  // row sums of heads h0 .. h0+31 (same in every lane)
-                TSI_TMEM_LD32(tmem + lane_base + kColL + h0, lv);
-                tc::tmem_wait_ld();
-                if (quad == 0 && lane == 0) {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) l_s[h0 + j] = __uint_as_float(lv[j]);
-                }
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const float L = __uint_as_float(lv[j]);
-                    lv[j] = __float_as_uint(L > 0.f ? 1.f / L : 0.f);
-                }
-                for (int m = 0; m < 4; ++m) {
-                    const int d = 128 * m + 32 * quad + lane;
-                    uint32_t o[32];
-                    TSI_TMEM_LD32(tmem + lane_base + kColO + 64 * m + h0, o);
-                    tc::tmem_wait_ld();
-                    if (p.part_o) {
-                        float* po = p.part_o +
-                                    ((static_cast<int64_t>(W.row) * p.n_splits + W.split) * kHeads + h0) * kDv + d;
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) po[static_cast<int64_t>(j) * kDv] = __uint_as_float(o[j]);
-                    } else {
-                        __nv_bfloat16* out = p.out + (static_cast<int64_t>(W.row) * kHeads + h0) * kDv + d;
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            out[static_cast<int64_t>(j) * kDv] =
-                                __float2bfloat16_rn(__uint_as_float(o[j]) * __uint_as_float(lv[j]));
+                    for (int j = 0; j < kGatherPer; ++j) {
+                        if (g + kGather * j < kPieces)
+                            tc::cp_async16(dst[j] + c * kChunkBytes,
+                                           src[j] + (nbytes[j] ? c * 64 : 0), nbytes[j]);
                     }
                 }
-                if (p.part_o) {
-                    named_bar(kSoftBar, kSoftThreads);
-                    if (st < 64) {
-                        const int64_t slot = (static_cast<int64_t>(W.row) * p.n_splits + W.split) * kHeads + st;
-                        p.part_ml[2 * slot] = m_s[st];
-                        p.part_ml[2 * slot + 1] = l_s[st];
-                    }
-                } else if (p.lse) {
-                    named_bar(kSoftBar, kSoftThreads);
-                    if (st < 64) p.lse[static_cast<int64_t>(W.row) * kHeads + st] = lse_of(m_s[st], l_s[st]);
-                }
-                tc::tc_fence_before();
-                tc::mbar_arrive(o_empty);
+                tc::cp_async_arrive_noinc(&sm.full[b]);
             }
         }
         asm volatile("cp.async.wait_all;" ::: "memory");
+    } else {
+        // ------------------------------------------------- softmax + row epilogue
+        // The S buffer's 16 used lanes of this warp's quadrant are read in the 16x256b
+        // shape: thread T holds heads hA = 16 q + T / 4 and hB = hA + 8, keys
+        // 8 m + 2 (T % 4) + {0, 1} for m = 0..7 (registers 4m, 4m+1 for hA, 4m+2, 4m+3 for
+        // hB); the four threads of a head combine maxima and sums with two shuffles.
+        const int q = warp;  // TMEM lane quadrant
+        const int t4 = lane & 3;
+        const int hA = 16 * q + (lane >> 2);
+        const int hB = hA + 8;
+        const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+        const float neg_inf = -__int_as_float(0x7f800000);
+        int it = 0, un = 0, q_issued = 0;
+        if (threadIdx.x == 0 && blockIdx.x < p.n_units) {
+            load_q(&tmap_q, qs, work_of(p, blockIdx.x).row, &sm.q_full);
+            ++q_issued;
+        }
+        for (int u = blockIdx.x; u < p.n_units; u += gridDim.x, ++un) {
+            const Work W = work_of(p, u);
+            const int nh = W.h1 - W.h0;
+            const int64_t len = seq_len(p.kv_len, W.b, p.S);
+            const int32_t* irow = p.idx + static_cast<int64_t>(W.row) * p.topk;
+            float mA = neg_inf, mB = neg_inf;  // running maxima (base 2, scaled)
+            float lA = 0.f, lB = 0.f;  // this thread's share of the row sums
+            for (int j = 0; j < nh; ++j, ++it) {
+                const int b = it & 1;
+                // which of the half-tile's 64 entries are keys: bit k of va / vb = entry k / 32+k
+                const int e0 = (W.h0 + j) * kHalf;
+                const int sa = e0 + lane < p.topk ? irow[e0 + lane] : -1;
+                const int sb = e0 + 32 + lane < p.topk ? irow[e0 + 32 + lane] : -1;
+                const uint32_t va = __ballot_sync(kFull, sa >= 0 && sa < len);
+                const uint32_t vb = __ballot_sync(kFull, sb >= 0 && sb < len);
+                uint32_t vbits = 0;  // bit 2m+e: key 8m + 2 t4 + e is a key
+#pragma unroll
+                for (int m = 0; m < 8; ++m) {
+                    const uint32_t w = m < 4 ? va : vb;
+                    vbits |= ((w >> ((8 * m + 2 * t4) & 31)) & 3u) << (2 * m);
+                }
+                tc::mbar_wait(&sm.s_full[b], (it >> 1) & 1, abort, p.err);
+                tc::tc_fence_after();
+                if (threadIdx.x == 0 && j == nh - 1 && !*abort) {
+                    // every S of this unit is done: the Q buffer is free for the next unit
+                    const int nu = u + gridDim.x;
+                    if (nu < p.n_units) {
+                        load_q(&tmap_q, qs, work_of(p, nu).row, &sm.q_full);
+                        ++q_issued;
+                    }
+                }
+                uint32_t r[32];
+                TSI_TMEM_LD16x256_X8(tmem + lane_base + kColS + 64 * b, r);
+                tc::tmem_wait_ld();
+                tc::tc_fence_before();
+                tc::mbar_arrive(&sm.s_empty[b]);
+                float xa = neg_inf, xb = neg_inf;
+#pragma unroll
+                for (int m = 0; m < 8; ++m) {
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const float za = __uint_as_float(r[4 * m + e]) * p.scale_log2;
+                        const float zb = __uint_as_float(r[4 * m + 2 + e]) * p.scale_log2;
+                        r[4 * m + e] = __float_as_uint(za);
+                        r[4 * m + 2 + e] = __float_as_uint(zb);
+                        if ((vbits >> (2 * m + e)) & 1u) {
+                            xa = fmaxf(xa, za);
+                            xb = fmaxf(xb, zb);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int o = 1; o < 4; o <<= 1) {
+                    xa = fmaxf(xa, __shfl_xor_sync(kFull, xa, o));
+                    xb = fmaxf(xb, __shfl_xor_sync(kFull, xb, o));
+                }
+                const bool needA = xa > mA + kRescaleLog2;
+                const bool needB = xb > mB + kRescaleLog2;
+                const bool rescale = tc::bar_red_or(kSoftBar, kSoftThreads, needA || needB);
+                float alphaA = 1.f, alphaB = 1.f;
+                if (needA) {
+                    alphaA = mA == neg_inf ? 0.f : ex2(mA - xa);
+                    mA = xa;
+                }
+                if (needB) {
+                    alphaB = mB == neg_inf ? 0.f : ex2(mB - xb);
+                    mB = xb;
+                }
+                // P^T rows of heads hA, hB (K-major B operand over the RoPE chunk's slot): the
+                // two keys of piece m go to bytes 4 t4 .. 4 t4 + 3 of the swizzled piece
+                uint8_t* pslot = kv + b * kBufBytes + kPSlot * kChunkBytes;
+                uint8_t* prowA = pslot + (hA >> 3) * 1024 + (hA & 7) * 128 + 4 * t4;
+                uint8_t* prowB = pslot + (hB >> 3) * 1024 + (hB & 7) * 128 + 4 * t4;
+                float sA = 0.f, sB = 0.f;
+#pragma unroll
+                for (int m = 0; m < 8; ++m) {
+                    const bool v0 = (vbits >> (2 * m)) & 1u;
+                    const bool v1 = (vbits >> (2 * m + 1)) & 1u;
+                    const float a0 = v0 ? ex2(__uint_as_float(r[4 * m]) - mA) : 0.f;
+                    const float a1 = v1 ? ex2(__uint_as_float(r[4 * m + 1]) - mA) : 0.f;
+                    const float b0 = v0 ? ex2(__uint_as_float(r[4 * m + 2]) - mB) : 0.f;
+                    const float b1 = v1 ? ex2(__uint_as_float(r[4 * m + 3]) - mB) : 0.f;
+                    *reinterpret_cast<uint32_t*>(prowA + ((m ^ (hA & 7)) << 4)) =
+                        pack_bf16(a0, a1, sA);
+                    *reinterpret_cast<uint32_t*>(prowB + ((m ^ (hB & 7)) << 4)) =
+                        pack_bf16(b0, b1, sB);
+                }
+                lA = lA * alphaA + sA;
+                lB = lB * alphaB + sB;
+                if (rescale && j > 0) {  // O^T holds this unit's earlier half-tiles: rescale it
+                    if (t4 == 0) {
+                        sm.alpha[hA] = alphaA;
+                        sm.alpha[hB] = alphaB;
+                    }
+                    tc::mbar_wait(&sm.pv_done, (it - 1) & 1, abort, p.err);
+                    named_bar(kSoftBar, kSoftThreads);
+                    tc::tc_fence_after();
+#pragma unroll 1
+                    for (int m = 0; m < 4; ++m) {  // rare: one 32-column block at a time
+#pragma unroll 1
+                        for (int half = 0; half < 2; ++half) {
+                            uint32_t o[32];
+                            const uint32_t ta = tmem + lane_base + kColO + 64 * m + 32 * half;
+                            TSI_TMEM_LD32(ta, o);
+                            tc::tmem_wait_ld();
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                o[i] = __float_as_uint(__uint_as_float(o[i]) *
+                                                       sm.alpha[32 * half + i]);
+                            TSI_TMEM_ST32(ta, o);
+                        }
+                    }
+                    tc::tmem_wait_st();
+                }
+                tc::fence_proxy_async();
+                tc::tc_fence_before();
+                tc::mbar_arrive(&sm.p_full[b]);
+            }
+            // ------------------------------------------------------ row epilogue
+#pragma unroll
+            for (int o = 1; o < 4; o <<= 1) {
+                lA += __shfl_xor_sync(kFull, lA, o);
+                lB += __shfl_xor_sync(kFull, lB, o);
+            }
+            tc::mbar_wait(&sm.o_full, un & 1, abort, p.err);
+            tc::tc_fence_after();
+            if (t4 == 0) {
+                sm.linv[hA] = lA > 0.f ? 1.f / lA : 0.f;
+                sm.linv[hB] = lB > 0.f ? 1.f / lB : 0.f;
+                if (p.part_o) {
+                    const int64_t slot0 =
+                        (static_cast<int64_t>(W.row) * p.n_splits + W.split) * kHeads;
+                    p.part_ml[2 * (slot0 + hA)] = mA;
+                    p.part_ml[2 * (slot0 + hA) + 1] = lA;
+                    p.part_ml[2 * (slot0 + hB)] = mB;
+                    p.part_ml[2 * (slot0 + hB) + 1] = lB;
+                } else if (p.lse) {
+                    p.lse[static_cast<int64_t>(W.row) * kHeads + hA] = lse_of(mA, lA);
+                    p.lse[static_cast<int64_t>(W.row) * kHeads + hB] = lse_of(mB, lB);
+                }
+            }
+            named_bar(kSoftBar, kSoftThreads);
+            for (int m = 0; m < 4; ++m) {
+                const int d = 128 * m + 32 * q + lane;  // this thread's value dim (TMEM lane)
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t o[32];  // O^T[d, heads 32 half .. 32 half + 31]
+                    TSI_TMEM_LD32(tmem + lane_base + kColO + 64 * m + 32 * half, o);
+                    tc::tmem_wait_ld();
+                    if (p.part_o) {
+                        float* po = p.part_o +
+                                    ((static_cast<int64_t>(W.row) * p.n_splits + W.split) * kHeads +
+                                     32 * half) * kDv + d;
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            po[static_cast<int64_t>(i) * kDv] = __uint_as_float(o[i]);
+                    } else {
+                        __nv_bfloat16* out =
+                            p.out + (static_cast<int64_t>(W.row) * kHeads + 32 * half) * kDv + d;
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            out[static_cast<int64_t>(i) * kDv] = __float2bfloat16_rn(
+                                __uint_as_float(o[i]) * sm.linv[32 * half + i]);
+                    }
+                }
+            }
+            tc::tc_fence_before();
+            tc::mbar_arrive(&sm.o_empty);
+        }
+        // a Q load still in flight after an abort must land before the CTA exits
+        if (threadIdx.x == 0 && *abort && q_issued > 0) {
+            const long long t0 = clock64();
+            while (!tc::mbar_try_wait(&sm.q_full, (q_issued - 1) & 1) &&
+                   clock64() - t0 < tc::kWaitCycles) {
+            }
+        }
     }
     tc::tc_fence_before();
     __syncthreads();
@@ -434,18 +507,19 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 constexpr int kPlanSMs = 152;
 
-void attn_tc_plan(int rows, int topk, int* n_splits, int* tiles_per_split, int* tiles) {
-    const int nt = (topk + kKeys - 1) / kKeys;
+// Half-tiles per row, and for few rows (decode) the split of a row's half-tiles over CTAs.
+void attn_tc_plan(int rows, int topk, int* n_splits, int* halves_per_split, int* halves) {
+    const int nh = (topk + kHalf - 1) / kHalf;
     int ns = 1;
     if (rows > 0 && rows < kPlanSMs) {
-        ns = (2 * kPlanSMs + rows - 1) / rows;
-        if (ns > nt) ns = nt;
+        ns = (kPlanSMs + rows - 1) / rows;
+        if (ns > nh) ns = nh;
         if (ns < 1) ns = 1;
     }
-    const int tps = (nt + ns - 1) / ns;
-    *tiles = nt;
-    *tiles_per_split = tps;
-    *n_splits = (nt + tps - 1) / tps;
+    const int hps = (nh + ns - 1) / ns;
+    *halves = nh;
+    *halves_per_split = hps;
+    *n_splits = (nh + hps - 1) / hps;
 }
 
 int sm_count() {
@@ -467,8 +541,8 @@ bool tc_attn_supported(int H, int Hkv, int Dqk, int Dv, bool v_from_k) {
 }
 
 size_t tc_attn_workspace_bytes(int B, int T, int H, int Dv, int topk) {
-    int ns, tps, nt;
-    attn_tc_plan(B * T, topk, &ns, &tps, &nt);
+    int ns, hps, nh;
+    attn_tc_plan(B * T, topk, &ns, &hps, &nh);
     if (ns <= 1) return 0;
     const size_t slots = static_cast<size_t>(B) * T * ns * H;
     return slots * Dv * sizeof(float) + slots * 2 * sizeof(float);
@@ -497,7 +571,7 @@ cudaError_t launch_attn_tc(const AttnArgs& a, void* workspace, cudaStream_t st) 
     p.T = a.T;
     p.S = a.S;
     p.topk = a.topk;
-    attn_tc_plan(rows, a.topk, &p.n_splits, &p.tiles_per_split, &p.tiles_per_row);
+    attn_tc_plan(rows, a.topk, &p.n_splits, &p.halves_per_split, &p.halves_per_row);
     p.n_units = rows * p.n_splits;
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.err = a.err;
