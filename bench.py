@@ -529,13 +529,15 @@ def measure_index_kl(cfg, ind, lay, idx, outs, ws, stream, reps=2):
                          "peak_source": f"{peaks['source']} hbm_gbs"}}
 
 
-def run_e2e(args, cfg, ind, lay, idx, outs, ws, stream, world):
+def run_e2e(args, cfg, ind, lay, idx, outs, ws, stream, world, n_copy_streams=4):
     """Same step with inputs copied host->device and results device->host inside the
-    timed region (pinned host buffers, one cudaMemcpyAsync per tensor).
+    timed region (pinned host buffers; every tensor moves as n_copy_streams contiguous
+    pieces, one cudaMemcpyAsync each, on as many streams, so several copy engines share
+    the transfer).
 
-    Copies overlap the kernels, as a pipelined caller would run them: an upload stream
-    moves each layer's Q and latent (and each group's indexer inputs) into that layer's
-    own device buffers ahead of the compute stream; a read-back stream copies each
+    Copies overlap the kernels, as a pipelined caller would run them: the upload streams
+    move each layer's Q and latent (and each group's indexer inputs) into that layer's
+    own device buffers ahead of the compute stream; the read-back streams copy each
     layer's output (and each group's index rows) to the host behind it.  Events order
     every reuse of a buffer: an upload waits until the previous step's kernels are done
     with its destination, a kernel waits for its inputs and for the read-back of the
@@ -557,8 +559,8 @@ def run_e2e(args, cfg, ind, lay, idx, outs, ws, stream, world):
     h_O = pin(outs[0])
     h_idx = pin(idx)
     idx_bufs = [idx, torch.empty_like(idx)]
-    up = torch.cuda.Stream(device=idx.device)
-    down = torch.cuda.Stream(device=idx.device)
+    ups = [torch.cuda.Stream(device=idx.device) for _ in range(n_copy_streams)]
+    downs = [torch.cuda.Stream(device=idx.device) for _ in range(n_copy_streams)]
     ev = lambda: torch.cuda.Event()  # noqa: E731
     h2d = d2h = 0
     steps = max(1, min(args.steps, 2))
@@ -568,65 +570,70 @@ def run_e2e(args, cfg, ind, lay, idx, outs, ws, stream, world):
     out_read = [None] * cfg.group
     idx_read = [None] * 2
 
+    def split_copy(dst, src, streams, after):
+        """dst <- src as len(streams) contiguous pieces, piece i on streams[i] once the
+        events `after` have fired; returns the events that mark each piece done."""
+        fd, fs = dst.view(-1), src.view(-1)
+        n = fd.numel()
+        per = (n + len(streams) - 1) // len(streams)
+        done = []
+        for i, st in enumerate(streams):
+            lo, hi = i * per, min(n, (i + 1) * per)
+            if lo >= hi:
+                continue
+            with torch.cuda.stream(st):
+                for e in after:
+                    if e is not None:
+                        st.wait_event(e)
+                fd[lo:hi].copy_(fs[lo:hi], non_blocking=True)
+                e = ev()
+                e.record(st)
+                done.append(e)
+        return done
+
     def step():
         nonlocal h2d, d2h
         in_ready, ind_ready = [], []
         for g in range(G):  # uploads, in the order the kernels need them
-            with torch.cuda.stream(up):
-                if idx_done[g] is not None:
-                    up.wait_event(idx_done[g])
-                for hx, dx in zip(h_ind, ind[g]):
-                    dx.copy_(hx, non_blocking=True)
-                    h2d += hx.numel() * hx.element_size()
-                e = ev()
-                e.record(up)
-                ind_ready.append(e)
-                for l0 in range(cfg.group):
-                    layer = g * cfg.group + l0
-                    Q, K, _ = lay[layer]
-                    if attn_done[layer] is not None:
-                        up.wait_event(attn_done[layer])
-                    Q.copy_(h_Q, non_blocking=True)
-                    K.copy_(h_K, non_blocking=True)
-                    h2d += h_Q.numel() * 2 + h_K.numel() * 2
-                    e = ev()
-                    e.record(up)
-                    in_ready.append(e)
+            evs = []
+            for hx, dx in zip(h_ind, ind[g]):
+                evs += split_copy(dx, hx, ups, [idx_done[g]])
+                h2d += hx.numel() * hx.element_size()
+            ind_ready.append(evs)
+            for l0 in range(cfg.group):
+                layer = g * cfg.group + l0
+                Q, K, _ = lay[layer]
+                evs = split_copy(Q, h_Q, ups, [attn_done[layer]])
+                evs += split_copy(K, h_K, ups, [attn_done[layer]])
+                h2d += h_Q.numel() * 2 + h_K.numel() * 2
+                in_ready.append(evs)
         for g in range(G):
             qI, kI, w = ind[g]
             ib = idx_bufs[g % 2]
-            stream.wait_event(ind_ready[g])
-            if idx_read[g % 2] is not None:
-                stream.wait_event(idx_read[g % 2])
+            for e in ind_ready[g]:
+                stream.wait_event(e)
+            for e in idx_read[g % 2] or []:
+                stream.wait_event(e)
             tsi.indexer_topk(qI, kI, w, cfg.topk, idx=ib, workspace=ws, stream=stream)
             e = ev()
             e.record(stream)
             idx_done[g] = e
-            with torch.cuda.stream(down):
-                down.wait_event(e)
-                h_idx.copy_(ib, non_blocking=True)
-                d2h += ib.numel() * ib.element_size()
-                r = ev()
-                r.record(down)
-                idx_read[g % 2] = r
+            idx_read[g % 2] = split_copy(h_idx, ib, downs, [e])
+            d2h += ib.numel() * ib.element_size()
             for l0 in range(cfg.group):
                 layer = g * cfg.group + l0
                 Q, K, V = lay[layer]
-                stream.wait_event(in_ready[layer])
-                if out_read[l0] is not None:
-                    stream.wait_event(out_read[l0])
+                for e in in_ready[layer]:
+                    stream.wait_event(e)
+                for e in out_read[l0] or []:
+                    stream.wait_event(e)
                 tsi.sparse_attn_group([Q], [K], None, ib, cfg.scale, outs=[outs[l0]],
                                       workspace=ws, stream=stream, Dv=cfg.Dv)
                 e = ev()
                 e.record(stream)
                 attn_done[layer] = e
-                with torch.cuda.stream(down):
-                    down.wait_event(e)
-                    h_O.copy_(outs[l0], non_blocking=True)
-                    d2h += h_O.numel() * 2
-                    r = ev()
-                    r.record(down)
-                    out_read[l0] = r
+                out_read[l0] = split_copy(h_O, outs[l0], downs, [e])
+                d2h += h_O.numel() * 2
 
     step()  # warm the copy path
     torch.cuda.synchronize()
@@ -634,19 +641,21 @@ def run_e2e(args, cfg, ind, lay, idx, outs, ws, stream, world):
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
     a.record(stream)
-    up.wait_event(a)  # no upload starts before the timer
+    for st in ups:
+        st.wait_event(a)  # no upload starts before the timer
     for _ in range(steps):
         step()
-    stream.wait_stream(down)
-    stream.wait_stream(up)
+    for st in ups + downs:
+        stream.wait_stream(st)
     b.record(stream)
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / steps
     return {"value": round(world * G * cfg.B * cfg.T / (ms / 1e3), 2), "unit": UNIT,
             "h2d_bytes_per_step": h2d // steps, "d2h_bytes_per_step": d2h // steps,
             "ms_per_step": round(ms, 2), "steps": steps,
-            "note": "every layer uploads Q and the latent from one pinned host buffer; "
-                    "copies run on their own streams, overlapping the kernels"}
+            "note": f"every layer uploads Q and the latent from one pinned host buffer; "
+                    f"copies run on {n_copy_streams} streams per direction, overlapping the "
+                    f"kernels"}
 
 
 # ----------------------------------------------------------------------------- CPU oracle
