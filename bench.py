@@ -313,7 +313,8 @@ def run_gpu(args, rank, world):
 
     # --- end to end through the C ABI with host buffers ---------------------------------
     if not args.no_e2e:
-        result["e2e"] = run_e2e(args, cfg, ind, lay, idx, outs, ws, stream, world)
+        result["e2e"] = run_e2e(args, cfg, ind, lay, idx, outs, ws, stream, world,
+                                n_copy_streams=args.copy_streams)
     return result
 
 
@@ -674,7 +675,9 @@ def run_cpu_oracle(cfg_id, budget_s, on_device=None):
     cores = oracle.n_threads_default()
     T, S = cfg.T, cfg.S
     n_idx_rows = max(cores, 2 * cores)
-    rows = np.unique(np.linspace(T - 1, 0, n_idx_rows).astype(np.int64))
+    rows = np.unique(np.linspace(cfg.B * T - 1, 0, n_idx_rows).astype(np.int64))
+    # keys of row r (sequence r // T, query r % T at position S - T + r % T)
+    n_keys = lambda r: max(0, S - T + int(r) % T + 1)  # noqa: E731
     # inputs of the sampled rows only (same distributions as the workload)
     kI = draw((cfg.B, S, cfg.d_I), cfg.qk_dist, cfg.qk_dtype, 1, "cpu", cfg.d_I)
     q_rows = draw((len(rows), cfg.H_I, cfg.d_I), cfg.qk_dist, cfg.qk_dtype, 2, "cpu", cfg.d_I)
@@ -682,7 +685,7 @@ def run_cpu_oracle(cfg_id, budget_s, on_device=None):
     t0 = time.perf_counter()
     idx_rows, _ = oracle.indexer_topk_rows(q_rows, kI, w_rows, cfg.topk, T, rows)
     t_idx = time.perf_counter() - t0
-    work_idx = sum(int(r) + 1 for r in rows)
+    work_idx = sum(n_keys(r) for r in rows)
     t_idx_full = t_idx * accounting.causal_pairs(cfg.B, T, S) / work_idx
     # attention: 4 layers on a subset of those rows
     n_att = max(cores, 16)
@@ -693,14 +696,15 @@ def run_cpu_oracle(cfg_id, budget_s, on_device=None):
     for _ in range(cfg.group):
         oracle.sparse_attn(Qr, K, None, idx_rows[:len(arows)], cfg.scale, T, arows, Dv=cfg.Dv)
     t_att = time.perf_counter() - t0
-    work_att = cfg.group * sum(min(cfg.topk, int(r) + 1) for r in arows)
+    work_att = cfg.group * sum(min(cfg.topk, n_keys(r)) for r in arows)
     t_att_full = t_att * cfg.group * accounting.selected_pairs(cfg.B, T, S, cfg.topk) / work_att
     t_group = t_idx_full + t_att_full
     return {"value": round(cfg.B * T / t_group, 4), "unit": UNIT, "cores": cores,
             "kind": "oracle",
             "sample": f"{len(rows)} stratified query rows (indexer + top-k, fp64) and "
                       f"{len(arows)} of them x {cfg.group} layers (sparse attention, fp64) of "
-                      f"one L={T} IndexShare group; scaled by causal pairs / selected keys",
+                      f"one IndexShare group ({cfg.B} x {T} query rows over L={S}); scaled "
+                      f"by causal pairs / selected keys",
             "sample_seconds": round(t_idx + t_att, 2)}
 
 
@@ -743,6 +747,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-cp", action="store_true",
                     help="skip the context-parallel indexer measurement after the timed steps")
+    ap.add_argument("--copy-streams", type=int, default=4,
+                    help="streams per direction for the end-to-end host copies")
     ap.add_argument("--no-kl", action="store_true",
                     help="skip the group-centroid KL measurement")
     ap.add_argument("--no-overlap", action="store_true",
