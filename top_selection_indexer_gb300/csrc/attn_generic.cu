@@ -102,34 +102,79 @@ __global__ void __launch_bounds__(kWarps * 32) attn_generic_kernel(AttnArgs a, i
     }
 }
 
-// One block per (row, head): merge the split partials.
-__global__ void attn_combine_kernel(AttnArgs a, int n_splits, const float* part_o,
-                                    const float* part_ml) {
+// One block per (row, head): merge the split partials.  The splits' maxima and sums go
+// through shared memory once; each thread then owns four value dims (float4 loads when Dv
+// is a multiple of 4) and accumulates them over the splits.
+constexpr int kCombineThreads = 128;
+constexpr int kMaxCombineSplits = 256;
+
+__global__ void __launch_bounds__(kCombineThreads) attn_combine_kernel(
+    AttnArgs a, int n_splits, const float* part_o, const float* part_ml) {
+    __shared__ float wsp[kMaxCombineSplits];  // weight of split sp: 2^(m_sp - M)
     const int row = blockIdx.x;
     const int h = blockIdx.y;
-    float M = -__int_as_float(0x7f800000);
-    for (int sp = 0; sp < n_splits; ++sp) {
-        const int64_t slot = (static_cast<int64_t>(row) * n_splits + sp) * a.H + h;
-        M = fmaxf(M, part_ml[2 * slot]);
+    const int tid = threadIdx.x;
+    const float neg_inf = -__int_as_float(0x7f800000);
+    const int64_t slot0 = static_cast<int64_t>(row) * n_splits * a.H + h;
+    float m = neg_inf;
+    for (int sp = tid; sp < n_splits; sp += kCombineThreads) {
+        const float l = part_ml[2 * (slot0 + static_cast<int64_t>(sp) * a.H) + 1];
+        if (l > 0.f) m = fmaxf(m, part_ml[2 * (slot0 + static_cast<int64_t>(sp) * a.H)]);
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+    if ((tid & 31) == 0) wsp[tid >> 5] = m;  // per-warp maxima (reused below)
+    __syncthreads();
+    float M = neg_inf;
+    for (int w = 0; w < kCombineThreads / 32; ++w) M = fmaxf(M, wsp[w]);
+    __syncthreads();
     float L = 0.f;
-    for (int sp = 0; sp < n_splits; ++sp) {
-        const int64_t slot = (static_cast<int64_t>(row) * n_splits + sp) * a.H + h;
-        const float l = part_ml[2 * slot + 1];
-        if (l > 0.f) L += l * exp2f(part_ml[2 * slot] - M);
+    for (int sp = tid; sp < n_splits; sp += kCombineThreads) {
+        const int64_t sl = slot0 + static_cast<int64_t>(sp) * a.H;
+        const float l = part_ml[2 * sl + 1];
+        const float w = l > 0.f ? exp2f(part_ml[2 * sl] - M) : 0.f;
+        wsp[sp] = w;
+        L += l * w;
     }
-    const float inv = L > 0.f ? 1.f / L : 0.f;
-    if (a.lse && threadIdx.x == 0) a.lse[static_cast<int64_t>(row) * a.H + h] = lse_of(M, L);
-    __nv_bfloat16* o = static_cast<__nv_bfloat16*>(a.out) +
-                       (static_cast<int64_t>(row) * a.H + h) * a.Dv;
-    for (int d = threadIdx.x; d < a.Dv; d += blockDim.x) {
-        float acc = 0.f;
-        for (int sp = 0; sp < n_splits; ++sp) {
-            const int64_t slot = (static_cast<int64_t>(row) * n_splits + sp) * a.H + h;
-            if (part_ml[2 * slot + 1] > 0.f)
-                acc += part_o[slot * a.Dv + d] * exp2f(part_ml[2 * slot] - M);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(kFull, L, o);
+    __shared__ float lsum[kCombineThreads / 32];
+    __syncthreads();  // every split weight written
+    if ((tid & 31) == 0) lsum[tid >> 5] = L;
+    __syncthreads();
+    float Lt = 0.f;
+    for (int w = 0; w < kCombineThreads / 32; ++w) Lt += lsum[w];
+    const float inv = Lt > 0.f ? 1.f / Lt : 0.f;
+    if (a.lse && tid == 0) a.lse[static_cast<int64_t>(row) * a.H + h] = lse_of(M, Lt);
+    __nv_bfloat16* o = static_cast<__nv_bfloat16*>(a.out) + (static_cast<int64_t>(row) * a.H + h) * a.Dv;
+    if ((a.Dv & 3) == 0) {
+        for (int d = 4 * tid; d < a.Dv; d += 4 * kCombineThreads) {
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int sp = 0; sp < n_splits; ++sp) {
+                const float w = wsp[sp];
+                if (w == 0.f) continue;
+                const float4 v = *reinterpret_cast<const float4*>(
+                    part_o + (slot0 + static_cast<int64_t>(sp) * a.H) * a.Dv + d);
+                acc.x = fmaf(w, v.x, acc.x);
+                acc.y = fmaf(w, v.y, acc.y);
+                acc.z = fmaf(w, v.z, acc.z);
+                acc.w = fmaf(w, v.w, acc.w);
+            }
+            o[d] = __float2bfloat16_rn(acc.x * inv);
+            o[d + 1] = __float2bfloat16_rn(acc.y * inv);
+            o[d + 2] = __float2bfloat16_rn(acc.z * inv);
+            o[d + 3] = __float2bfloat16_rn(acc.w * inv);
         }
-        o[d] = __float2bfloat16_rn(acc * inv);
+    } else {
+        for (int d = tid; d < a.Dv; d += kCombineThreads) {
+            float acc = 0.f;
+            for (int sp = 0; sp < n_splits; ++sp) {
+                const float w = wsp[sp];
+                if (w != 0.f)
+                    acc = fmaf(w, part_o[(slot0 + static_cast<int64_t>(sp) * a.H) * a.Dv + d], acc);
+            }
+            o[d] = __float2bfloat16_rn(acc * inv);
+        }
     }
 }
 
@@ -176,7 +221,7 @@ cudaError_t launch_attn_generic(const AttnArgs& a, void* workspace, cudaStream_t
     note_launches(1);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || ns == 1) return e;
-    attn_combine_kernel<<<dim3(rows, a.H), 128, 0, st>>>(a, ns, part_o, part_ml);
+    attn_combine_kernel<<<dim3(rows, a.H), kCombineThreads, 0, st>>>(a, ns, part_o, part_ml);
     note_launches(1);
     return cudaGetLastError();
 }
@@ -187,7 +232,9 @@ namespace tsi {
 
 cudaError_t launch_attn_combine(const AttnArgs& a, int n_splits, const float* part_o,
                                 const float* part_ml, cudaStream_t st) {
-    attn_combine_kernel<<<dim3(a.B * a.T, a.H), 128, 0, st>>>(a, n_splits, part_o, part_ml);
+    if (n_splits > kMaxCombineSplits) return cudaErrorInvalidValue;
+    attn_combine_kernel<<<dim3(a.B * a.T, a.H), kCombineThreads, 0, st>>>(a, n_splits, part_o,
+                                                                           part_ml);
     note_launches(1);
     return cudaGetLastError();
 }
