@@ -65,10 +65,15 @@ struct TileCfg<TSI_BF16> {
     static constexpr int kKSteps = 4;  // per chunk, K = 16 per MMA
 };
 
-template <int QK>
+// R = query rows per unit: the format's default, or 1 for one query per sequence (decode),
+// where the four warp sets of the single row share out the key tiles instead of idling.
+template <int QK, int R = TileCfg<QK>::kRows>
 struct Lay {
     using C = TileCfg<QK>;
-    static constexpr int kR = C::kRows;
+    static constexpr int kR = R;
+    // selector capacity: the row's warp sets offer up to 4 kGroupThreads keys between two
+    // room checks (see the trigger in the epilogue), beyond the k that are kept
+    static constexpr int kCap = R == 1 ? 5120 : C::kCap;
     static constexpr int kN = 64 * kR;             // MMA N
     static constexpr int kAccBufs = kTmemCols / kN;
     static constexpr int kSubs = 4 / kR;           // warp sets per row sharing out the tiles
@@ -77,7 +82,7 @@ struct Lay {
     static constexpr int kStageBytes = C::kChunks * kChunkBytes;
     static constexpr int kQChunkBytes = kN * 128;  // kN rows of 128 bytes per K chunk
     static constexpr int kQBytes = C::kChunks * kQChunkBytes;
-    static constexpr int kSelBytes = (selector_smem_bytes<C::kCap>() + 15) & ~15;
+    static constexpr int kSelBytes = (selector_smem_bytes<kCap>() + 15) & ~15;
     static constexpr uint32_t kIdesc = tc::instr_desc(C::kFmt, kTileKeys, kN);
     static constexpr int kBars = 2 * C::kStages + 2 * kAccBufs + 3;
     static constexpr int kSmem = 1024 /* alignment slack */ + C::kStages * kStageBytes +
@@ -191,13 +196,12 @@ __device__ __forceinline__ float tile_score(uint32_t tmem, int quad, int r, int 
     return mine;
 }
 
-template <int QK>
+template <int QK, int R>
 __global__ void __launch_bounds__(kThreads, 1)
     tsi_indexer_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                           const __grid_constant__ CUtensorMap tmap_q, const TcParams p) {
     using C = TileCfg<QK>;
-    using L = Lay<QK>;
-    constexpr int R = L::kR;
+    using L = Lay<QK, R>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -337,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int sub = (ew >> 2) % L::kSubs;  // this warp scores tiles i with i % kSubs == sub
         const int quad = warp & 3;  // TMEM lanes [32*quad, 32*quad+32) this warp may read
         const int gtid = (ew % (4 * L::kSubs)) * 32 + lane;
-        TopKSelector<L::kGroupThreads, C::kCap> sel;
+        TopKSelector<L::kGroupThreads, L::kCap> sel;
         sel.bind(sel_mem + r * L::kSelBytes, gtid, 1 + r, p.err);
         int acc_base = 0;  // accumulator counter of the unit's first tile
         for (int u = blockIdx.x; u < p.n_units; u += gridDim.x) {
@@ -387,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // One barrier: each thread's count may miss the other warps' offers of the
                 // last round (at most 2 NT keys), and this round adds at most 2 NT more, so
                 // the trigger leaves 4 NT of room.  The rows then settle their exact counts.
-                constexpr int kTrigger = C::kCap - 4 * L::kGroupThreads;
+                constexpr int kTrigger = L::kCap - 4 * L::kGroupThreads;
                 if (tc::bar_red_or(kAllBar, 32 * kEpiWarps, sel.count() > kTrigger)) {
                     const int held = sel.settled_count();
                     if (held > (p.topk + kTrigger) / 2)
@@ -432,14 +436,15 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// Row-major [rows, 128 elements] tensor, 128-row boxes of 128 bytes, 128-byte swizzle.
-bool encode_rows128(CUtensorMap* map, const void* ptr, int64_t rows, int qk_dtype) {
+// Row-major [rows, 128 elements] tensor, boxes of box_rows rows x 128 bytes, 128-byte swizzle.
+bool encode_rows128(CUtensorMap* map, const void* ptr, int64_t rows, int qk_dtype,
+                    uint32_t box_rows = 128) {
     auto fn = encode_fn();
     if (!fn) return false;
     const bool bf16 = qk_dtype == TSI_BF16;
     cuuint64_t dims[2] = {128, static_cast<cuuint64_t>(rows)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(bf16 ? 256 : 128)};
-    cuuint32_t box[2] = {bf16 ? 64u : 128u, 128u};
+    cuuint32_t box[2] = {bf16 ? 64u : 128u, box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
                     const_cast<void*>(ptr), dims, strides, box, estr,
@@ -450,11 +455,13 @@ bool encode_rows128(CUtensorMap* map, const void* ptr, int64_t rows, int qk_dtyp
 
 constexpr int kPlanSMs = 152;
 
-int rows_per_unit(int qk_dtype) { return qk_dtype == TSI_E4M3 ? 4 : 2; }
+int rows_per_unit(int qk_dtype, int T) {
+    return T == 1 ? 1 : qk_dtype == TSI_E4M3 ? TileCfg<TSI_E4M3>::kRows : TileCfg<TSI_BF16>::kRows;
+}
 
 // Key chunks per row for decode-sized requests (too few units to fill the GPU).
 void tc_plan(int qk_dtype, int B, int T, int S, int* n_chunks, int* chunk_keys) {
-    const int R = rows_per_unit(qk_dtype);
+    const int R = rows_per_unit(qk_dtype, T);
     const int64_t groups = static_cast<int64_t>(B) * ((T + R - 1) / R);
     int nc = 1;
     if (groups < kPlanSMs && S > 4096) {
@@ -482,11 +489,14 @@ int sm_count() {
     return n;
 }
 
-template <int QK>
+template <int QK, int R>
 cudaError_t launch_qk(const IndexerArgs& a, void* workspace, cudaStream_t st) {
+    using L = Lay<QK, R>;
     CUtensorMap tk, tq;
+    // the query box is one unit's rows (64 per query row), at most 128 per copy
     if (!encode_rows128(&tk, a.kI, static_cast<int64_t>(a.B) * a.S, QK) ||
-        !encode_rows128(&tq, a.qI, static_cast<int64_t>(a.B) * a.T * 64, QK))
+        !encode_rows128(&tq, a.qI, static_cast<int64_t>(a.B) * a.T * 64, QK,
+                        L::kN < 128 ? L::kN : 128))
         return cudaErrorInvalidValue;
     TcParams p{};
     p.w = a.w;
@@ -502,7 +512,6 @@ cudaError_t launch_qk(const IndexerArgs& a, void* workspace, cudaStream_t st) {
     p.score = a.score;
     p.err = a.err;
     tc_plan(QK, a.B, a.T, a.S, &p.n_chunks, &p.chunk_keys);
-    constexpr int R = Lay<QK>::kR;
     const int64_t groups = static_cast<int64_t>(a.B) * ((a.T + R - 1) / R);
     p.n_units = static_cast<int>(groups * p.n_chunks);
     const int rows = a.B * a.T;
@@ -514,12 +523,12 @@ cudaError_t launch_qk(const IndexerArgs& a, void* workspace, cudaStream_t st) {
         p.cand_cnt =
             reinterpret_cast<int*>(p.cand + static_cast<size_t>(rows) * p.n_chunks * a.topk);
     }
-    constexpr int smem = Lay<QK>::kSmem;
-    cudaError_t e = cudaFuncSetAttribute(tsi_indexer_tc_kernel<QK>,
+    constexpr int smem = L::kSmem;
+    cudaError_t e = cudaFuncSetAttribute(tsi_indexer_tc_kernel<QK, R>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const int grid = p.n_units < sm_count() ? p.n_units : sm_count();
-    tsi_indexer_tc_kernel<QK><<<grid, kThreads, smem, st>>>(tk, tq, p);
+    tsi_indexer_tc_kernel<QK, R><<<grid, kThreads, smem, st>>>(tk, tq, p);
     note_launches(1);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -558,8 +567,12 @@ size_t tc_indexer_split_workspace_bytes(int qk_dtype, int B, int T, int S, int t
 
 cudaError_t launch_indexer_tc(const IndexerArgs& a, void* workspace, cudaStream_t st) {
     if (a.B * a.T == 0) return cudaSuccess;
-    return a.qk_dtype == TSI_E4M3 ? launch_qk<TSI_E4M3>(a, workspace, st)
-                                  : launch_qk<TSI_BF16>(a, workspace, st);
+    if (rows_per_unit(a.qk_dtype, a.T) == 1)
+        return a.qk_dtype == TSI_E4M3 ? launch_qk<TSI_E4M3, 1>(a, workspace, st)
+                                      : launch_qk<TSI_BF16, 1>(a, workspace, st);
+    return a.qk_dtype == TSI_E4M3
+               ? launch_qk<TSI_E4M3, TileCfg<TSI_E4M3>::kRows>(a, workspace, st)
+               : launch_qk<TSI_BF16, TileCfg<TSI_BF16>::kRows>(a, workspace, st);
 }
 
 }  // namespace tsi
