@@ -80,6 +80,13 @@ def test_decode_two_stage_merge_integer_exact(cuda_lib, B, kv):
                    71 + B, exact=True, kv_len=kv)
 
 
+def test_decode_bf16_integer_exact(cuda_lib):
+    # one query per sequence with bf16 operands (the one-row tensor-core units of the bf16
+    # format); integers in [-8, 8] are exact in bf16, so the rows match the oracle exactly
+    _run_and_check(cuda_lib, 3, 1, 20000, 64, 128, 2048, "bf16", "bf16", "int8", "pow2", 81,
+                   exact=True, kv_len=[20000, 7001, 3])
+
+
 def test_decode_generic_heads_split_merge(cuda_lib):
     # few rows + long cache: keys split over blocks and merged (CUDA-core path)
     _run_and_check(cuda_lib, 4, 1, 30000, 4, 32, 512, "f32", "f32", "int4", "int03", 61,
