@@ -68,6 +68,17 @@ def _profiled_traffic(kernel, src_files, workload):
     return None
 
 
+def _kernel_files(kernel):
+    """Source files that define a kernel's device code (its traffic is keyed to them)."""
+    return {
+        "tsi_attn_tc_kernel": ["attn_tc.cu", "latent_gather.cuh", "tc_common.cuh"],
+        "attn_generic_kernel": ["attn_generic.cu"],
+        "tsi_indexer_tc_kernel": ["indexer_tc.cu", "topk_select.cuh", "tc_common.cuh"],
+        "indexer_generic_kernel": ["indexer_generic.cu", "topk_select.cuh"],
+        "tsi_index_kl_tc_kernel": ["index_kl_tc.cu", "latent_gather.cuh", "tc_common.cuh"],
+    }[kernel]
+
+
 def _traffic_workload(cfg, what):
     """Name of a captured workload in profiles/traffic.txt: whole prefills of one sequence."""
     if cfg.B != 1 or cfg.T != cfg.S:
@@ -243,8 +254,7 @@ def run_gpu(args, rank, world):
     roof_attn = {"kernel": attn_kernel, "bound": "hbm", "achieved": round(attn_achieved, 1),
                  "peak": peaks["hbm_gbs"], "unit": "GB/s",
                  "frac": round(attn_achieved / peaks["hbm_gbs"], 4),
-                 "traffic": _profiled_traffic(attn_kernel, ["attn_tc.cu", "attn_generic.cu",
-                                                             "latent_gather.cuh"],
+                 "traffic": _profiled_traffic(attn_kernel, _kernel_files(attn_kernel),
                                               _traffic_workload(cfg, "layer")),
                  "algorithmic_bytes_per_launch": attn_bytes, "ms_per_launch": round(ms_attn, 4),
                  "tc_tflops": round(attn_tc, 1),
@@ -252,8 +262,7 @@ def run_gpu(args, rank, world):
     roof_idx = {"kernel": idx_kernel, "bound": "tensor", "achieved": round(idx_achieved, 1),
                 "peak": round(tc_peak, 1), "unit": "TFLOP/s",
                 "frac": round(idx_achieved / tc_peak, 4),
-                "traffic": _profiled_traffic(idx_kernel, ["indexer_tc.cu", "indexer_generic.cu",
-                                                          "topk_select.cuh"],
+                "traffic": _profiled_traffic(idx_kernel, _kernel_files(idx_kernel),
                                              _traffic_workload(cfg, "group")),
                 "algorithmic_flops_per_launch": idx_flops, "ms_per_launch": round(ms_idx, 4),
                 "peak_source": f"{peaks['source']} bf16 sustained x {FP8_PER_BF16:g} (fp8)"
@@ -522,8 +531,7 @@ def measure_index_kl(cfg, ind, lay, idx, outs, ws, stream, reps=2):
             "roofline": {"kernel": kernel, "bound": "hbm", "achieved": round(achieved, 1),
                          "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": round(achieved / peaks["hbm_gbs"], 4),
-                         "traffic": _profiled_traffic(kernel, ["index_kl_tc.cu",
-                                                               "latent_gather.cuh"],
+                         "traffic": _profiled_traffic(kernel, _kernel_files(kernel),
                                                       _traffic_workload(cfg, "group_kl")),
                          "algorithmic_bytes_per_launch": nbytes,
                          "tc_tflops": round(flops / (ms / 1e3) / 1e12, 1),
