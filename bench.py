@@ -192,7 +192,7 @@ def run_gpu(args, rank, world):
                 b = torch.cuda.Event(enable_timing=True)
                 b.record(stream)
                 ev["idx"].append((a, b))
-            for l0 in range(cfg.group):
+            for l0 in range(min(cfg.group, cfg.n_layers - g * cfg.group)):
                 Q, K, V = lay[g * cfg.group + l0]
                 if record:
                     a = torch.cuda.Event(enable_timing=True)
@@ -229,7 +229,7 @@ def run_gpu(args, rank, world):
         dist.barrier()
     ms_step = ms_total / args.steps
     ms_idx = statistics.mean(a.elapsed_time(b) for a, b in ev["idx"])
-    ms_attn = statistics.mean(a.elapsed_time(b) for a, b in ev["attn"])
+    ms_attn = statistics.mean(a.elapsed_time(b) for a, b in ev["attn"]) if ev["attn"] else 0.0
 
     # --- rates and roofline ------------------------------------------------------------
     rows = cfg.B * cfg.T
@@ -244,8 +244,9 @@ def run_gpu(args, rank, world):
     idx_achieved = idx_flops / (ms_idx / 1e3) / 1e12
     attn_bytes = accounting.attn_bytes(valid_k, rows, cfg.H, cfg.Hkv, cfg.Dqk, cfg.Dv,
                                        cfg.topk, cfg.v_from_k)
-    attn_achieved = attn_bytes / (ms_attn / 1e3) / 1e9
-    attn_tc = accounting.attn_flops(valid_k, cfg.H, cfg.Dqk, cfg.Dv) / (ms_attn / 1e3) / 1e12
+    attn_achieved = attn_bytes / (ms_attn / 1e3) / 1e9 if ms_attn else 0.0
+    attn_tc = accounting.attn_flops(valid_k, cfg.H, cfg.Dqk, cfg.Dv) / (ms_attn / 1e3) / 1e12 \
+        if ms_attn else 0.0
     qk_code = tsi.E4M3 if cfg.qk_dtype == "e4m3" else tsi.BF16 if cfg.qk_dtype == "bf16" else tsi.F32
     attn_kernel = "tsi_attn_tc_kernel" if tsi.attn_path(cfg.H, cfg.Hkv, cfg.Dqk, cfg.Dv,
                                                         cfg.v_from_k) == 1 else "attn_generic_kernel"
@@ -317,7 +318,8 @@ def run_gpu(args, rank, world):
         result["overlap"] = measure_overlap(cfg, ind, idx, ws, stream)
     if not args.no_cp:
         result["context_parallel"] = measure_cp(cfg, ind, idx, stream)
-    if not args.no_kl and tsi.attn_path(cfg.H, cfg.Hkv, cfg.Dqk, cfg.Dv, cfg.v_from_k) == 1:
+    if not args.no_kl and cfg.n_layers >= 1 and \
+            tsi.attn_path(cfg.H, cfg.Hkv, cfg.Dqk, cfg.Dv, cfg.v_from_k) == 1:
         result["index_kl"] = measure_index_kl(cfg, ind, lay, idx, outs, ws, stream)
 
     # --- end to end through the C ABI with host buffers ---------------------------------
@@ -561,11 +563,16 @@ def run_e2e(args, cfg, ind, lay, idx, outs, ws, stream, world, n_copy_streams=4)
     h_ind = tuple(pin(x) for x in ind[0])
     for hx, dx in zip(h_ind, ind[0]):
         hx.copy_(dx)
-    Q0, K0, _ = lay[0]
-    h_Q, h_K = pin(Q0), pin(K0)
-    h_Q.copy_(Q0)
-    h_K.copy_(K0)
-    h_O = pin(outs[0])
+    h_Q = h_K = h_V = h_O = None
+    if nl:  # one pinned host copy of a layer's Q and latent serves every layer's upload
+        Q0, K0, V0 = lay[0]
+        h_Q, h_K = pin(Q0), pin(K0)
+        h_Q.copy_(Q0)
+        h_K.copy_(K0)
+        h_V = None if V0 is None else pin(V0)
+        if h_V is not None:
+            h_V.copy_(V0)
+        h_O = pin(outs[0])
     h_idx = pin(idx)
     idx_bufs = [idx, torch.empty_like(idx)]
     ups = [torch.cuda.Stream(device=idx.device) for _ in range(n_copy_streams)]
@@ -609,12 +616,15 @@ def run_e2e(args, cfg, ind, lay, idx, outs, ws, stream, world, n_copy_streams=4)
                 evs += split_copy(dx, hx, ups, [idx_done[g]])
                 h2d += hx.numel() * hx.element_size()
             ind_ready.append(evs)
-            for l0 in range(cfg.group):
+            for l0 in range(min(cfg.group, nl - g * cfg.group)):
                 layer = g * cfg.group + l0
-                Q, K, _ = lay[layer]
+                Q, K, V = lay[layer]
                 evs = split_copy(Q, h_Q, ups, [attn_done[layer]])
                 evs += split_copy(K, h_K, ups, [attn_done[layer]])
                 h2d += h_Q.numel() * 2 + h_K.numel() * 2
+                if V is not None:  # separate values (MHA); the MQA latent carries them
+                    evs += split_copy(V, h_V, ups, [attn_done[layer]])
+                    h2d += h_V.numel() * 2
                 in_ready.append(evs)
         for g in range(G):
             qI, kI, w = ind[g]
@@ -629,7 +639,7 @@ def run_e2e(args, cfg, ind, lay, idx, outs, ws, stream, world, n_copy_streams=4)
             idx_done[g] = e
             idx_read[g % 2] = split_copy(h_idx, ib, downs, [e])
             d2h += ib.numel() * ib.element_size()
-            for l0 in range(cfg.group):
+            for l0 in range(min(cfg.group, nl - g * cfg.group)):
                 layer = g * cfg.group + l0
                 Q, K, V = lay[layer]
                 for e in in_ready[layer]:
@@ -695,22 +705,26 @@ def run_cpu_oracle(cfg_id, budget_s, on_device=None):
     t_idx = time.perf_counter() - t0
     work_idx = sum(n_keys(r) for r in rows)
     t_idx_full = t_idx * accounting.causal_pairs(cfg.B, T, S) / work_idx
-    # attention: 4 layers on a subset of those rows
+    # attention: the group's layers on a subset of those rows
     n_att = max(cores, 16)
     arows = rows[:n_att]
-    K = draw((cfg.B, S, cfg.Hkv, cfg.Dqk), "normal", "bf16", 4, "cpu")
-    Qr = draw((len(arows), cfg.H, cfg.Dqk), "normal", "bf16", 5, "cpu")
-    t0 = time.perf_counter()
-    for _ in range(cfg.group):
-        oracle.sparse_attn(Qr, K, None, idx_rows[:len(arows)], cfg.scale, T, arows, Dv=cfg.Dv)
-    t_att = time.perf_counter() - t0
-    work_att = cfg.group * sum(min(cfg.topk, n_keys(r)) for r in arows)
-    t_att_full = t_att * cfg.group * accounting.selected_pairs(cfg.B, T, S, cfg.topk) / work_att
+    n_lay = min(cfg.group, cfg.n_layers)
+    t_att = t_att_full = 0.0
+    if n_lay:
+        K = draw((cfg.B, S, cfg.Hkv, cfg.Dqk), "normal", "bf16", 4, "cpu")
+        Qr = draw((len(arows), cfg.H, cfg.Dqk), "normal", "bf16", 5, "cpu")
+        V = None if cfg.v_from_k else draw((cfg.B, S, cfg.Hkv, cfg.Dv), "normal", "bf16", 6, "cpu")
+        t0 = time.perf_counter()
+        for _ in range(n_lay):
+            oracle.sparse_attn(Qr, K, V, idx_rows[:len(arows)], cfg.scale, T, arows, Dv=cfg.Dv)
+        t_att = time.perf_counter() - t0
+        work_att = n_lay * sum(min(cfg.topk, n_keys(r)) for r in arows)
+        t_att_full = t_att * n_lay * accounting.selected_pairs(cfg.B, T, S, cfg.topk) / work_att
     t_group = t_idx_full + t_att_full
     return {"value": round(cfg.B * T / t_group, 4), "unit": UNIT, "cores": cores,
             "kind": "oracle",
             "sample": f"{len(rows)} stratified query rows (indexer + top-k, fp64) and "
-                      f"{len(arows)} of them x {cfg.group} layers (sparse attention, fp64) of "
+                      f"{len(arows)} of them x {n_lay} layers (sparse attention, fp64) of "
                       f"one IndexShare group ({cfg.B} x {T} query rows over L={S}); scaled "
                       f"by causal pairs / selected keys",
             "sample_seconds": round(t_idx + t_att, 2)}
