@@ -80,3 +80,18 @@ def test_layers_share_index_but_not_outputs(cuda_lib):
     outs = _run(cuda_lib, 1, 64, 64, 4, 4, 64, 64, 16, False, 4, 600)
     for l in range(1, 4):
         assert not torch.equal(outs[0], outs[l])
+
+
+@pytest.mark.parametrize("topk", [65, 129, 1000])
+def test_mqa_latent_ragged_half_tiles(cuda_lib, topk):
+    # the tensor-core kernel takes keys 64 at a time: a last half-tile with 1, 1 or 40 keys,
+    # padding anywhere in the rows, two sequences of different lengths
+    rows = np.unique(np.r_[0, 1, np.linspace(0, 399, 20).astype(int), 199, 200, 399])
+    _run(cuda_lib, 2, 200, 1500, 64, 1, 576, 512, topk, True, 1, 700 + topk,
+         kv_len=[1500, 700], pad_frac=0.2, rows=rows)
+
+
+def test_mqa_latent_decode_one_half_tile_per_split(cuda_lib):
+    # four rows of 128 keys: every row splits into two CTAs of one 64-key half-tile each
+    _run(cuda_lib, 4, 1, 5000, 64, 1, 576, 512, 128, True, 2, 800,
+         kv_len=[5000, 129, 64, 2000])
