@@ -213,7 +213,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             tc::mma_commit(&sm.done[0]);
-            tc::mbar_wait(&sm.done[0], 0, abort, p.err);
+            if (!tc::mbar_wait(&sm.done[0], 0, abort, p.err))
+                tc::mbar_drain(&sm.done[0], 0);  // issued MMAs finish before TMEM is freed
         } else if (lane == 0) {
             int it = 0, un = 0;
             for (int u = blockIdx.x; u < p.n_units; u += gridDim.x, ++un) {
@@ -245,7 +246,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc::mma_commit(&sm.o_full);
             }
             tc::mma_commit(&sm.done[1]);
-            tc::mbar_wait(&sm.done[1], 0, abort, p.err);
+            if (!tc::mbar_wait(&sm.done[1], 0, abort, p.err))
+                tc::mbar_drain(&sm.done[1], 0);  // issued MMAs finish before TMEM is freed
         }
     } else if (warp > kPvWarp) {
         // ------------------------------------------------------------ gather

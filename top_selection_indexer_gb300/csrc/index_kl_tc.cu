@@ -177,7 +177,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             tc::mma_commit(&sm.done);
-            tc::mbar_wait(&sm.done, 0, abort, p.err);
+            if (!tc::mbar_wait(&sm.done, 0, abort, p.err))
+                tc::mbar_drain(&sm.done, 0);  // issued MMAs finish before TMEM is freed
         }
     } else if (warp > kMmaWarp) {
         // ------------------------------------------------------------ gather

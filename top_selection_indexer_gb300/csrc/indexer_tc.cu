@@ -253,10 +253,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             int s = 0;
             uint32_t ph = 0;  // phase of the ring slot s
             int unit_it = 0;
+            int q_last = -1;  // unit of the last query load issued
+            uint32_t loaded = 0, last_ph = 0;  // per slot (bit s): loaded once, last phase
             for (int u = blockIdx.x; u < p.n_units; u += gridDim.x, ++unit_it) {
                 const Unit U = unit_of<R>(p, u);
                 tc::mbar_wait(qempty, (unit_it & 1) ^ 1, abort, p.err);
                 if (!*abort) {
+                    q_last = unit_it;
                     tc::mbar_expect_tx(qfull, L::kQBytes);
                     const int qrow = (U.b * p.T + U.t_hi - (R - 1)) * 64;
                     for (int c = 0; c < C::kChunks; ++c)
@@ -267,6 +270,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int i = 0; i < U.ntiles; ++i) {
                     const bool ready = tc::mbar_try_wait(&empty[s], ph ^ 1);
                     if (wait_fast(&empty[s], ph ^ 1, ready, abort, p.err) && !*abort) {
+                        loaded |= 1u << s;
+                        last_ph = (last_ph & ~(1u << s)) | (ph << s);
                         tc::mbar_expect_tx(&full[s], L::kStageBytes);
                         const int krow = static_cast<int>(static_cast<int64_t>(U.b) * p.S + U.key_lo +
                                                           static_cast<int64_t>(i) * kTileKeys);
@@ -279,6 +284,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ph ^= 1;
                     }
                 }
+            }
+            if (*abort) {  // loads still in flight must land before the CTA exits (at most
+                           // one per slot: a slot is reloaded only after its data was used)
+                if (q_last >= 0) tc::mbar_drain(qfull, q_last & 1);
+                for (int i = 0; i < C::kStages; ++i)
+                    if ((loaded >> i) & 1u) tc::mbar_drain(&full[i], (last_ph >> i) & 1u);
             }
         }
     } else if (warp == 1) {
@@ -332,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // every MMA issued by this thread has finished before TMEM is released
             tc::mma_commit(done);
-            tc::mbar_wait(done, 0, abort, p.err);
+            if (!tc::mbar_wait(done, 0, abort, p.err)) tc::mbar_drain(done, 0);
         }
     } else {
         // ------------------------------------------------------------ epilogue groups

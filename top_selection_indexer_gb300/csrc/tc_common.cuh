@@ -70,6 +70,16 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     return true;
 }
 
+// Bounded wait that ignores the abort flag: after an abort, for the asynchronous work this
+// thread has already started (MMAs, TMA loads) to finish before shared memory or TMEM is
+// given up.  Returns false if the bound runs out.
+__device__ __forceinline__ bool mbar_drain(uint64_t* bar, uint32_t parity) {
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity))
+        if (clock64() - t0 > kWaitCycles) return false;
+    return true;
+}
+
 // 2D tiled TMA load into shared memory, completing on `bar` (tx bytes).
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
                                             uint64_t* bar) {
