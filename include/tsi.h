@@ -291,6 +291,17 @@ tsi_status tsi_topk_overlap(const int32_t* idx_a, const int32_t* idx_b, int rows
                             int32_t* inter, int32_t* card_a, void* stream);
 
 /*
+ * Self-test of the failure path, for tests of error handling without a GPU fault.  Launches
+ * one block in which a single thread waits, through the same bounded-wait helper the
+ * tensor-core kernels use, on an mbarrier that nothing completes.  After the wait's clock
+ * budget (about a second) the helper sets the device error word and the kernel returns:
+ * nothing faults, traps or spins without bound.  tsi_device_status(stream) then returns
+ * TSI_ERR_TIMEOUT (and clears the word), and the context stays usable.  Returns TSI_OK once
+ * launched.
+ */
+tsi_status tsi_selftest_wait_timeout(void* stream);
+
+/*
  * Waits for `stream`, then reads and clears the device error word of the current
  * device.  Returns TSI_OK, TSI_ERR_TIMEOUT (a bounded wait ran out),
  * TSI_ERR_DEVICE_ASSERT (a device check failed) or TSI_ERR_CUDA.

@@ -26,7 +26,8 @@ EXPORTS = ("tsi_indexer_topk_workspace", "tsi_indexer_topk", "tsi_sparse_attn_wo
            "tsi_launch_count", "tsi_indexer_topk_noalloc", "tsi_indexer_topk_noalloc_limit",
            "tsi_indexer_topk_path", "tsi_sparse_attn_path", "tsi_index_share_layers",
            "tsi_topk_overlap", "tsi_indexer_topk_shard_workspace", "tsi_indexer_topk_shard",
-           "tsi_topk_merge", "tsi_sparse_attn_group_lse", "tsi_index_kl")
+           "tsi_topk_merge", "tsi_sparse_attn_group_lse", "tsi_index_kl",
+           "tsi_selftest_wait_timeout")
 
 
 class TSIError(RuntimeError):
@@ -91,6 +92,8 @@ def load():
             lib.tsi_index_kl.argtypes = [i32, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp, vp,
                                          i32, vp, vp, vp, vp, vp]
             lib.tsi_index_kl.restype = i32
+            lib.tsi_selftest_wait_timeout.argtypes = [vp]
+            lib.tsi_selftest_wait_timeout.restype = i32
             _lib = lib
     return _lib
 
@@ -286,6 +289,12 @@ def index_kl(qs, ks, lses, idx, score, scale, kv_len=None, want_grad=False, want
     if want_pbar or pbar is not None:
         out += (pbar,)
     return out[0] if len(out) == 1 else out
+
+
+def selftest_wait_timeout(stream=None):
+    """Launch the failure-path self-test (tsi_selftest_wait_timeout): a bounded device
+    wait that runs out; device_status() afterwards raises TSIError(ERR_TIMEOUT)."""
+    _check(load().tsi_selftest_wait_timeout(_stream_handle(stream)))
 
 
 def device_status(stream=None):

@@ -41,6 +41,10 @@ struct IndexKlArgs {
     unsigned* err;
 };
 bool tc_index_kl_supported(int H, int Dqk);
+
+// One thread waits on an mbarrier that nothing completes; the bounded wait runs out and
+// sets kErrTimeout in `err` (self-test of the failure path).
+cudaError_t launch_wait_timeout_probe(unsigned* err, cudaStream_t st);
 cudaError_t launch_index_kl_tc(const IndexKlArgs& a, cudaStream_t st);
 
 }  // namespace tsi

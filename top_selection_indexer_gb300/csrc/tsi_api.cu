@@ -332,6 +332,15 @@ tsi_status tsi_index_kl(int n_layers, const void* const* q, const void* const* k
     return ok();
 }
 
+tsi_status tsi_selftest_wait_timeout(void* stream) {
+    unsigned* err = nullptr;
+    tsi_status st = device_error_word(&err);
+    if (st != TSI_OK) return st;
+    cudaError_t e = tsi::launch_wait_timeout_probe(err, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(TSI_ERR_CUDA, "self-test launch: %s", cudaGetErrorString(e));
+    return ok();
+}
+
 tsi_status tsi_index_share_layers(int n_layers, int freq, int skip_offset, const char* pattern,
                                   int32_t* anchor) {
     if (n_layers < 0) return fail(TSI_ERR_INVALID_ARG, "n_layers=%d", n_layers);
