@@ -73,7 +73,8 @@ def _kernel_files(kernel):
     return {
         "tsi_attn_tc_kernel": ["attn_tc.cu", "latent_gather.cuh", "tc_common.cuh"],
         "attn_generic_kernel": ["attn_generic.cu"],
-        "tsi_indexer_tc_kernel": ["indexer_tc.cu", "topk_select.cuh", "tc_common.cuh"],
+        "tsi_indexer_tc_kernel": ["indexer_tc.cu", "topk_rows.cu", "topk_select.cuh",
+                                  "rank_sort.cuh", "tc_common.cuh"],
         "indexer_generic_kernel": ["indexer_generic.cu", "topk_select.cuh"],
         "tsi_index_kl_tc_kernel": ["index_kl_tc.cu", "latent_gather.cuh", "tc_common.cuh"],
     }[kernel]

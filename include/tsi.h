@@ -57,10 +57,14 @@ typedef enum { TSI_F32 = 0, TSI_BF16 = 1, TSI_E4M3 = 2 } tsi_dtype;
 
 /*
  * Workspace bytes needed by tsi_indexer_topk for these sizes (0 when none is needed).
- * The workspace holds candidate lists of 8-byte keys, topk per row and key split,
- * plus a count per list: the tensor-core path always leaves each row's best keys there
- * unordered for a ranking pass; the CUDA-core path only when rows are few and key
- * ranges are split across thread blocks (decode).
+ *   - Tensor-core path, T > 1: the fp32 scores of one chunk of query rows, rows of
+ *     S (rounded up to 4) floats for every sequence, the chunk as many rows as fit in
+ *     about 8 GiB (all T rows when they fit; at least the rows of one tensor-core unit).
+ *     The rows are scored chunk by chunk, then each row's top-k is selected from its
+ *     stored scores.
+ *   - Tensor-core path, T = 1 (decode), and the CUDA-core path when rows are few and key
+ *     ranges are split across thread blocks: candidate lists of 8-byte keys, topk per row
+ *     and key split, plus a count per list (and merge staging space).
  */
 size_t tsi_indexer_topk_workspace(int B, int T, int S, int H_I, int d_I, int topk,
                                   int qk_dtype);
@@ -224,8 +228,10 @@ tsi_status tsi_index_kl(int n_layers, const void* const* q, const void* const* k
  *   cand_cnt  [B*T] int32 (out): how many keys of the row the shard holds, at most topk
  *
  * Requires 0 <= key_offset, key_offset + S_shard <= S_total, and
- * workspace_bytes >= tsi_indexer_topk_shard_workspace(...) (0 unless rows are few enough
- * that keys are split across thread blocks).  Other rules as tsi_indexer_topk.
+ * workspace_bytes >= tsi_indexer_topk_shard_workspace(...): the stored scores of the
+ * tensor-core path for T > 1 (as tsi_indexer_topk_workspace describes, with S_shard
+ * keys), else 0 unless rows are few enough that keys are split across thread blocks.
+ * Other rules as tsi_indexer_topk.
  */
 size_t tsi_indexer_topk_shard_workspace(int B, int T, int S_shard, int H_I, int d_I, int topk,
                                         int qk_dtype);

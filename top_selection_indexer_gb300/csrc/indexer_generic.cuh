@@ -72,6 +72,29 @@ cudaError_t launch_topk_merge_two_stage(int rows, int topk, int n_lists, const u
                                         uint64_t* out_keys, int* out_cnt, unsigned* err,
                                         cudaStream_t st);
 
+// Stored score rows of one chunk of query rows (the two-pass tensor-core indexer): row
+// rr = b * rows + (t - t0) of `scores` (stride ld floats, a multiple of 4, 16-byte aligned
+// base) holds I[b, t, s] for the call's keys s = 0 .. n_t - 1, n_t = min(S, p_t + 1 -
+// key_offset) (p_t the row's position in the whole cache).  Each row's top-k (positions
+// in the whole cache) goes rank-ordered to idx / score [(b * T + t) * topk ..] (score may
+// be null), or, when idx is null, as unordered 64-bit rank keys to cand[(b * T + t) *
+// topk ..] with its count at cand_cnt[b * T + t].
+struct ScoreRows {
+    const float* scores;
+    int64_t ld;
+    int B, T, S, S_total, topk;
+    int t0, rows;
+    int64_t key_offset;
+    const int32_t* kv_len;
+    int32_t* idx;
+    float* score;
+    uint64_t* cand;
+    int* cand_cnt;
+    unsigned* err;
+};
+size_t topk_rows_smem_bytes();
+cudaError_t launch_topk_rows(const ScoreRows& r, cudaStream_t st);
+
 // Rank one unordered list of at most topk distinct keys per row ([rows][topk] keys +
 // counts) into rank-ordered idx / score rows.
 cudaError_t launch_topk_rank(int rows, int topk, const uint64_t* cand, const int* cand_cnt,

@@ -67,7 +67,7 @@ struct TileCfg<TSI_BF16> {
 
 // R = query rows per unit: the format's default, or 1 for one query per sequence (decode),
 // where the four warp sets of the single row share out the key tiles instead of idling.
-template <int QK, int R = TileCfg<QK>::kRows>
+template <int QK, int R = TileCfg<QK>::kRows, bool kStore = false>
 struct Lay {
     using C = TileCfg<QK>;
     static constexpr int kR = R;
@@ -82,7 +82,8 @@ struct Lay {
     static constexpr int kStageBytes = C::kChunks * kChunkBytes;
     static constexpr int kQChunkBytes = kN * 128;  // kN rows of 128 bytes per K chunk
     static constexpr int kQBytes = C::kChunks * kQChunkBytes;
-    static constexpr int kSelBytes = (selector_smem_bytes<kCap>() + 15) & ~15;
+    // the store variant keeps no selector: scores go to global memory
+    static constexpr int kSelBytes = kStore ? 0 : (selector_smem_bytes<kCap>() + 15) & ~15;
     static constexpr uint32_t kIdesc = tc::instr_desc(C::kFmt, kTileKeys, kN);
     static constexpr int kBars = 2 * C::kStages + 2 * kAccBufs + 3;
     static constexpr int kSmem = 1024 /* alignment slack */ + C::kStages * kStageBytes +
@@ -103,6 +104,9 @@ struct TcParams {
     uint64_t* cand;
     int* cand_cnt;
     int n_chunks, chunk_keys, n_units;
+    int t_begin, t_end;  // query rows [t_begin, t_end) of every sequence in this launch
+    float* scores;       // store variant: row (b, t) at (b * (t_end - t_begin) + t - t_begin) * ld
+    int64_t ld;
     unsigned* err;
 };
 
@@ -112,8 +116,9 @@ struct Unit {
     int ntiles;
 };
 
-// Unit u: row group j = u / (B * n_chunks) counted from the end of the sequence (longest
-// rows first), sequence b, key chunk.  Rows t_hi - R + 1 .. t_hi (the first may be < 0).
+// Unit u: row group j = u / (B * n_chunks) counted from the end of the launch's rows
+// (longest rows first), sequence b, key chunk.  Rows t_hi - R + 1 .. t_hi (the first may be
+// below t_begin: those belong to another launch and are skipped).
 template <int R>
 __device__ __forceinline__ Unit unit_of(const TcParams& p, int u) {
     Unit U;
@@ -121,7 +126,7 @@ __device__ __forceinline__ Unit unit_of(const TcParams& p, int u) {
     const int pu = u / p.n_chunks;
     const int j = pu / p.B;
     U.b = pu % p.B;
-    U.t_hi = p.T - 1 - R * j;
+    U.t_hi = p.t_end - 1 - R * j;
     // positions relative to key 0 of this call; keys beyond the shard are not here
     const int64_t p_hi = query_position(p.kv_len, U.b, p.T, p.S_total, U.t_hi) - p.key_offset;
     int64_t end = p_hi + 1 > 0 ? p_hi + 1 : 0;
@@ -196,12 +201,12 @@ __device__ __forceinline__ float tile_score(uint32_t tmem, int quad, int r, int 
     return mine;
 }
 
-template <int QK, int R>
+template <int QK, int R, bool kStore>
 __global__ void __launch_bounds__(kThreads, 1)
     tsi_indexer_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                           const __grid_constant__ CUtensorMap tmap_q, const TcParams p) {
     using C = TileCfg<QK>;
-    using L = Lay<QK, R>;
+    using L = Lay<QK, R, kStore>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -353,12 +358,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int quad = warp & 3;  // TMEM lanes [32*quad, 32*quad+32) this warp may read
         const int gtid = (ew % (4 * L::kSubs)) * 32 + lane;
         TopKSelector<L::kGroupThreads, L::kCap> sel;
-        sel.bind(sel_mem + r * L::kSelBytes, gtid, 1 + r, p.err);
+        if (!kStore) sel.bind(sel_mem + r * L::kSelBytes, gtid, 1 + r, p.err);
         int acc_base = 0;  // accumulator counter of the unit's first tile
         for (int u = blockIdx.x; u < p.n_units; u += gridDim.x) {
             const Unit U = unit_of<R>(p, u);
             const int t = U.t_hi - (R - 1) + r;
-            const bool row_ok = t >= 0;
+            const bool row_ok = t >= p.t_begin;
             int64_t limit = 0;  // keys s < limit belong to this row
             float2 w2[8];
 #pragma unroll
@@ -374,21 +379,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                     w2[m] = make_float2(load_elem(p.w, h, p.w_dtype), load_elem(p.w, h + 1, p.w_dtype));
                 }
             }
-            sel.reset();
+            // key of this thread's score in a tile: off; whole-cache position of key 0
+            const int off = quad * 32 + scored_lane(lane);
+            if constexpr (kStore) {
+                // every tile of the row: its scores to the row's stored scores (a warp writes
+                // 32 consecutive keys, one 128-byte line); the selection runs afterwards
+                float* srow = p.scores + (static_cast<int64_t>(U.b) * (p.t_end - p.t_begin) +
+                                          (t - p.t_begin)) * p.ld;
+                for (int i = sub; i < U.ntiles; i += L::kSubs) {
+                    const int acc = acc_base + i;
+                    const int a = acc % L::kAccBufs;
+                    tc::mbar_wait(&tfull[a], (acc / L::kAccBufs) & 1, abort, p.err);
+                    const float sc = tile_score<L::kN>(tmem, quad, r, a, tempty, w2);
+                    const int64_t key = U.key_lo + static_cast<int64_t>(i) * kTileKeys + off;
+                    if (key < limit) srow[key] = sc;
+                }
+                acc_base += U.ntiles;
+                continue;
+            }
             // per round each warp scores two of its tiles, then one room check covers the
             // group's offers of both
+            sel.reset();
+            const uint32_t pos0 = static_cast<uint32_t>(U.key_lo + p.key_offset);
             for (int i0 = 0; i0 < U.ntiles; i0 += 2 * L::kSubs) {
                 float sc[2];
-                int64_t key[2];
-                bool has[2];
+                int rem[2];  // keys of tile i that belong to this row (0..128)
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
                     const int i = i0 + j * L::kSubs + sub;
-                    has[j] = i < U.ntiles;
-                    key[j] = U.key_lo + static_cast<int64_t>(i) * kTileKeys + quad * 32 +
-                             scored_lane(lane);
+                    const int64_t left = limit - (U.key_lo + static_cast<int64_t>(i) * kTileKeys);
+                    rem[j] = left <= 0 ? 0 : left >= kTileKeys ? kTileKeys : static_cast<int>(left);
                     sc[j] = 0.f;
-                    if (has[j]) {
+                    if (i < U.ntiles) {
                         const int acc = acc_base + i;
                         const int a = acc % L::kAccBufs;
                         tc::mbar_wait(&tfull[a], (acc / L::kAccBufs) & 1, abort, p.err);
@@ -409,10 +431,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         sel.compact(p.topk, held, false, (kTrigger - p.topk) / 4);
                 }
                 const uint64_t thr = *reinterpret_cast<volatile uint64_t*>(sel.thr);
-                sel.offer2_thr(has[0] && row_ok && key[0] < limit,
-                               make_key(sc[0], static_cast<uint32_t>(key[0] + p.key_offset)),
-                               has[1] && row_ok && key[1] < limit,
-                               make_key(sc[1], static_cast<uint32_t>(key[1] + p.key_offset)), thr);
+                const uint32_t i_a = static_cast<uint32_t>((i0 + sub) * kTileKeys + off);
+                const uint32_t i_b = static_cast<uint32_t>((i0 + L::kSubs + sub) * kTileKeys + off);
+                sel.offer2_scored(off < rem[0], sc[0], pos0 + i_a, off < rem[1], sc[1], pos0 + i_b,
+                                  thr, score_floor(thr));
             }
             acc_base += U.ntiles;
             if (row_ok) {
@@ -500,9 +522,38 @@ int sm_count() {
     return n;
 }
 
-template <int QK, int R>
+// Stored-score layout of the two-pass path: rows of ld floats (a multiple of 4, so that a
+// row starts on 16 bytes), at most about kScoreScratch bytes per launch pair.
+constexpr size_t kScoreScratch = size_t(8) << 30;
+
+int64_t score_ld(int S) { return (static_cast<int64_t>(S) + 3) & ~int64_t(3); }
+
+// Query rows per launch pair of the two-pass path: a multiple of R, all T when they fit.
+int score_chunk_rows(int qk_dtype, int B, int T, int S) {
+    const int R = rows_per_unit(qk_dtype, T);
+    const int64_t per_row = static_cast<int64_t>(B) * score_ld(S) * 4;
+    int64_t rows = per_row > 0 ? static_cast<int64_t>(kScoreScratch) / per_row : T;
+    rows = rows / R * R;
+    if (rows < R) rows = R;
+    return rows >= T ? T : static_cast<int>(rows);
+}
+
+size_t score_scratch_bytes(int qk_dtype, int B, int T, int S) {
+    if (rows_per_unit(qk_dtype, T) == 1) return 0;  // decode selects inside the kernel
+    return static_cast<size_t>(B) * score_chunk_rows(qk_dtype, B, T, S) * score_ld(S) * 4;
+}
+
+// Candidate lists [slots][topk] (8 bytes a key) and their counts [slots] right after them;
+// the size keeps whatever follows on a 16-byte boundary.
+size_t cand_bytes(int B, int T, int topk, int n_chunks) {
+    const size_t slots = static_cast<size_t>(B) * T * n_chunks;
+    return ((slots * topk * sizeof(uint64_t) + 15) & ~size_t(15)) +
+           ((slots * sizeof(int) + 255) & ~size_t(255));
+}
+
+template <int QK, int R, bool kStore>
 cudaError_t launch_qk(const IndexerArgs& a, void* workspace, cudaStream_t st) {
-    using L = Lay<QK, R>;
+    using L = Lay<QK, R, kStore>;
     CUtensorMap tk, tq;
     // the query box is one unit's rows (64 per query row), at most 128 per copy
     if (!encode_rows128(&tk, a.kI, static_cast<int64_t>(a.B) * a.S, QK) ||
@@ -523,27 +574,61 @@ cudaError_t launch_qk(const IndexerArgs& a, void* workspace, cudaStream_t st) {
     p.score = a.score;
     p.err = a.err;
     tc_plan(QK, a.B, a.T, a.S, &p.n_chunks, &p.chunk_keys);
-    const int64_t groups = static_cast<int64_t>(a.B) * ((a.T + R - 1) / R);
-    p.n_units = static_cast<int>(groups * p.n_chunks);
     const int rows = a.B * a.T;
-    if (p.n_chunks == 1 && a.out_cand) {  // one list per row: the candidates are the output
+    // Candidate lists: the caller's (one list per row), else the workspace's (the fused
+    // variant: one per key chunk).  The store variant ranks each row itself, or leaves it
+    // unordered in the caller's lists, so its workspace holds the stored scores only.
+    const int lists = p.n_chunks;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    if ((kStore || lists == 1) && a.out_cand) {
         p.cand = a.out_cand;
         p.cand_cnt = a.out_cnt;
-    } else {
-        p.cand = static_cast<uint64_t*>(workspace);
-        p.cand_cnt =
-            reinterpret_cast<int*>(p.cand + static_cast<size_t>(rows) * p.n_chunks * a.topk);
+    } else if (!kStore) {
+        p.cand = reinterpret_cast<uint64_t*>(ws);
+        p.cand_cnt = reinterpret_cast<int*>(p.cand + static_cast<size_t>(rows) * lists * a.topk);
+        ws += cand_bytes(a.B, a.T, a.topk, lists);
     }
     constexpr int smem = L::kSmem;
-    cudaError_t e = cudaFuncSetAttribute(tsi_indexer_tc_kernel<QK, R>,
+    cudaError_t e = cudaFuncSetAttribute(tsi_indexer_tc_kernel<QK, R, kStore>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    const int grid = p.n_units < sm_count() ? p.n_units : sm_count();
-    tsi_indexer_tc_kernel<QK, R><<<grid, kThreads, smem, st>>>(tk, tq, p);
-    note_launches(1);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    if (p.n_chunks == 1)
+    const int chunk_rows = kStore ? score_chunk_rows(QK, a.B, a.T, a.S) : a.T;
+    p.scores = kStore ? reinterpret_cast<float*>(ws) : nullptr;
+    p.ld = score_ld(a.S);
+    // Launch pairs over chunks of query rows, the last rows first (each chunk's rows are
+    // a multiple of R except the first rows of the sequences).
+    for (int t_end = a.T; t_end > 0; t_end -= chunk_rows) {
+        p.t_end = t_end;
+        p.t_begin = t_end > chunk_rows ? t_end - chunk_rows : 0;
+        const int n = p.t_end - p.t_begin;
+        p.n_units = static_cast<int>(static_cast<int64_t>(a.B) * ((n + R - 1) / R) * p.n_chunks);
+        const int grid = p.n_units < sm_count() ? p.n_units : sm_count();
+        tsi_indexer_tc_kernel<QK, R, kStore><<<grid, kThreads, smem, st>>>(tk, tq, p);
+        note_launches(1);
+        e = cudaGetLastError();
+        if (e != cudaSuccess || !kStore) break;
+        ScoreRows sr{};
+        sr.scores = p.scores;
+        sr.ld = p.ld;
+        sr.B = a.B;
+        sr.T = a.T;
+        sr.S = a.S;
+        sr.S_total = p.S_total;
+        sr.topk = a.topk;
+        sr.t0 = p.t_begin;
+        sr.rows = n;
+        sr.key_offset = a.key_offset;
+        sr.kv_len = a.kv_len;
+        sr.idx = a.out_cand ? nullptr : a.idx;
+        sr.score = a.out_cand ? nullptr : a.score;
+        sr.cand = p.cand;
+        sr.cand_cnt = p.cand_cnt;
+        sr.err = a.err;
+        e = launch_topk_rows(sr, st);
+        if (e != cudaSuccess) break;
+    }
+    if (e != cudaSuccess || kStore) return e;
+    if (lists == 1)
         return a.out_cand ? e
                           : launch_topk_rank(rows, a.topk, p.cand, p.cand_cnt, a.idx, a.score,
                                              a.err, st);
@@ -563,14 +648,17 @@ bool tc_indexer_supported(int qk_dtype, int H_I, int d_I) {
 }
 
 size_t tc_indexer_workspace_bytes(int qk_dtype, int B, int T, int S, int topk) {
+    if (rows_per_unit(qk_dtype, T) > 1)  // two passes: the stored scores
+        return score_scratch_bytes(qk_dtype, B, T, S);
     int nc, ck;
     tc_plan(qk_dtype, B, T, S, &nc, &ck);
-    const size_t slots = static_cast<size_t>(B) * T * nc;
-    return slots * topk * sizeof(uint64_t) + ((slots * sizeof(int) + 255) & ~size_t(255)) +
+    return cand_bytes(B, T, topk, nc) +
            (nc > 1 ? topk_merge_stage_bytes(B * T, topk, nc) : 0);
 }
 
 size_t tc_indexer_split_workspace_bytes(int qk_dtype, int B, int T, int S, int topk) {
+    // the caller's lists take the candidates of a one-list-per-row launch
+    if (rows_per_unit(qk_dtype, T) > 1) return score_scratch_bytes(qk_dtype, B, T, S);
     int nc, ck;
     tc_plan(qk_dtype, B, T, S, &nc, &ck);
     return nc <= 1 ? 0 : tc_indexer_workspace_bytes(qk_dtype, B, T, S, topk);
@@ -579,11 +667,11 @@ size_t tc_indexer_split_workspace_bytes(int qk_dtype, int B, int T, int S, int t
 cudaError_t launch_indexer_tc(const IndexerArgs& a, void* workspace, cudaStream_t st) {
     if (a.B * a.T == 0) return cudaSuccess;
     if (rows_per_unit(a.qk_dtype, a.T) == 1)
-        return a.qk_dtype == TSI_E4M3 ? launch_qk<TSI_E4M3, 1>(a, workspace, st)
-                                      : launch_qk<TSI_BF16, 1>(a, workspace, st);
+        return a.qk_dtype == TSI_E4M3 ? launch_qk<TSI_E4M3, 1, false>(a, workspace, st)
+                                      : launch_qk<TSI_BF16, 1, false>(a, workspace, st);
     return a.qk_dtype == TSI_E4M3
-               ? launch_qk<TSI_E4M3, TileCfg<TSI_E4M3>::kRows>(a, workspace, st)
-               : launch_qk<TSI_BF16, TileCfg<TSI_BF16>::kRows>(a, workspace, st);
+               ? launch_qk<TSI_E4M3, TileCfg<TSI_E4M3>::kRows, true>(a, workspace, st)
+               : launch_qk<TSI_BF16, TileCfg<TSI_BF16>::kRows, true>(a, workspace, st);
 }
 
 }  // namespace tsi

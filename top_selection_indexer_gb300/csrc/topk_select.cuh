@@ -34,6 +34,15 @@ __device__ __forceinline__ uint64_t make_key(float score, uint32_t s) {
            static_cast<uint64_t>(0xFFFFFFFFu - s);
 }
 
+// The smallest fp32 score whose keys can reach `threshold`: a finite score x has
+// make_key(x, s) >= threshold for some s exactly when x >= score_floor(threshold) (the
+// order is monotone in the score, -0.0 and +0.0 alike).  Thresholds whose score word lies
+// below every real score give -inf.
+__device__ __forceinline__ float score_floor(uint64_t threshold) {
+    const uint32_t o = static_cast<uint32_t>(threshold >> 32);
+    return o < 0x00800000u ? -__int_as_float(0x7f800000) : order_bits_score(o);
+}
+
 __device__ __forceinline__ int32_t key_position(uint64_t key) {
     return static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(key));
 }
@@ -133,6 +142,18 @@ struct TopKSelector {
         return *reinterpret_cast<volatile uint64_t*>(thr);
     }
 
+    // Collective: empty the buffer; from now on only keys >= threshold are admitted.
+    __device__ void restart(uint64_t threshold) {
+        sync();
+        if (tid == 0) {
+            ctl[0] = 0;
+            ctl[4] = 0;
+            *thr = threshold;
+            *rng = 0ull;
+        }
+        sync();
+    }
+
     // Collective: offer against a threshold returned by make_room.
     __device__ __forceinline__ void offer_thr(bool has, uint64_t key, uint64_t threshold) {
         const int lane = threadIdx.x & 31;
@@ -184,6 +205,21 @@ struct TopKSelector {
                     atomicOr(err, kErrAssert);
             }
         }
+    }
+
+    // Warp-collective: offer2_thr of two scored positions per thread, (s0, pos0) and
+    // (s1, pos1), each taken part only when ok0 / ok1.  Most offers fall below the
+    // threshold once the row has seen a few thousand keys, so the fp32 scores are first
+    // compared with the threshold's score (score_floor of `threshold`): a key below it is
+    // below the threshold whatever its position, and a warp with no lane at or above it
+    // builds no 64-bit key at all.
+    __device__ __forceinline__ void offer2_scored(bool ok0, float s0, uint32_t pos0, bool ok1,
+                                                  float s1, uint32_t pos1, uint64_t threshold,
+                                                  float floor) {
+        const bool c0 = ok0 && s0 >= floor;
+        const bool c1 = ok1 && s1 >= floor;
+        if (!__any_sync(kFull, c0 || c1)) return;
+        offer2_thr(c0, make_key(s0, pos0), c1, make_key(s1, pos1), threshold);
     }
 
     // Collective: drop held keys that cannot be among the k largest (no-op when n <= k).
@@ -303,29 +339,37 @@ struct TopKSelector {
         const int kept = k - need + inbin;
         // keep keys >= prefix, compacted to the front in place.  Each round reads the next
         // kRound * NT slots into registers before any thread writes; a write lands below
-        // the count kept so far, which is below every later read.  ctl[4] is 0 here: the
-        // last user set it back (or reset() did).
+        // the count kept so far, which is below every later read.  A warp reserves the
+        // slots for all its keys of the round with one atomic (offsets from a warp scan
+        // of the per-thread counts).  ctl[4] is 0 here: the last user set it back (or
+        // reset() did).
         constexpr int kRound = 8;
         const int lane = threadIdx.x & 31;
         for (int base = 0; base < n; base += kRound * NT) {
             uint64_t v[kRound];
+            unsigned keep = 0u;  // bit j: v[j] is kept
 #pragma unroll
             for (int j = 0; j < kRound; ++j) {
                 const int i = base + j * NT + tid;
                 v[j] = i < n ? buf[i] : 0ull;
+                if (i < n && v[j] >= prefix) keep |= 1u << j;
             }
+            const int c = __popc(keep);
+            int incl = c;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int t = __shfl_up_sync(kFull, incl, o);
+                if (lane >= o) incl += t;
+            }
+            int at = 0;
+            if (lane == 31 && incl) at = atomicAdd(&ctl[4], incl);
+            at = __shfl_sync(kFull, at, 31) + incl - c;
             sync();
 #pragma unroll
             for (int j = 0; j < kRound; ++j) {
-                const bool keep = base + j * NT + tid < n && v[j] >= prefix;
-                const unsigned m = __ballot_sync(kFull, keep);
-                if (m) {
-                    const int leader = __ffs(m) - 1;
-                    int at = 0;
-                    if (lane == leader) at = atomicAdd(&ctl[4], __popc(m));
-                    at = __shfl_sync(kFull, at, leader);
-                    const int pos = at + __popc(m & ((1u << lane) - 1u));
-                    if (keep && pos < CAP) buf[pos] = v[j];
+                if ((keep >> j) & 1u) {
+                    if (at < CAP) buf[at] = v[j];
+                    ++at;
                 }
             }
         }
