@@ -75,38 +75,48 @@ __device__ __forceinline__ void stream_row(Sel& sel, const float* row, int64_t n
 // iteration a thread holds kDepth pieces (the next kDepth load meanwhile), marks the keys
 // that pass in a bit mask, and its warp reserves the slots of all of them with one atomic
 // (offsets from a warp scan of the per-thread counts).  A key passes when its score lies
-// above the threshold's score, or equals it and the 64-bit key reaches the threshold.
-__device__ __forceinline__ void filter_row(Sel& sel, const float* row, int64_t n, int64_t stride4,
+// above the threshold's score; a score equal to it (rare) is decided by the 64-bit key, in
+// a branch that only warps holding such a score take.  Indices fit 32 bits: n < 2^31.
+__device__ __forceinline__ void filter_row(Sel& sel, const float* row, int n, int stride4,
                                            uint32_t pos0, uint64_t threshold) {
     const float floor = score_floor(threshold);
-    const int64_t n4 = (n + 3) / 4;
+    const int n4 = (n + 3) / 4;
     const int lane = threadIdx.x & 31;
-    auto load = [&](int64_t j) {
+    auto load = [&](int j) {
         return j < n4 ? __ldcs(reinterpret_cast<const float4*>(row + 4 * j * stride4))
                       : make_float4(0.f, 0.f, 0.f, 0.f);
     };
-    auto passes = [&](float x, uint32_t pos, bool valid) {
-        return valid && (x > floor || (x == floor && make_key(x, pos) >= threshold));
-    };
     float4 v[kDepth];
-    int64_t j = threadIdx.x;
+    int j = threadIdx.x;
 #pragma unroll
     for (int d = 0; d < kDepth; ++d) v[d] = load(j + d * kRowThreads);
-    for (int64_t base = 0; base < n4; base += kDepth * kRowThreads) {
+    for (int base = 0; base < n4; base += kDepth * kRowThreads) {
         float4 w[kDepth];
 #pragma unroll
         for (int d = 0; d < kDepth; ++d) w[d] = load(j + (kDepth + d) * kRowThreads);
-        uint32_t p[kDepth];
-        unsigned mask = 0u;  // bit 4 d + e: key e of piece d passes
+        unsigned mask = 0u, tie = 0u;  // bit 4 d + e: key e of piece d passes / ties
 #pragma unroll
         for (int d = 0; d < kDepth; ++d) {
-            const int64_t jj = j + d * kRowThreads;
-            const int64_t left = jj < n4 ? n - 4 * jj : 0;  // keys of the piece in the row
-            p[d] = pos0 + static_cast<uint32_t>(4 * jj * stride4);
-            mask |= (passes(v[d].x, p[d], left > 0) ? 1u : 0u) << (4 * d);
-            mask |= (passes(v[d].y, p[d] + 1, left > 1) ? 1u : 0u) << (4 * d + 1);
-            mask |= (passes(v[d].z, p[d] + 2, left > 2) ? 1u : 0u) << (4 * d + 2);
-            mask |= (passes(v[d].w, p[d] + 3, left > 3) ? 1u : 0u) << (4 * d + 3);
+            const int jj = j + d * kRowThreads;
+            const int keys = jj < n4 ? min(4, n - 4 * jj) : 0;  // keys of the piece in the row
+            const float x[4] = {v[d].x, v[d].y, v[d].z, v[d].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                mask |= static_cast<unsigned>(e < keys && x[e] > floor) << (4 * d + e);
+                tie |= static_cast<unsigned>(e < keys && x[e] == floor) << (4 * d + e);
+            }
+        }
+        if (__any_sync(kFull, tie != 0u)) {
+#pragma unroll
+            for (int d = 0; d < kDepth; ++d) {
+                const uint32_t p = pos0 + 4u * static_cast<uint32_t>(j + d * kRowThreads) *
+                                                static_cast<uint32_t>(stride4);
+                const float x[4] = {v[d].x, v[d].y, v[d].z, v[d].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (((tie >> (4 * d + e)) & 1u) && make_key(x[e], p + e) >= threshold)
+                        mask |= 1u << (4 * d + e);
+            }
         }
         const int c = __popc(mask);
         int incl = c;
@@ -122,11 +132,13 @@ __device__ __forceinline__ void filter_row(Sel& sel, const float* row, int64_t n
             at = __shfl_sync(kFull, at, 31) + incl - c;
 #pragma unroll
             for (int d = 0; d < kDepth; ++d) {
+                const uint32_t p = pos0 + 4u * static_cast<uint32_t>(j + d * kRowThreads) *
+                                                static_cast<uint32_t>(stride4);
                 const float x[4] = {v[d].x, v[d].y, v[d].z, v[d].w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     if ((mask >> (4 * d + e)) & 1u) {
-                        if (at < kRowCap) sel.buf[at] = make_key(x[e], p[d] + e);
+                        if (at < kRowCap) sel.buf[at] = make_key(x[e], p + e);
                         ++at;
                     }
                 }
@@ -156,7 +168,7 @@ __global__ void __launch_bounds__(kRowThreads) topk_rows_kernel(const ScoreRows 
         int64_t G = (limit + kRowCap - 1) / kRowCap;
         G = G < kSampleEvery ? kSampleEvery : G;
         const int64_t whole = limit / (4 * G);  // blocks of G pieces wholly inside the row
-        filter_row(sel, row, 4 * whole, G, pos0, 0ull);
+        filter_row(sel, row, static_cast<int>(4 * whole), static_cast<int>(G), pos0, 0ull);
         // The row holds limit / (4 whole) keys per sampled key, so m sampled keys at or
         // above the threshold promise about m limit / (4 whole) row keys: m = 1.5 k 4 whole
         // / limit leaves a margin of 1.5.  A loose compaction stops at a bin edge at or
@@ -170,7 +182,7 @@ __global__ void __launch_bounds__(kRowThreads) topk_rows_kernel(const ScoreRows 
         }
         sel.restart(start);
     }
-    filter_row(sel, row, limit, 1, pos0, start);
+    filter_row(sel, row, static_cast<int>(limit), 1, pos0, start);
     const int held = sel.settled_count();
     if (held > kRowCap || (start != 0ull && held < r.topk)) {
         // the buffer overflowed, or the sample misled: stream the row with room checks
