@@ -144,8 +144,12 @@ __device__ __forceinline__ bool wait_fast(uint64_t* bar, uint32_t parity, bool p
     return probed || tc::mbar_wait(bar, parity, abort, err);
 }
 
-__device__ __forceinline__ float2 relu2(uint32_t a, uint32_t b) {
-    return make_float2(fmaxf(__uint_as_float(a), 0.f), fmaxf(__uint_as_float(b), 0.f));
+// 2 ReLU(x) of two accumulator words as x + |x|: exact (2x for x > 0, +0 otherwise), and an
+// add on the FMA pipe instead of a max on the half-rate ALU pipe.  The gate weights are
+// halved to match, so w/2 * (x + |x|) is exactly the product w * ReLU(x).
+__device__ __forceinline__ float2 relu2_twice(uint32_t a, uint32_t b) {
+    const float x = __uint_as_float(a), y = __uint_as_float(b);
+    return make_float2(__fadd_rn(x, fabsf(x)), __fadd_rn(y, fabsf(y)));
 }
 
 // Key lane (within the warp's 32 TMEM lanes) whose score tile_score returns to this
@@ -153,7 +157,7 @@ __device__ __forceinline__ float2 relu2(uint32_t a, uint32_t b) {
 __device__ __forceinline__ int scored_lane(int lane) { return 8 * (lane & 3) + (lane >> 2); }
 
 // Scores of query row r of the unit from accumulator buffer a: sum over the 64 heads of
-// w[h] * max(0, q[h].k), in packed fp32 pairs.
+// w[h] * max(0, q[h].k), in packed fp32 pairs (w2 holds w / 2, see relu2_twice).
 //
 // The warp reads its 32 TMEM lanes (keys) as two 16-lane slices of the row's 64 columns
 // (16x256b shape).  Thread T then holds, for two keys, the head pairs 8m + 2c + {0, 1}
@@ -184,10 +188,10 @@ __device__ __forceinline__ float tile_score(uint32_t tmem, int quad, int r, int 
         float2 a0 = make_float2(0.f, 0.f), a1 = a0, b0 = a0, b1 = a0;
 #pragma unroll
         for (int m = 0; m < 8; m += 2) {
-            a0 = __ffma2_rn(w2[m], relu2(v[4 * m + 0], v[4 * m + 1]), a0);
-            b0 = __ffma2_rn(w2[m], relu2(v[4 * m + 2], v[4 * m + 3]), b0);
-            a1 = __ffma2_rn(w2[m + 1], relu2(v[4 * m + 4], v[4 * m + 5]), a1);
-            b1 = __ffma2_rn(w2[m + 1], relu2(v[4 * m + 6], v[4 * m + 7]), b1);
+            a0 = __ffma2_rn(w2[m], relu2_twice(v[4 * m + 0], v[4 * m + 1]), a0);
+            b0 = __ffma2_rn(w2[m], relu2_twice(v[4 * m + 2], v[4 * m + 3]), b0);
+            a1 = __ffma2_rn(w2[m + 1], relu2_twice(v[4 * m + 4], v[4 * m + 5]), a1);
+            b1 = __ffma2_rn(w2[m + 1], relu2_twice(v[4 * m + 6], v[4 * m + 7]), b1);
         }
         float sa = (a0.x + a0.y) + (a1.x + a1.y);  // key lane 16 slice + T / 4
         float sb = (b0.x + b0.y) + (b1.x + b1.y);  // key lane 16 slice + 8 + T / 4
@@ -372,11 +376,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int64_t pr = query_position(p.kv_len, U.b, p.T, p.S_total, t) - p.key_offset;
                 limit = pr + 1 < U.key_hi ? pr + 1 : U.key_hi;
                 const int64_t wrow = (static_cast<int64_t>(U.b) * p.T + t) * 64;
-                // this thread's 16 gate weights (see tile_score)
+                // this thread's 16 gate weights, halved (see tile_score, relu2_twice)
 #pragma unroll
                 for (int m = 0; m < 8; ++m) {
                     const int64_t h = wrow + 8 * m + 2 * (lane & 3);
-                    w2[m] = make_float2(load_elem(p.w, h, p.w_dtype), load_elem(p.w, h + 1, p.w_dtype));
+                    w2[m] = make_float2(0.5f * load_elem(p.w, h, p.w_dtype),
+                                        0.5f * load_elem(p.w, h + 1, p.w_dtype));
                 }
             }
             // key of this thread's score in a tile: off; whole-cache position of key 0
