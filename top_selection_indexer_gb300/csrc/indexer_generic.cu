@@ -159,7 +159,7 @@ __global__ void __launch_bounds__(kRankThreads) topk_rank_kernel(int topk, const
                                                                   const int* cand_cnt,
                                                                   int32_t* idx, float* score,
                                                                   unsigned* err) {
-    __shared__ __align__(16) uint64_t xs[kRankN];
+    __shared__ __align__(16) uint64_t xs[2 * kRankN];  // keys, then ranking scratch
     const int row = blockIdx.x;
     const int t = threadIdx.x;
     int n = cand_cnt[row];
@@ -170,7 +170,7 @@ __global__ void __launch_bounds__(kRankThreads) topk_rank_kernel(int topk, const
     const uint64_t* c = cand + static_cast<int64_t>(row) * topk;
     for (int i = t; i < kRankN; i += kRankThreads) xs[i] = i < n ? c[i] : 0ull;
     __syncthreads();
-    rank_sort_write(xs, n, topk, idx + static_cast<int64_t>(row) * topk,
+    rank_merge_write(xs, xs + kRankN, n, topk, idx + static_cast<int64_t>(row) * topk,
                     score ? score + static_cast<int64_t>(row) * topk : nullptr, t, 1);
 }
 
@@ -186,7 +186,7 @@ constexpr size_t kMaxStageBytes = 160 * 1024;  // candidates a merge block stage
 // over the lists in global memory: the bits above the highest bit in which the smallest
 // and the largest candidate differ are skipped, then 8-bit digits narrow down the bin of
 // the k-th key until exactly k keys are at or above the prefix (keys are distinct).  The
-// k survivors are gathered into shared memory and ranked by rank_sort_write.
+// k survivors are gathered into shared memory and ranked by rank_merge_write.
 template <int kMergeThreads>
 __global__ void __launch_bounds__(kMergeThreads) topk_split_merge_kernel(
     int topk, int n_splits, int lists_per_group, const uint64_t* cand, int64_t row_stride,
@@ -196,7 +196,7 @@ __global__ void __launch_bounds__(kMergeThreads) topk_split_merge_kernel(
     // every pass reads them there (empty slots hold 0, which no rank key equals: its low
     // word is 0xFFFFFFFF - position)
     extern __shared__ uint64_t stg[];
-    __shared__ __align__(16) uint64_t xs[kRankN];
+    __shared__ __align__(16) uint64_t xs[2 * kRankN];  // keys, then ranking scratch
     __shared__ unsigned hist[256];
     __shared__ unsigned long long range[2];
     __shared__ int ctl[4];  // 0 digit, 1 above, 2 in-bin, 3 write cursor
@@ -379,8 +379,8 @@ __global__ void __launch_bounds__(kMergeThreads) topk_split_merge_kernel(
         return;
     }
     if (tid < kRankThreads)
-        rank_sort_write(xs, n, topk, idx + static_cast<int64_t>(v) * topk,
-                        score ? score + static_cast<int64_t>(v) * topk : nullptr, tid, 1);
+        rank_merge_write(xs, xs + kRankN, n, topk, idx + static_cast<int64_t>(v) * topk,
+                         score ? score + static_cast<int64_t>(v) * topk : nullptr, tid, 1);
 }
 
 }  // namespace

@@ -30,7 +30,8 @@ constexpr int kSampleEvery = 32;   // at least one float4 of every 32 in the sam
 constexpr int kDepth = 4;          // float4 loads of the filter pass in flight per thread
 
 static_assert(kRowCap - 2 * kRound > TSI_MAX_TOPK, "the room trigger lies above k keys");
-static_assert(kRowThreads == kRankThreads && kRowCap >= kRankN, "the block ranks its buffer");
+static_assert(kRowThreads == kRankThreads && kRowCap >= 2 * kRankN,
+              "the block ranks in its buffer, the second half as scratch");
 
 using Sel = TopKSelector<kRowThreads, kRowCap>;
 
@@ -194,14 +195,14 @@ __global__ void __launch_bounds__(kRowThreads) topk_rows_kernel(const ScoreRows 
         sel.dump(r.topk, r.cand + slot * r.topk, r.cand_cnt + slot);
         return;
     }
-    // the exact top k, then the register network of rank_sort.cuh over the first kRankN
-    // slots (empty slots hold key 0, below every real key)
+    // the exact top k, then ranked by rank_merge_write (rank_sort.cuh) over the first kRankN
+    // slots (empty slots hold key 0, below every real key), the next kRankN as scratch
     sel.compact(r.topk, sel.settled_count());
     const int n = sel.settled_count();
     for (int i = n + threadIdx.x; i < kRankN; i += kRowThreads) sel.buf[i] = 0ull;
     sel.sync();
-    rank_sort_write(sel.buf, n, r.topk, r.idx + slot * r.topk,
-                    r.score ? r.score + slot * r.topk : nullptr, threadIdx.x, 1);
+    rank_merge_write(sel.buf, sel.buf + kRankN, n, r.topk, r.idx + slot * r.topk,
+                     r.score ? r.score + slot * r.topk : nullptr, threadIdx.x, 1);
 }
 
 }  // namespace
