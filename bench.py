@@ -550,7 +550,9 @@ def run_e2e(args, cfg, ind, lay, idx, outs, ws, stream, world, n_copy_streams=4)
     Copies overlap the kernels, as a pipelined caller would run them: the upload streams
     move each layer's Q and latent (and each group's indexer inputs) into that layer's
     own device buffers ahead of the compute stream; the read-back streams copy each
-    layer's output (and each group's index rows) to the host behind it.  Events order
+    layer's output (and each group's index rows) to the host behind it -- with
+    --readback result (the default) only the step's result, the stack's last output, as
+    a caller that keeps the intermediate layers on the device would.  Events order
     every reuse of a buffer: an upload waits until the previous step's kernels are done
     with its destination, a kernel waits for its inputs and for the read-back of the
     output buffer it overwrites, and the timer stops after the last read-back.
@@ -638,8 +640,9 @@ def run_e2e(args, cfg, ind, lay, idx, outs, ws, stream, world, n_copy_streams=4)
             e = ev()
             e.record(stream)
             idx_done[g] = e
-            idx_read[g % 2] = split_copy(h_idx, ib, downs, [e])
-            d2h += ib.numel() * ib.element_size()
+            if args.readback == "all" or (nl == 0 and g == G - 1):  # no layers: the rows
+                idx_read[g % 2] = split_copy(h_idx, ib, downs, [e])
+                d2h += ib.numel() * ib.element_size()
             for l0 in range(min(cfg.group, nl - g * cfg.group)):
                 layer = g * cfg.group + l0
                 Q, K, V = lay[layer]
@@ -652,8 +655,9 @@ def run_e2e(args, cfg, ind, lay, idx, outs, ws, stream, world, n_copy_streams=4)
                 e = ev()
                 e.record(stream)
                 attn_done[layer] = e
-                out_read[l0] = split_copy(h_O, outs[l0], downs, [e])
-                d2h += h_O.numel() * 2
+                if args.readback == "all" or layer == nl - 1:
+                    out_read[l0] = split_copy(h_O, outs[l0], downs, [e])
+                    d2h += h_O.numel() * 2
 
     step()  # warm the copy path
     torch.cuda.synchronize()
@@ -675,7 +679,10 @@ def run_e2e(args, cfg, ind, lay, idx, outs, ws, stream, world, n_copy_streams=4)
             "ms_per_step": round(ms, 2), "steps": steps,
             "note": f"every layer uploads Q and the latent from one pinned host buffer; "
                     f"copies run on {n_copy_streams} streams per direction, overlapping the "
-                    f"kernels"}
+                    f"kernels; read back: "
+                    + ("every layer's output and the index rows" if args.readback == "all"
+                       else "the step's result (the last layer's output; the index rows "
+                            "when there are no layers)")}
 
 
 # ----------------------------------------------------------------------------- CPU oracle
@@ -772,6 +779,9 @@ def main():
                     help="skip the context-parallel indexer measurement after the timed steps")
     ap.add_argument("--copy-streams", type=int, default=4,
                     help="streams per direction for the end-to-end host copies")
+    ap.add_argument("--readback", choices=("result", "all"), default="result",
+                    help="end-to-end read-back: the step's result (the last layer's output) "
+                         "or every layer's output and the index rows")
     ap.add_argument("--no-kl", action="store_true",
                     help="skip the group-centroid KL measurement")
     ap.add_argument("--no-overlap", action="store_true",
