@@ -81,6 +81,36 @@ def test_decode_needs_workspace(lib):
     assert st == tsi.ERR_WORKSPACE
 
 
+def _scores_bytes(B, T, S, R, budget=8 << 30):
+    """Stored scores of the two-pass tensor-core indexer: one chunk of query rows, rows of
+    S floats rounded up to 4, the chunk as many rows (a multiple of R) as fit the budget."""
+    ld = (S + 3) // 4 * 4
+    rows = budget // (B * ld * 4) // R * R
+    rows = min(T, max(R, rows))
+    return B * rows * ld * 4
+
+
+@pytest.mark.parametrize("B,T,S,qk,R", [
+    (1, 300, 1000, tsi.E4M3, 4),        # all rows in one chunk
+    (3, 5, 10, tsi.E4M3, 4),            # rows padded to 12 floats
+    (1, 131072, 131072, tsi.E4M3, 4),   # 16384-row chunks: 8 GiB
+    (1, 131072, 131071, tsi.BF16, 2),   # padded row, bf16 units of two rows
+    (64, 4096, 131072, tsi.E4M3, 4),    # 256-row chunks across 64 sequences
+])
+def test_two_pass_workspace_holds_one_chunk_of_scores(lib, B, T, S, qk, R):
+    need = lib.tsi_indexer_topk_workspace(B, T, S, 64, 128, 2048, qk)
+    assert need == _scores_bytes(B, T, S, R)
+    # key shards: the same scores, no candidate lists (the caller's take them)
+    assert lib.tsi_indexer_topk_shard_workspace(B, T, S, 64, 128, 2048, qk) == need
+
+
+def test_decode_workspace_holds_candidate_lists(lib):
+    # one query per sequence: key-range candidate lists (8 B a key) and counts, no scores
+    need = lib.tsi_indexer_topk_workspace(8, 1, 131072, 64, 128, 2048, tsi.E4M3)
+    assert need >= 8 * 2048 * 8 * 2  # at least two key ranges per row
+    assert need < 8 * 131072 * 4     # far below one row of stored scores per sequence
+
+
 def _attn(lib, n=1, **kw):
     P = ctypes.c_void_p * n
     a = dict(q=P(*[FAKE] * n), k=P(*[FAKE] * n), v=None, B=1, T=4, S=4, H=64, Hkv=1,
