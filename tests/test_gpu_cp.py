@@ -39,6 +39,8 @@ CASES = [
     (1, 3000, 3000, 64, 128, "bf16", (1500,), None),
     (2, 300, 1000, 64, 128, "e4m3", (333, 700), [1000, 900]),
     (4, 1, 40000, 64, 128, "e4m3", (12345, 30000), [40000, 20000, 7, 31000]),
+    # shards of up to 15000 keys per query row: the two-pass row selection samples them
+    (2, 64, 40000, 64, 128, "e4m3", (15000, 26000), [40000, 23456]),
     (1, 700, 700, 4, 32, "f32", (100, 101, 650), None),
     (3, 1, 30000, 4, 32, "f32", (9000,), [30000, 8999, 9001]),
 ]

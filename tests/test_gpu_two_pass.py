@@ -7,6 +7,7 @@ on inputs that drive its row selection off the common path, against the oracle:
 - those keys alone score high: the sampled threshold admits fewer than k keys, so the row
   is streamed again from threshold 0;
 - every score equal: the tie rule (lower position first) over rows of 40000 keys;
+- sequences of different cached lengths, their rows long enough to be sampled;
 - a full-size L = 131072 prefill with integer-valued inputs, checked on the rows at the
   borders of the launch chunks (multiples of 4096 rows from the end) and their neighbours.
 
@@ -80,6 +81,22 @@ def test_sampled_keys_alone_score_high(cuda_lib, qk):
         assert n_high < topk
         row = idx[0, t]
         assert torch.all((row[:n_high] % 128) < 4) and torch.all((row[n_high:] % 128) >= 4)
+
+
+@pytest.mark.parametrize("qk", ["e4m3", "bf16"])
+def test_ragged_sequences_sampled_rows(cuda_lib, qk):
+    # per-sequence cache lengths: sampled rows of 12k to 30k keys end where each sequence
+    # ends, and a third sequence is shorter than the row buffer
+    B, T, S, topk = 3, 64, 30000, 2048
+    qI = draw((B, T, H, D), "int8", qk, 31, "cuda", D)
+    kI = draw((B, S, D), "int8", qk, 32, "cuda", D)
+    w = draw((B, T, H), "pow2", "bf16", 33, "cuda", D)
+    kv = torch.tensor([30000, 12345, 4000], dtype=torch.int32, device="cuda")
+    idx, sc = cuda_lib.indexer_topk(qI, kI, w, topk, kv_len=kv, want_score=True)
+    cuda_lib.device_status()
+    rows = sorted({0, T - 1, T, 2 * T - 1, 2 * T, 3 * T - 1} | set(range(5, B * T, 23)))
+    check_indexer(qI.cpu(), kI.cpu(), w.cpu(), topk, idx.cpu(), sc.cpu(), kv_len=kv.cpu(),
+                  rows=np.array(rows), exact=True)
 
 
 def test_full_size_chunk_borders_integer_exact(cuda_lib):
