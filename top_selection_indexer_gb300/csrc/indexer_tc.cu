@@ -1,31 +1,34 @@
-// Tensor-core lightning indexer + streaming top-k for sm_103a (tcgen05 / TMEM / TMA).
+// Tensor-core lightning indexer for sm_103a (tcgen05 / TMEM / TMA).
 //
 // I[t,s] = sum_j w[t,j] * ReLU(qI[t,j] . kI[s]) for s <= p_t, then the top-k keys of
 // each row ("GLM-5.2 技术报告速览", §IndexShare: the score equation, k = 2048; the
-// ReLU form is chosen there for speed and FP8 friendliness).  The L x L score matrix
-// never leaves the chip: each 128-key tile is scored in TMEM and streamed into a
-// shared-memory top-k selector per query row.
+// ReLU form is chosen there for speed and FP8 friendliness).  Two variants of one kernel:
+//   - store (launches of several query rows per sequence): every causal score goes to a
+//     row-major fp32 buffer, a chunk of query rows at a time; topk_rows.cu then selects
+//     and ranks each row's k best keys from it.  The selection thus never stalls the
+//     MMA pipeline, at 4 B of HBM writes per causal pair.
+//   - select (one query row per sequence, decode): each 128-key tile is scored in TMEM
+//     and streamed into a shared-memory top-k selector; the row's keys are split into
+//     chunks whose lists the CUDA-core merge kernel merges and ranks.
 //
 // MMA shape: keys on M (128 rows of kI per tile, the A operand), the 64 heads of R
 // consecutive query rows on N = 64 R (the B operand), d_I = 128 on K, fp32 accumulators
-// in TMEM.  R = 4 for e4m3 (N = 256) and 2 for bf16 (N = 128, where shared memory holds
-// fewer selectors).  A thread of the epilogue owns one key (one TMEM lane) and reduces
-// the 64 heads of its query row inside its registers: ReLU, times the gate weight,
-// summed -- no cross-thread reduction.  The larger R, the more query rows share each
-// key tile: fewer tiles, fewer MMA issues and barrier round trips, less L2 traffic.
+// in TMEM.  R = 4 for e4m3 (N = 256), 2 for bf16 (N = 128), 1 for decode.  The larger R,
+// the more query rows share each key tile: fewer tiles, MMA issues and barrier round
+// trips, less L2 traffic.  An epilogue warp reads its 32 TMEM lanes (keys) in the
+// 16x256b shape (see tile_score): each thread sums 16 heads of two keys, four threads
+// combine their sums with two shuffles.
 //
 // Roles of one persistent CTA (576 threads):
 //   warp 0       TMA producer: Q tile of the unit, key tiles into a ring of stages
 //   warp 1       TMEM allocator + single-thread MMA issuer (512 TMEM columns: 512 / N
 //                accumulators, so the MMA runs that many tiles ahead)
 //   warps 2..17  R epilogue groups of 16 / R warps, one per query row of the unit; group
-//                r reads columns [64r, 64r+64) of an accumulator and owns a selector.
-//                With R = 2 the group's first 4 warps take the even tiles, the other 4
-//                the odd tiles.
+//                r reads columns [64r, 64r+64) of an accumulator (and, selecting, owns a
+//                selector).  With 16 / R > 4 warps per row, the row's warp sets share out
+//                the tiles.
 // Units (R consecutive query rows x one key range) are visited longest first and spread
-// round-robin over the CTAs.  Decode-sized requests split each row's keys into chunks.
-// Each row (chunk) leaves its k best keys unordered in the workspace; the CUDA-core merge
-// kernel ranks them (and merges a row's chunks), so no sort stalls the MMA pipeline.
+// round-robin over the CTAs.
 #include <mutex>
 
 #include <cudaTypedefs.h>
@@ -51,7 +54,6 @@ struct TileCfg<TSI_E4M3> {
     static constexpr int kRows = 4;    // query rows per unit
     static constexpr int kChunks = 1;  // 128-byte pieces of a d_I = 128 row
     static constexpr int kStages = 4;
-    static constexpr int kCap = 3584;  // selector capacity per row
     static constexpr uint32_t kFmt = 0;
     static constexpr int kKSteps = 4;  // K = 32 per MMA
 };
@@ -60,20 +62,22 @@ struct TileCfg<TSI_BF16> {
     static constexpr int kRows = 2;
     static constexpr int kChunks = 2;
     static constexpr int kStages = 3;
-    static constexpr int kCap = 4096;
     static constexpr uint32_t kFmt = 1;
     static constexpr int kKSteps = 4;  // per chunk, K = 16 per MMA
 };
 
 // R = query rows per unit: the format's default, or 1 for one query per sequence (decode),
 // where the four warp sets of the single row share out the key tiles instead of idling.
+// kStore: the epilogue stores the scores (multi-row launches); otherwise it selects the
+// row's top k itself (one query row per unit).
 template <int QK, int R = TileCfg<QK>::kRows, bool kStore = false>
 struct Lay {
     using C = TileCfg<QK>;
     static constexpr int kR = R;
+    static_assert(kStore || R == 1, "the in-kernel selection takes one query row per unit");
     // selector capacity: the row's warp sets offer up to 4 kGroupThreads keys between two
     // room checks (see the trigger in the epilogue), beyond the k that are kept
-    static constexpr int kCap = R == 1 ? 5120 : C::kCap;
+    static constexpr int kCap = 5120;
     static constexpr int kN = 64 * kR;             // MMA N
     static constexpr int kAccBufs = kTmemCols / kN;
     static constexpr int kSubs = 4 / kR;           // warp sets per row sharing out the tiles
