@@ -148,9 +148,32 @@ __global__ void __launch_bounds__(kCombineThreads) attn_combine_kernel(
     if (a.lse && tid == 0) a.lse[static_cast<int64_t>(row) * a.H + h] = lse_of(M, Lt);
     __nv_bfloat16* o = static_cast<__nv_bfloat16*>(a.out) + (static_cast<int64_t>(row) * a.H + h) * a.Dv;
     if ((a.Dv & 3) == 0) {
+        // eight splits' partials load at once, then accumulate in split order.  Every
+        // split has its slot in the workspace, so the loads stay in bounds; a split
+        // without keys has weight 0 and its slot (possibly never written) is not used.
+        constexpr int kBatch = 8;
         for (int d = 4 * tid; d < a.Dv; d += 4 * kCombineThreads) {
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int sp = 0; sp < n_splits; ++sp) {
+            int sp = 0;
+            for (; sp + kBatch <= n_splits; sp += kBatch) {
+                float w[kBatch];
+                float4 v[kBatch];
+#pragma unroll
+                for (int u = 0; u < kBatch; ++u) {
+                    w[u] = wsp[sp + u];
+                    v[u] = *reinterpret_cast<const float4*>(
+                        part_o + (slot0 + static_cast<int64_t>(sp + u) * a.H) * a.Dv + d);
+                }
+#pragma unroll
+                for (int u = 0; u < kBatch; ++u) {
+                    if (w[u] == 0.f) continue;
+                    acc.x = fmaf(w[u], v[u].x, acc.x);
+                    acc.y = fmaf(w[u], v[u].y, acc.y);
+                    acc.z = fmaf(w[u], v[u].z, acc.z);
+                    acc.w = fmaf(w[u], v[u].w, acc.w);
+                }
+            }
+            for (; sp < n_splits; ++sp) {
                 const float w = wsp[sp];
                 if (w == 0.f) continue;
                 const float4 v = *reinterpret_cast<const float4*>(
