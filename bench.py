@@ -319,6 +319,9 @@ def run_gpu(args, rank, world):
         result["overlap"] = measure_overlap(cfg, ind, idx, ws, stream)
     if not args.no_cp:
         result["context_parallel"] = measure_cp(cfg, ind, idx, stream)
+    if cfg.T > 1 and tsi.indexer_path(qk_code, cfg.H_I, cfg.d_I) == 1:
+        result["indexer_onchip"] = measure_onchip(cfg, ind, idx, stream, idx_flops, tc_peak,
+                                                  ms_idx, qk_code)
     if not args.no_kl and cfg.n_layers >= 1 and \
             tsi.attn_path(cfg.H, cfg.Hkv, cfg.Dqk, cfg.Dv, cfg.v_from_k) == 1:
         result["index_kl"] = measure_index_kl(cfg, ind, lay, idx, outs, ws, stream)
@@ -362,6 +365,40 @@ def _balanced_edges(cfg, shards, align=128):
         edges.append(min(cfg.S, max(edges[-1], (lo + align // 2) // align * align)))
     edges.append(cfg.S)
     return edges
+
+
+def measure_onchip(cfg, ind, idx, stream, flops, peak, ms_default, qk_code, reps=2):
+    """Group 0's indexer + top-k with every score kept on chip (tsi_indexer_topk_onchip: the
+    selection runs in the scoring kernel's epilogue), beside the default two-pass call: time
+    per call, the fraction of the tensor peak, and whether the rows equal the default's."""
+    import torch
+
+    import top_selection_indexer_gb300 as tsi
+
+    qI, kI, w = ind[0]
+    out = torch.empty_like(idx)
+    ws = torch.empty(max(1, tsi.indexer_topk_workspace(cfg.B, cfg.T, cfg.S, cfg.H_I, cfg.d_I,
+                                                       cfg.topk, qk_code, onchip=True)),
+                     dtype=torch.uint8, device=idx.device)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(reps)]
+    for r in range(reps + 1):  # the first call warms up
+        if r:
+            ev[r - 1][0].record(stream)
+        tsi.indexer_topk(qI, kI, w, cfg.topk, idx=out, workspace=ws, stream=stream, onchip=True)
+        if r:
+            ev[r - 1][1].record(stream)
+    tsi.device_status(stream)
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    tsi.indexer_topk(qI, kI, w, cfg.topk, idx=idx, stream=stream)
+    same = bool(torch.equal(out, idx))
+    tf = flops / (ms / 1e3) / 1e12
+    return {"ms_per_call": round(ms, 3), "achieved_tflops": round(tf, 1),
+            "frac": round(tf / peak, 4), "ms_default_two_pass": round(ms_default, 3),
+            "equals_default": same,
+            "workspace_bytes": int(ws.numel()),
+            "note": "scores kept in the scoring kernel (selection in its epilogue); the default "
+                    "call stores them for a second pass"}
 
 
 def measure_cp(cfg, ind, idx, stream, shards=2, reps=3):

@@ -93,6 +93,26 @@ tsi_status tsi_indexer_topk(const void* qI, const void* kI, const void* w, int q
                             size_t workspace_bytes, void* stream);
 
 /*
+ * The same results as tsi_indexer_topk, with every score kept on chip: on the tensor-core
+ * path with several query rows per sequence, each 128-key tile is scored in tensor memory
+ * and streamed into a shared-memory top-k selector per query row inside the scoring
+ * kernel, so no score is written to HBM ("GLM-5.2 技术报告速览", §IndexShare; the Ascend
+ * operator the pages describe also fuses score, ReLU and top-k).  tsi_indexer_topk instead
+ * stores the scores of a chunk of rows and selects in a second kernel, which is faster on
+ * a GB300 at the cost of ~8 GiB of workspace; this form needs only candidate lists
+ * (8 B x topk per row, plus a count per row).  Shapes the tensor-core path does not take,
+ * and one query row per sequence, run exactly as in tsi_indexer_topk.  Arguments, layouts
+ * and rules as tsi_indexer_topk, with workspace_bytes >=
+ * tsi_indexer_topk_onchip_workspace(...).
+ */
+size_t tsi_indexer_topk_onchip_workspace(int B, int T, int S, int H_I, int d_I, int topk,
+                                         int qk_dtype);
+tsi_status tsi_indexer_topk_onchip(const void* qI, const void* kI, const void* w, int qk_dtype,
+                                   int w_dtype, int B, int T, int S, int H_I, int d_I, int topk,
+                                   const int32_t* kv_len, int32_t* idx, float* score,
+                                   void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * tsi_indexer_topk without a workspace argument and without allocating anything.
  * The paper has no counterpart: this is a convenience of this library.
  *

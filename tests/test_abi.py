@@ -104,6 +104,16 @@ def test_two_pass_workspace_holds_one_chunk_of_scores(lib, B, T, S, qk, R):
     assert lib.tsi_indexer_topk_shard_workspace(B, T, S, 64, 128, 2048, qk) == need
 
 
+@pytest.mark.parametrize("B,T,S,qk", [(1, 131072, 131072, tsi.E4M3), (2, 3000, 3000, tsi.BF16)])
+def test_onchip_workspace_holds_candidate_lists_only(lib, B, T, S, qk):
+    # the on-chip form stores no score: one list of k 8-byte keys per row (these shapes
+    # have enough rows to keep each row's keys in one range) and a count per row
+    need = lib.tsi_indexer_topk_onchip_workspace(B, T, S, 64, 128, 2048, qk)
+    slots = B * T
+    assert need == (slots * 2048 * 8 + 15) // 16 * 16 + (slots * 4 + 255) // 256 * 256
+    assert need < lib.tsi_indexer_topk_workspace(B, T, S, 64, 128, 2048, qk) or T * S < 1 << 24
+
+
 def test_decode_workspace_holds_candidate_lists(lib):
     # one query per sequence: key-range candidate lists (8 B a key) and counts, no scores
     need = lib.tsi_indexer_topk_workspace(8, 1, 131072, 64, 128, 2048, tsi.E4M3)

@@ -21,7 +21,8 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT, ERR_
 F32, BF16, E4M3 = 0, 1, 2
 MAX_TOPK = 2048
 
-EXPORTS = ("tsi_indexer_topk_workspace", "tsi_indexer_topk", "tsi_sparse_attn_workspace",
+EXPORTS = ("tsi_indexer_topk_workspace", "tsi_indexer_topk", "tsi_indexer_topk_onchip_workspace",
+           "tsi_indexer_topk_onchip", "tsi_sparse_attn_workspace",
            "tsi_sparse_attn_group", "tsi_device_status", "tsi_last_error", "tsi_version",
            "tsi_launch_count", "tsi_indexer_topk_noalloc", "tsi_indexer_topk_noalloc_limit",
            "tsi_indexer_topk_path", "tsi_sparse_attn_path", "tsi_index_share_layers",
@@ -51,6 +52,10 @@ def load():
             lib.tsi_indexer_topk.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32,
                                              vp, vp, vp, vp, sz, vp]
             lib.tsi_indexer_topk.restype = i32
+            lib.tsi_indexer_topk_onchip_workspace.argtypes = [i32] * 7
+            lib.tsi_indexer_topk_onchip_workspace.restype = sz
+            lib.tsi_indexer_topk_onchip.argtypes = lib.tsi_indexer_topk.argtypes
+            lib.tsi_indexer_topk_onchip.restype = i32
             lib.tsi_sparse_attn_workspace.argtypes = [i32] * 8
             lib.tsi_sparse_attn_workspace.restype = sz
             lib.tsi_sparse_attn_group.argtypes = [i32, vp, vp, vp, i32, i32, i32, i32, i32, i32,
@@ -149,13 +154,16 @@ def _stream_handle(stream):
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
-def indexer_topk_workspace(B, T, S, H_I, d_I, topk, qk_dtype) -> int:
-    return load().tsi_indexer_topk_workspace(B, T, S, H_I, d_I, topk, qk_dtype)
+def indexer_topk_workspace(B, T, S, H_I, d_I, topk, qk_dtype, onchip=False) -> int:
+    lib = load()
+    fn = lib.tsi_indexer_topk_onchip_workspace if onchip else lib.tsi_indexer_topk_workspace
+    return fn(B, T, S, H_I, d_I, topk, qk_dtype)
 
 
 def indexer_topk(qI, kI, w, topk, kv_len=None, idx=None, score=None, workspace=None,
-                 stream=None, want_score=False):
-    """Top-k key positions of the lightning-indexer score (``tsi_indexer_topk``).
+                 stream=None, want_score=False, onchip=False):
+    """Top-k key positions of the lightning-indexer score (``tsi_indexer_topk``, or
+    ``tsi_indexer_topk_onchip`` with ``onchip``: the same results, no score stored).
 
     qI [B,T,H_I,d_I], kI [B,S,d_I] (f32/bf16/e4m3), w [B,T,H_I] (f32/bf16),
     kv_len [B] int32 or None.  Returns idx [B,T,topk] int32 (and score float32
@@ -172,11 +180,12 @@ def indexer_topk(qI, kI, w, topk, kv_len=None, idx=None, score=None, workspace=N
     code = _dtype_code(qI)
     if _dtype_code(kI) != code:
         raise TypeError("qI and kI must share a dtype")
-    need = indexer_topk_workspace(B, T, S, H_I, d_I, topk, code)
+    need = indexer_topk_workspace(B, T, S, H_I, d_I, topk, code, onchip)
     if workspace is None and need:
         workspace = torch.empty(need, dtype=torch.uint8, device=qI.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _check(load().tsi_indexer_topk(
+    lib = load()
+    _check((lib.tsi_indexer_topk_onchip if onchip else lib.tsi_indexer_topk)(
         _dev(qI, "qI"), _dev(kI, "kI"), _dev(w, "w"), code, _dtype_code(w), B, T, S, H_I, d_I,
         topk, _dev(kv_len, "kv_len"), _dev(idx, "idx"), _dev(score, "score"),
         _dev(workspace, "workspace"), ws_bytes, _stream_handle(stream)))

@@ -3,13 +3,14 @@
 // I[t,s] = sum_j w[t,j] * ReLU(qI[t,j] . kI[s]) for s <= p_t, then the top-k keys of
 // each row ("GLM-5.2 技术报告速览", §IndexShare: the score equation, k = 2048; the
 // ReLU form is chosen there for speed and FP8 friendliness).  Two variants of one kernel:
-//   - store (launches of several query rows per sequence): every causal score goes to a
-//     row-major fp32 buffer, a chunk of query rows at a time; topk_rows.cu then selects
-//     and ranks each row's k best keys from it.  The selection thus never stalls the
-//     MMA pipeline, at 4 B of HBM writes per causal pair.
-//   - select (one query row per sequence, decode): each 128-key tile is scored in TMEM
-//     and streamed into a shared-memory top-k selector; the row's keys are split into
-//     chunks whose lists the CUDA-core merge kernel merges and ranks.
+//   - store (the default for several query rows per sequence): every causal score goes
+//     to a row-major fp32 buffer, a chunk of query rows at a time; topk_rows.cu then
+//     selects and ranks each row's k best keys from it.  The selection thus never stalls
+//     the MMA pipeline, at 4 B of HBM writes per causal pair.
+//   - select (one query row per sequence, and any launch asked to keep its scores on
+//     chip): each 128-key tile is scored in TMEM and streamed into a shared-memory top-k
+//     selector per query row, so no score reaches HBM; each row (or key chunk) leaves its
+//     k best keys unordered, for the ranking or merge kernels.
 //
 // MMA shape: keys on M (128 rows of kI per tile, the A operand), the 64 heads of R
 // consecutive query rows on N = 64 R (the B operand), d_I = 128 on K, fp32 accumulators
@@ -52,6 +53,7 @@ struct TileCfg;
 template <>
 struct TileCfg<TSI_E4M3> {
     static constexpr int kRows = 4;    // query rows per unit
+    static constexpr int kCap = 3584;  // selector capacity per row (on-chip selection)
     static constexpr int kChunks = 1;  // 128-byte pieces of a d_I = 128 row
     static constexpr int kStages = 4;
     static constexpr uint32_t kFmt = 0;
@@ -60,6 +62,7 @@ struct TileCfg<TSI_E4M3> {
 template <>
 struct TileCfg<TSI_BF16> {
     static constexpr int kRows = 2;
+    static constexpr int kCap = 4096;
     static constexpr int kChunks = 2;
     static constexpr int kStages = 3;
     static constexpr uint32_t kFmt = 1;
@@ -68,16 +71,14 @@ struct TileCfg<TSI_BF16> {
 
 // R = query rows per unit: the format's default, or 1 for one query per sequence (decode),
 // where the four warp sets of the single row share out the key tiles instead of idling.
-// kStore: the epilogue stores the scores (multi-row launches); otherwise it selects the
-// row's top k itself (one query row per unit).
+// kStore: the epilogue stores the scores; otherwise it selects each row's top k itself.
 template <int QK, int R = TileCfg<QK>::kRows, bool kStore = false>
 struct Lay {
     using C = TileCfg<QK>;
     static constexpr int kR = R;
-    static_assert(kStore || R == 1, "the in-kernel selection takes one query row per unit");
     // selector capacity: the row's warp sets offer up to 4 kGroupThreads keys between two
     // room checks (see the trigger in the epilogue), beyond the k that are kept
-    static constexpr int kCap = 5120;
+    static constexpr int kCap = R == 1 ? 5120 : C::kCap;
     static constexpr int kN = 64 * kR;             // MMA N
     static constexpr int kAccBufs = kTmemCols / kN;
     static constexpr int kSubs = 4 / kR;           // warp sets per row sharing out the tiles
@@ -656,8 +657,8 @@ bool tc_indexer_supported(int qk_dtype, int H_I, int d_I) {
     return (qk_dtype == TSI_BF16 || qk_dtype == TSI_E4M3) && H_I == 64 && d_I == 128;
 }
 
-size_t tc_indexer_workspace_bytes(int qk_dtype, int B, int T, int S, int topk) {
-    if (rows_per_unit(qk_dtype, T) > 1)  // two passes: the stored scores
+size_t tc_indexer_workspace_bytes(int qk_dtype, int B, int T, int S, int topk, bool onchip) {
+    if (rows_per_unit(qk_dtype, T) > 1 && !onchip)  // two passes: the stored scores
         return score_scratch_bytes(qk_dtype, B, T, S);
     int nc, ck;
     tc_plan(qk_dtype, B, T, S, &nc, &ck);
@@ -670,7 +671,7 @@ size_t tc_indexer_split_workspace_bytes(int qk_dtype, int B, int T, int S, int t
     if (rows_per_unit(qk_dtype, T) > 1) return score_scratch_bytes(qk_dtype, B, T, S);
     int nc, ck;
     tc_plan(qk_dtype, B, T, S, &nc, &ck);
-    return nc <= 1 ? 0 : tc_indexer_workspace_bytes(qk_dtype, B, T, S, topk);
+    return nc <= 1 ? 0 : tc_indexer_workspace_bytes(qk_dtype, B, T, S, topk, false);
 }
 
 cudaError_t launch_indexer_tc(const IndexerArgs& a, void* workspace, cudaStream_t st) {
@@ -678,6 +679,10 @@ cudaError_t launch_indexer_tc(const IndexerArgs& a, void* workspace, cudaStream_
     if (rows_per_unit(a.qk_dtype, a.T) == 1)
         return a.qk_dtype == TSI_E4M3 ? launch_qk<TSI_E4M3, 1, false>(a, workspace, st)
                                       : launch_qk<TSI_BF16, 1, false>(a, workspace, st);
+    if (a.onchip)
+        return a.qk_dtype == TSI_E4M3
+                   ? launch_qk<TSI_E4M3, TileCfg<TSI_E4M3>::kRows, false>(a, workspace, st)
+                   : launch_qk<TSI_BF16, TileCfg<TSI_BF16>::kRows, false>(a, workspace, st);
     return a.qk_dtype == TSI_E4M3
                ? launch_qk<TSI_E4M3, TileCfg<TSI_E4M3>::kRows, true>(a, workspace, st)
                : launch_qk<TSI_BF16, TileCfg<TSI_BF16>::kRows, true>(a, workspace, st);

@@ -72,6 +72,61 @@ bool use_tc_attn(int H, int Hkv, int Dqk, int Dv, bool v_from_k) {
 
 }  // namespace
 
+namespace {
+
+size_t indexer_workspace(int B, int T, int S, int H_I, int d_I, int topk, int qk_dtype,
+                         bool onchip) {
+    if (B <= 0 || T <= 0 || S < 0 || topk < 1) return 0;
+    if (use_tc_indexer(qk_dtype, H_I, d_I))
+        return tsi::tc_indexer_workspace_bytes(qk_dtype, B, T, S, topk, onchip);
+    return tsi::generic_workspace_bytes(B, T, S, topk);
+}
+
+// tsi_indexer_topk and its on-chip form: onchip keeps the tensor-core path's scores in
+// the scoring kernel (selection in its epilogue) instead of storing them for a second pass.
+tsi_status indexer_topk(const void* qI, const void* kI, const void* w, int qk_dtype, int w_dtype,
+                        int B, int T, int S, int H_I, int d_I, int topk, const int32_t* kv_len,
+                        int32_t* idx, float* score, void* workspace, size_t workspace_bytes,
+                        void* stream, bool onchip) {
+    if (!qk_dtype_ok(qk_dtype)) return fail(TSI_ERR_INVALID_ARG, "qk_dtype %d unknown", qk_dtype);
+    if (!w_dtype_ok(w_dtype)) return fail(TSI_ERR_INVALID_ARG, "w_dtype %d unknown", w_dtype);
+    if (B < 0 || T < 0 || S < 0)
+        return fail(TSI_ERR_INVALID_ARG, "negative size (B=%d T=%d S=%d)", B, T, S);
+    if (topk < 1 || topk > TSI_MAX_TOPK)
+        return fail(TSI_ERR_UNSUPPORTED, "topk=%d outside [1, %d]", topk, TSI_MAX_TOPK);
+    if (H_I < 1 || d_I < 1) return fail(TSI_ERR_INVALID_ARG, "H_I=%d d_I=%d", H_I, d_I);
+    const bool tc = use_tc_indexer(qk_dtype, H_I, d_I);
+    if (!tc && !tsi::generic_supported(H_I, d_I))
+        return fail(TSI_ERR_UNSUPPORTED, "H_I=%d d_I=%d unsupported (d_I<=256, H_I<=128, "
+                    "H_I*d_I<=8192)", H_I, d_I);
+    if (static_cast<int64_t>(B) * T > (1ll << 31) - 1 || static_cast<int64_t>(B) * S > (1ll << 31) - 1)
+        return fail(TSI_ERR_UNSUPPORTED, "B*T or B*S exceeds 2^31-1");
+    if (B == 0 || T == 0) return ok();
+    if (!qI || !w || !idx || (S > 0 && !kI))
+        return fail(TSI_ERR_INVALID_ARG, "NULL tensor pointer");
+    if (!aligned16(qI) || !aligned16(kI) || !aligned16(w) || !aligned16(idx) ||
+        !aligned16(score) || !aligned16(kv_len))
+        return fail(TSI_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+    const size_t need = indexer_workspace(B, T, S, H_I, d_I, topk, qk_dtype, onchip);
+    if (workspace_bytes < need || (need > 0 && !workspace))
+        return fail(TSI_ERR_WORKSPACE, "workspace %zu bytes, need %zu", workspace_bytes, need);
+    if (need > 0 && !aligned16(workspace))
+        return fail(TSI_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+    unsigned* err = nullptr;
+    tsi_status st = device_error_word(&err);
+    if (st != TSI_OK) return st;
+    tsi::IndexerArgs a{qI, kI, w, qk_dtype, w_dtype, B, T, S, H_I, d_I, topk, kv_len,
+                       idx, score, err};
+    a.onchip = onchip;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = tc ? tsi::launch_indexer_tc(a, workspace, s)
+                       : tsi::launch_indexer_generic(a, workspace, s);
+    if (e != cudaSuccess) return fail(TSI_ERR_CUDA, "indexer launch: %s", cudaGetErrorString(e));
+    return ok();
+}
+
+}  // namespace
+
 extern "C" {
 
 int tsi_version(void) { return 100; }
@@ -93,49 +148,28 @@ const char* tsi_last_error(void) { return g_msg; }
 
 size_t tsi_indexer_topk_workspace(int B, int T, int S, int H_I, int d_I, int topk,
                                   int qk_dtype) {
-    if (B <= 0 || T <= 0 || S < 0 || topk < 1) return 0;
-    if (use_tc_indexer(qk_dtype, H_I, d_I)) return tsi::tc_indexer_workspace_bytes(qk_dtype, B, T, S, topk);
-    return tsi::generic_workspace_bytes(B, T, S, topk);
+    return indexer_workspace(B, T, S, H_I, d_I, topk, qk_dtype, false);
+}
+
+size_t tsi_indexer_topk_onchip_workspace(int B, int T, int S, int H_I, int d_I, int topk,
+                                         int qk_dtype) {
+    return indexer_workspace(B, T, S, H_I, d_I, topk, qk_dtype, true);
 }
 
 tsi_status tsi_indexer_topk(const void* qI, const void* kI, const void* w, int qk_dtype,
                             int w_dtype, int B, int T, int S, int H_I, int d_I, int topk,
                             const int32_t* kv_len, int32_t* idx, float* score, void* workspace,
                             size_t workspace_bytes, void* stream) {
-    if (!qk_dtype_ok(qk_dtype)) return fail(TSI_ERR_INVALID_ARG, "qk_dtype %d unknown", qk_dtype);
-    if (!w_dtype_ok(w_dtype)) return fail(TSI_ERR_INVALID_ARG, "w_dtype %d unknown", w_dtype);
-    if (B < 0 || T < 0 || S < 0)
-        return fail(TSI_ERR_INVALID_ARG, "negative size (B=%d T=%d S=%d)", B, T, S);
-    if (topk < 1 || topk > TSI_MAX_TOPK)
-        return fail(TSI_ERR_UNSUPPORTED, "topk=%d outside [1, %d]", topk, TSI_MAX_TOPK);
-    if (H_I < 1 || d_I < 1) return fail(TSI_ERR_INVALID_ARG, "H_I=%d d_I=%d", H_I, d_I);
-    const bool tc = use_tc_indexer(qk_dtype, H_I, d_I);
-    if (!tc && !tsi::generic_supported(H_I, d_I))
-        return fail(TSI_ERR_UNSUPPORTED, "H_I=%d d_I=%d unsupported (d_I<=256, H_I<=128, "
-                    "H_I*d_I<=8192)", H_I, d_I);
-    if (static_cast<int64_t>(B) * T > (1ll << 31) - 1 || static_cast<int64_t>(B) * S > (1ll << 31) - 1)
-        return fail(TSI_ERR_UNSUPPORTED, "B*T or B*S exceeds 2^31-1");
-    if (B == 0 || T == 0) return ok();
-    if (!qI || !w || !idx || (S > 0 && !kI))
-        return fail(TSI_ERR_INVALID_ARG, "NULL tensor pointer");
-    if (!aligned16(qI) || !aligned16(kI) || !aligned16(w) || !aligned16(idx) ||
-        !aligned16(score) || !aligned16(kv_len))
-        return fail(TSI_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
-    const size_t need = tsi_indexer_topk_workspace(B, T, S, H_I, d_I, topk, qk_dtype);
-    if (workspace_bytes < need || (need > 0 && !workspace))
-        return fail(TSI_ERR_WORKSPACE, "workspace %zu bytes, need %zu", workspace_bytes, need);
-    if (need > 0 && !aligned16(workspace))
-        return fail(TSI_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
-    unsigned* err = nullptr;
-    tsi_status st = device_error_word(&err);
-    if (st != TSI_OK) return st;
-    tsi::IndexerArgs a{qI, kI, w, qk_dtype, w_dtype, B, T, S, H_I, d_I, topk, kv_len,
-                       idx, score, err};
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = tc ? tsi::launch_indexer_tc(a, workspace, s)
-                       : tsi::launch_indexer_generic(a, workspace, s);
-    if (e != cudaSuccess) return fail(TSI_ERR_CUDA, "indexer launch: %s", cudaGetErrorString(e));
-    return ok();
+    return indexer_topk(qI, kI, w, qk_dtype, w_dtype, B, T, S, H_I, d_I, topk, kv_len, idx, score,
+                        workspace, workspace_bytes, stream, false);
+}
+
+tsi_status tsi_indexer_topk_onchip(const void* qI, const void* kI, const void* w, int qk_dtype,
+                                   int w_dtype, int B, int T, int S, int H_I, int d_I, int topk,
+                                   const int32_t* kv_len, int32_t* idx, float* score,
+                                   void* workspace, size_t workspace_bytes, void* stream) {
+    return indexer_topk(qI, kI, w, qk_dtype, w_dtype, B, T, S, H_I, d_I, topk, kv_len, idx, score,
+                        workspace, workspace_bytes, stream, true);
 }
 
 size_t tsi_indexer_topk_shard_workspace(int B, int T, int S_shard, int H_I, int d_I, int topk,
