@@ -178,7 +178,8 @@ __global__ void __launch_bounds__(kRowThreads) topk_rows_kernel(const ScoreRows 
                           (2 * limit);
         const int held = sel.settled_count();
         if (held > m) {
-            sel.compact(static_cast<int>(m), held, false, static_cast<int>(m / 4));
+            // only the threshold is needed: the buffer is emptied right after
+            sel.compact(static_cast<int>(m), held, false, static_cast<int>(m / 4), false);
             start = *reinterpret_cast<volatile uint64_t*>(sel.thr);
         }
         sel.restart(start);

@@ -232,8 +232,9 @@ struct TopKSelector {
     // exactly k keys are kept.  Otherwise stop at the first digit whose bin keeps at most
     // k + slack keys: every key dropped is below the k-th largest, so nothing of the
     // final top k is lost.  The admission threshold rises to the kept bin's lower edge.
-    // Between compactions hist[] is all zero and rng[0] is 0.
-    __device__ void compact(int k, int n, bool exact = true, int slack = 0) {
+    // move = false only sets that threshold and leaves the buffer as it is (for a caller
+    // that empties it next).  Between compactions hist[] is all zero and rng[0] is 0.
+    __device__ void compact(int k, int n, bool exact = true, int slack = 0, bool move = true) {
         if (n <= k) return;
         constexpr int U = 4;  // keys in flight per thread
         uint64_t hi = 0ull;
@@ -337,6 +338,11 @@ struct TopKSelector {
             shift -= width;
         }
         const int kept = k - need + inbin;
+        if (!move) {  // every thread has read ctl[] before the loop's last barrier
+            if (tid == 0) *thr = prefix;
+            sync();
+            return;
+        }
         // keep keys >= prefix, compacted to the front in place.  Each round reads the next
         // kRound * NT slots into registers before any thread writes; a write lands below
         // the count kept so far, which is below every later read.  A warp reserves the
