@@ -78,15 +78,26 @@ def test_config2_indexer_int_e4m3_exact(cuda_lib):
 
 def test_config3_group_bf16(cuda_lib):
     cfg = get_config(3)
-    rows = stratified_rows(cfg.T, 40, cfg.topk)
-    rec = _group(cuda_lib, cfg, 0, rows, stratified_rows(cfg.T, 16, cfg.topk), exact=False)
+    rows = stratified_rows(cfg.T, 260, cfg.topk)
+    arows = stratified_rows(cfg.T, 66, cfg.topk)
+    assert len(rows) >= 256 and len(arows) >= 64
+    rec = _group(cuda_lib, cfg, 0, rows, arows, exact=False)
     assert rec > 0.99
 
 
-def test_config4_group_e4m3_full_size(cuda_lib):
+@pytest.mark.parametrize("group", [0, 1, 2, 3])
+def test_config4_group_e4m3_full_size(cuda_lib, group):
+    # every IndexShare group of the 16-layer stack: 256 stratified indexer rows and 64
+    # attention rows per layer, the sample shifted per group so the groups cover different rows
     cfg = get_config(4)
-    rows = stratified_rows(cfg.T, 12, cfg.topk)
-    rec = _group(cuda_lib, cfg, 0, rows, stratified_rows(cfg.T, 8, cfg.topk), exact=False)
+    shift = 997 * group
+    rows = [(r + shift) % cfg.T if 0 < r < cfg.T - 2 else r
+            for r in stratified_rows(cfg.T, 260, cfg.topk)]
+    arows = [(r + shift) % cfg.T if 0 < r < cfg.T - 2 else r
+             for r in stratified_rows(cfg.T, 66, cfg.topk)]
+    rows, arows = sorted(set(rows)), sorted(set(arows))
+    assert len(rows) >= 256 and len(arows) >= 64
+    rec = _group(cuda_lib, cfg, group, rows, arows, exact=False)
     assert rec > 0.99
 
 

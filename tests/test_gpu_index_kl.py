@@ -4,8 +4,11 @@ log-partitions it is fed (tsi_sparse_attn_group_lse), against the oracle.
 Tolerances, from the arithmetic: the kernel's logits are bf16 products summed in fp32 on
 the tensor core (relative error ~1e-6 of |logit| <~ 10), its exponentials ex2.approx
 (~2^-22), its head / layer sums fp32: pbar within 2e-4 relative.  The attention's
-log-partition sums the bf16-rounded probabilities that multiply V (each within 2^-9),
-so it sits within 2e-3 of the exact one, and pbar computed from it within 5e-3."""
+log-partition sums the bf16-rounded probabilities that multiply V (each within a relative
+2^-8), so it sits within ln(1 + 2^-8) < 3.9e-3 of the exact one; with N(0, 1) inputs many
+keys share a head's weight and their rounding errors average out, so these rows stay within
+2e-3, and pbar computed from it within 5e-3 (the rescale tests, with one key dominating a
+head, use the full bound)."""
 import numpy as np
 import pytest
 import torch
