@@ -29,6 +29,7 @@ sys.path.insert(0, ROOT)
 METRIC = "indexer+top-k query rows/s and group prefill tok/s @L=128K; % TC peak / HBM BW"
 UNIT = "tok/s"
 FP8_PER_BF16 = 2.0  # nominal dense FP8 : BF16 tensor ratio (4.5 : 2.25 PFLOP/s)
+NOMINAL_TFLOPS = {"e4m3": 4500.0, "bf16": 2250.0}  # datasheet dense peaks, context only
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -268,7 +269,11 @@ def run_gpu(args, rank, world):
                                              _traffic_workload(cfg, "group")),
                 "algorithmic_flops_per_launch": idx_flops, "ms_per_launch": round(ms_idx, 4),
                 "peak_source": f"{peaks['source']} bf16 sustained x {FP8_PER_BF16:g} (fp8)"
-                               if cfg.qk_dtype == "e4m3" else f"{peaks['source']} bf16 sustained"}
+                               if cfg.qk_dtype == "e4m3" else f"{peaks['source']} bf16 sustained",
+                "frac_of_burst": round(idx_achieved / (peaks["bf16_tflops"] * (
+                    FP8_PER_BF16 if cfg.qk_dtype == "e4m3" else 1.0)), 4),
+                "frac_of_nominal": round(idx_achieved / NOMINAL_TFLOPS.get(cfg.qk_dtype, 1e30), 4),
+                "scores_to_hbm": False}
     if cfg.T == 1:
         # decode: one query per sequence scans its whole key cache once -- HBM-bound
         idx_bytes = accounting.indexer_bytes(rows, cfg.B * cfg.S, cfg.H_I, cfg.d_I, qk_bytes,
@@ -315,13 +320,15 @@ def run_gpu(args, rank, world):
                          "ms_draft_recomputing_indices": round(n * (ms_idx + ms_attn), 4)}
     if cfg.T == 1:
         result["decode_graph"] = measure_decode_graph(cfg, ind, lay, idx, outs, ws)
+    elif cfg.id == 4 and not args.no_decode and not args.tail_rows and not args.groups:
+        result["decode"] = measure_decode(dev)
     if G >= 2 and not args.no_overlap:
         result["overlap"] = measure_overlap(cfg, ind, idx, ws, stream)
     if not args.no_cp:
         result["context_parallel"] = measure_cp(cfg, ind, idx, stream)
-    if cfg.T > 1 and tsi.indexer_path(qk_code, cfg.H_I, cfg.d_I) == 1:
-        result["indexer_onchip"] = measure_onchip(cfg, ind, idx, stream, idx_flops, tc_peak,
-                                                  ms_idx, qk_code)
+    if cfg.T > 1 and tsi.indexer_path(qk_code, cfg.H_I, cfg.d_I) == 1 and not args.no_two_pass:
+        result["indexer_two_pass"] = measure_two_pass(cfg, ind, idx, stream, idx_flops, tc_peak,
+                                                      ms_idx, qk_code)
     if not args.no_kl and cfg.n_layers >= 1 and \
             tsi.attn_path(cfg.H, cfg.Hkv, cfg.Dqk, cfg.Dv, cfg.v_from_k) == 1:
         result["index_kl"] = measure_index_kl(cfg, ind, lay, idx, outs, ws, stream)
@@ -367,10 +374,11 @@ def _balanced_edges(cfg, shards, align=128):
     return edges
 
 
-def measure_onchip(cfg, ind, idx, stream, flops, peak, ms_default, qk_code, reps=2):
-    """Group 0's indexer + top-k with every score kept on chip (tsi_indexer_topk_onchip: the
-    selection runs in the scoring kernel's epilogue), beside the default two-pass call: time
-    per call, the fraction of the tensor peak, and whether the rows equal the default's."""
+def measure_two_pass(cfg, ind, idx, stream, flops, peak, ms_default, qk_code, reps=2):
+    """Group 0's indexer + top-k through the two-pass alternative (tsi_indexer_topk_two_pass:
+    every score stored to HBM, then selected by a second kernel) beside the default, which
+    keeps every score on chip: time per call, the fraction of the tensor peak, and whether
+    the rows equal the default's."""
     import torch
 
     import top_selection_indexer_gb300 as tsi
@@ -378,27 +386,32 @@ def measure_onchip(cfg, ind, idx, stream, flops, peak, ms_default, qk_code, reps
     qI, kI, w = ind[0]
     out = torch.empty_like(idx)
     ws = torch.empty(max(1, tsi.indexer_topk_workspace(cfg.B, cfg.T, cfg.S, cfg.H_I, cfg.d_I,
-                                                       cfg.topk, qk_code, onchip=True)),
+                                                       cfg.topk, qk_code, two_pass=True)),
                      dtype=torch.uint8, device=idx.device)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(reps)]
     for r in range(reps + 1):  # the first call warms up
         if r:
             ev[r - 1][0].record(stream)
-        tsi.indexer_topk(qI, kI, w, cfg.topk, idx=out, workspace=ws, stream=stream, onchip=True)
+        tsi.indexer_topk(qI, kI, w, cfg.topk, idx=out, workspace=ws, stream=stream,
+                         two_pass=True)
         if r:
             ev[r - 1][1].record(stream)
     tsi.device_status(stream)
     ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    del ws
     tsi.indexer_topk(qI, kI, w, cfg.topk, idx=idx, stream=stream)
     same = bool(torch.equal(out, idx))
     tf = flops / (ms / 1e3) / 1e12
     return {"ms_per_call": round(ms, 3), "achieved_tflops": round(tf, 1),
-            "frac": round(tf / peak, 4), "ms_default_two_pass": round(ms_default, 3),
+            "frac": round(tf / peak, 4), "ms_default_onchip": round(ms_default, 3),
             "equals_default": same,
-            "workspace_bytes": int(ws.numel()),
-            "note": "scores kept in the scoring kernel (selection in its epilogue); the default "
-                    "call stores them for a second pass"}
+            "workspace_bytes": int(tsi.indexer_topk_workspace(cfg.B, cfg.T, cfg.S, cfg.H_I,
+                                                              cfg.d_I, cfg.topk, qk_code,
+                                                              two_pass=True)),
+            "note": "scores stored to HBM by the scoring kernel, then selected by a second "
+                    "kernel; the default keeps them on chip (selection in the scoring "
+                    "kernel's epilogue from a sampled threshold)"}
 
 
 def measure_cp(cfg, ind, idx, stream, shards=2, reps=3):
@@ -471,10 +484,12 @@ def measure_overlap(cfg, ind, idx, ws, stream, reps=5):
             "algorithmic_bytes_per_launch": nbytes, "mean_overlap_rate": round(rate, 5)}
 
 
-def measure_decode_graph(cfg, ind, lay, idx, outs, ws, reps=20):
+def measure_decode_graph(cfg, ind, lay, idx, outs, ws, reps=20, flush=None):
     """Latency of one IndexShare group of a decode step (the Full layer's indexer + top-k,
     then the group's sparse attention layers) replayed from a CUDA graph, against the same
-    calls launched one by one."""
+    calls launched one by one.  With ``flush`` (a device buffer larger than L2) the buffer is
+    overwritten before every timed repetition, so no repetition finds the previous one's
+    keys in L2."""
     import torch
 
     import top_selection_indexer_gb300 as tsi
@@ -504,17 +519,29 @@ def measure_decode_graph(cfg, ind, lay, idx, outs, ws, reps=20):
     torch.cuda.synchronize()
 
     def timed(fn):
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(side):
             for _ in range(3):
                 fn()
-            a.record(side)
+            if flush is None:
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(side)
+                for _ in range(reps):
+                    fn()
+                b.record(side)
+                b.synchronize()
+                return a.elapsed_time(b) / reps * 1e3
+            evs = []
             for _ in range(reps):
+                flush.add_(1)
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(side)
                 fn()
-            b.record(side)
-        b.synchronize()
-        return a.elapsed_time(b) / reps * 1e3
+                b.record(side)
+                evs.append((a, b))
+        torch.cuda.synchronize()
+        return statistics.median(a.elapsed_time(b) for a, b in evs) * 1e3
 
     us_graph = timed(graph.replay)
     us_eager = timed(lambda: group_step(side))
@@ -522,7 +549,87 @@ def measure_decode_graph(cfg, ind, lay, idx, outs, ws, reps=20):
     return {"what": f"one group of a decode step: indexer + top-k of the Full layer, then "
                     f"{len(layers)} sparse-attention layers (B={cfg.B}, one query each)",
             "kernel_launches": int(launches), "us_graph_replay": round(us_graph, 2),
-            "us_eager": round(us_eager, 2), "reps": reps}
+            "us_eager": round(us_eager, 2), "reps": reps,
+            "l2": "flushed before every repetition" if flush is not None else "not flushed"}
+
+
+def measure_decode(dev, reps=30):
+    """The decode workload (B = 8 sequences, one new query each over a 131072-token cache,
+    one IndexShare group of 4 layers), timed after the prefill step: the indexer + top-k
+    and each attention layer with CUDA events (median over repetitions, L2 flushed before
+    each), the group replayed from a CUDA graph, and their HBM fractions in algorithmic
+    bytes.  Its tensors are freed afterwards."""
+    import torch
+
+    import top_selection_indexer_gb300 as tsi
+    from top_selection_indexer_gb300 import accounting
+    from workloads import get_config, make_attn_inputs, make_indexer_inputs
+
+    cfg = get_config(5)
+    stream = torch.cuda.current_stream()
+    ind = [make_indexer_inputs(cfg, 0, dev)]
+    lay = [make_attn_inputs(cfg, l, dev) for l in range(cfg.group)]
+    idx = torch.empty((cfg.B, cfg.T, cfg.topk), dtype=torch.int32, device=dev)
+    outs = [torch.empty((cfg.B, cfg.T, cfg.H, cfg.Dv), dtype=torch.bfloat16, device=dev)
+            for _ in range(cfg.group)]
+    code = tsi.E4M3
+    ws = torch.empty(max(16, tsi.indexer_topk_workspace(cfg.B, cfg.T, cfg.S, cfg.H_I, cfg.d_I,
+                                                        cfg.topk, code),
+                         tsi.sparse_attn_workspace(cfg.B, cfg.T, cfg.S, cfg.H, cfg.Hkv,
+                                                   cfg.Dqk, cfg.Dv, cfg.topk)),
+                     dtype=torch.uint8, device=dev)
+    flush = torch.zeros(64 << 20, dtype=torch.float32, device=dev)  # 256 MB > L2
+    qI, kI, w = ind[0]
+
+    def stage(fn):
+        for _ in range(3):
+            fn()
+        evs = []
+        for _ in range(reps):
+            flush.add_(1)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            evs.append((a, b))
+        torch.cuda.synchronize()
+        return statistics.median(a.elapsed_time(b) for a, b in evs) * 1e3
+
+    us_idx = stage(lambda: tsi.indexer_topk(qI, kI, w, cfg.topk, idx=idx, workspace=ws,
+                                            stream=stream))
+    us_attn = [stage(lambda l=l: tsi.sparse_attn_group(
+        [lay[l][0]], [lay[l][1]], None, idx, cfg.scale, outs=[outs[l]], workspace=ws,
+        stream=stream, Dv=cfg.Dv)) for l in range(cfg.group)]
+    tsi.device_status(stream)
+    graph = measure_decode_graph(cfg, ind, lay, idx, outs, ws, reps=reps, flush=flush)
+    peaks = _peaks()
+    rows = cfg.B * cfg.T
+    idx_bytes = accounting.indexer_bytes(rows, cfg.B * cfg.S, cfg.H_I, cfg.d_I, 1, 2, cfg.topk)
+    valid_k = accounting.selected_pairs(cfg.B, cfg.T, cfg.S, cfg.topk)
+    attn_bytes = accounting.attn_bytes(valid_k, rows, cfg.H, cfg.Hkv, cfg.Dqk, cfg.Dv, cfg.topk,
+                                       cfg.v_from_k)
+    us_attn_mean = statistics.mean(us_attn)
+    res = {"workload": f"decode B={cfg.B} over L={cfg.S}: indexer H_I={cfg.H_I} d_I={cfg.d_I} "
+                       f"e4m3, k={cfg.topk}, {cfg.group} layers of MQA {cfg.H} heads over a "
+                       f"{cfg.Dqk}-d bf16 latent cache",
+           "us_indexer_topk": round(us_idx, 2),
+           "us_attn_per_layer": round(us_attn_mean, 2),
+           "us_group_graph": graph["us_graph_replay"], "us_group_eager": graph["us_eager"],
+           "kernel_launches_per_group": graph["kernel_launches"],
+           "tok_s": round(rows / (graph["us_graph_replay"] / 1e6), 1),
+           "indexer_hbm": {"algorithmic_bytes": idx_bytes,
+                           "achieved_gbs": round(idx_bytes / (us_idx / 1e6) / 1e9, 1),
+                           "frac": round(idx_bytes / (us_idx / 1e6) / 1e9 / peaks["hbm_gbs"], 4)},
+           "attn_hbm": {"algorithmic_bytes": attn_bytes,
+                        "achieved_gbs": round(attn_bytes / (us_attn_mean / 1e6) / 1e9, 1),
+                        "frac": round(attn_bytes / (us_attn_mean / 1e6) / 1e9 / peaks["hbm_gbs"],
+                                      4)},
+           "peak_source": f"{peaks['source']} hbm_gbs",
+           "l2": "a 256 MB buffer is overwritten before every timed repetition"}
+    del ind, lay, idx, outs, ws, flush
+    torch.cuda.empty_cache()
+    return res
 
 
 def measure_index_kl(cfg, ind, lay, idx, outs, ws, stream, reps=2):
@@ -619,7 +726,8 @@ def run_e2e(args, cfg, ind, lay, idx, outs, ws, stream, world, n_copy_streams=4)
     downs = [torch.cuda.Stream(device=idx.device) for _ in range(n_copy_streams)]
     ev = lambda: torch.cuda.Event()  # noqa: E731
     h2d = d2h = 0
-    steps = max(1, min(args.steps, 2))
+    steps = max(5, min(args.steps, 8))
+    decode = cfg.T == 1  # a decode step uploads the new token only, not the caches
     # events of the previous step: layer / group kernels done, read-backs done
     attn_done = [None] * nl
     idx_done = [None] * G
@@ -647,12 +755,31 @@ def run_e2e(args, cfg, ind, lay, idx, outs, ws, stream, world, n_copy_streams=4)
                 done.append(e)
         return done
 
+    def new_token_copy(cache, h_cache, after):
+        """The newest cached row of every sequence (position S - 1) from the pinned host
+        copy: one small copy per sequence, on the first upload stream."""
+        st = ups[0]
+        with torch.cuda.stream(st):
+            for e in after:
+                if e is not None:
+                    st.wait_event(e)
+            for b in range(cache.shape[0]):
+                cache[b, -1].copy_(h_cache[b, -1], non_blocking=True)
+            e = ev()
+            e.record(st)
+        return [e], cache.shape[0] * cache[0, -1].numel() * cache.element_size()
+
     def step():
         nonlocal h2d, d2h
         in_ready, ind_ready = [], []
         for g in range(G):  # uploads, in the order the kernels need them
             evs = []
-            for hx, dx in zip(h_ind, ind[g]):
+            for j, (hx, dx) in enumerate(zip(h_ind, ind[g])):
+                if decode and j == 1:  # the key cache: only the new token's row
+                    e, n = new_token_copy(dx, hx, [idx_done[g]])
+                    evs += e
+                    h2d += n
+                    continue
                 evs += split_copy(dx, hx, ups, [idx_done[g]])
                 h2d += hx.numel() * hx.element_size()
             ind_ready.append(evs)
@@ -660,8 +787,14 @@ def run_e2e(args, cfg, ind, lay, idx, outs, ws, stream, world, n_copy_streams=4)
                 layer = g * cfg.group + l0
                 Q, K, V = lay[layer]
                 evs = split_copy(Q, h_Q, ups, [attn_done[layer]])
-                evs += split_copy(K, h_K, ups, [attn_done[layer]])
-                h2d += h_Q.numel() * 2 + h_K.numel() * 2
+                h2d += h_Q.numel() * 2
+                if decode:
+                    e, n = new_token_copy(K, h_K, [attn_done[layer]])
+                    evs += e
+                    h2d += n
+                else:
+                    evs += split_copy(K, h_K, ups, [attn_done[layer]])
+                    h2d += h_K.numel() * 2
                 if V is not None:  # separate values (MHA); the MQA latent carries them
                     evs += split_copy(V, h_V, ups, [attn_done[layer]])
                     h2d += h_V.numel() * 2
@@ -714,8 +847,11 @@ def run_e2e(args, cfg, ind, lay, idx, outs, ws, stream, world, n_copy_streams=4)
     return {"value": round(world * G * cfg.B * cfg.T / (ms / 1e3), 2), "unit": UNIT,
             "h2d_bytes_per_step": h2d // steps, "d2h_bytes_per_step": d2h // steps,
             "ms_per_step": round(ms, 2), "steps": steps,
-            "note": f"every layer uploads Q and the latent from one pinned host buffer; "
-                    f"copies run on {n_copy_streams} streams per direction, overlapping the "
+            "note": (f"decode: every step uploads the new token only (queries, gate weights, "
+                     f"each layer's Q, and the newest row of the key and latent caches), the "
+                     f"caches stay resident; " if decode else
+                     f"every layer uploads Q and the latent from one pinned host buffer; ")
+                    + f"copies run on {n_copy_streams} streams per direction, overlapping the "
                     f"kernels; read back: "
                     + ("every layer's output and the index rows" if args.readback == "all"
                        else "the step's result (the last layer's output; the index rows "
@@ -724,9 +860,13 @@ def run_e2e(args, cfg, ind, lay, idx, outs, ws, stream, world, n_copy_streams=4)
 
 # ----------------------------------------------------------------------------- CPU oracle
 
-def run_cpu_oracle(cfg_id, budget_s, on_device=None):
+def run_cpu_oracle(cfg_id, n_idx_rows=None, n_att_rows=None, phase=0):
     """Time the CPU oracle on a bounded, stratified row sample of one IndexShare group of
-    the workload and scale it to the metric (group prefill tok/s)."""
+    the workload and scale it to the metric (group prefill tok/s).
+
+    Default sample: every row up to L = 8192, 512 rows at L = 32768, 256 beyond (the
+    indexer + top-k), and 64 of them through the group's attention layers; ``phase``
+    shifts the sample so repeated calls cover different rows."""
     import torch
 
     import oracle
@@ -737,8 +877,16 @@ def run_cpu_oracle(cfg_id, budget_s, on_device=None):
     cfg = get_config(cfg_id)
     cores = oracle.n_threads_default()
     T, S = cfg.T, cfg.S
-    n_idx_rows = max(cores, 2 * cores)
-    rows = np.unique(np.linspace(cfg.B * T - 1, 0, n_idx_rows).astype(np.int64))
+    n_all = cfg.B * T
+    if n_idx_rows is None:
+        n_idx_rows = n_all if T <= 8192 else 512 if T <= 32768 else 256
+    n_idx_rows = min(n_idx_rows, n_all)
+    if n_att_rows is None:
+        n_att_rows = 64
+    step = n_all / n_idx_rows
+    off = (phase * 0.618034 * step) % step if n_idx_rows < n_all else 0.0
+    rows = np.unique(np.minimum(n_all - 1, (np.arange(n_idx_rows) * step + off).astype(np.int64)))
+    rows = rows[::-1].copy()  # longest rows first
     # keys of row r (sequence r // T, query r % T at position S - T + r % T)
     n_keys = lambda r: max(0, S - T + int(r) % T + 1)  # noqa: E731
     # inputs of the sampled rows only (same distributions as the workload)
@@ -751,17 +899,18 @@ def run_cpu_oracle(cfg_id, budget_s, on_device=None):
     work_idx = sum(n_keys(r) for r in rows)
     t_idx_full = t_idx * accounting.causal_pairs(cfg.B, T, S) / work_idx
     # attention: the group's layers on a subset of those rows
-    n_att = max(cores, 16)
-    arows = rows[:n_att]
+    arows = rows[np.unique(np.linspace(0, len(rows) - 1, min(n_att_rows, len(rows))).astype(int))]
     n_lay = min(cfg.group, cfg.n_layers)
     t_att = t_att_full = 0.0
     if n_lay:
         K = draw((cfg.B, S, cfg.Hkv, cfg.Dqk), "normal", "bf16", 4, "cpu")
         Qr = draw((len(arows), cfg.H, cfg.Dqk), "normal", "bf16", 5, "cpu")
         V = None if cfg.v_from_k else draw((cfg.B, S, cfg.Hkv, cfg.Dv), "normal", "bf16", 6, "cpu")
+        pos = {int(r): i for i, r in enumerate(rows)}
+        idx_sel = idx_rows[[pos[int(r)] for r in arows]]
         t0 = time.perf_counter()
         for _ in range(n_lay):
-            oracle.sparse_attn(Qr, K, V, idx_rows[:len(arows)], cfg.scale, T, arows, Dv=cfg.Dv)
+            oracle.sparse_attn(Qr, K, V, idx_sel, cfg.scale, T, arows, Dv=cfg.Dv)
         t_att = time.perf_counter() - t0
         work_att = n_lay * sum(min(cfg.topk, n_keys(r)) for r in arows)
         t_att_full = t_att * n_lay * accounting.selected_pairs(cfg.B, T, S, cfg.topk) / work_att
@@ -780,8 +929,11 @@ def run_reference(args, rank, world):
         return None
     vals = []
     info = None
-    for _ in range(args.warmup + args.steps):
-        info = run_cpu_oracle(args.config, budget_s=20)
+    cores = __import__("oracle").n_threads_default()
+    for i in range(args.warmup + args.steps):
+        # each step a bounded sample (two rows per core), shifted so the steps cover
+        # different rows of the workload
+        info = run_cpu_oracle(args.config, n_idx_rows=2 * cores, n_att_rows=cores, phase=i)
         vals.append(info["value"])
     v = statistics.mean(vals[args.warmup:]) if args.steps else vals[-1]
     from workloads import get_config
@@ -823,6 +975,11 @@ def main():
                     help="skip the group-centroid KL measurement")
     ap.add_argument("--no-overlap", action="store_true",
                     help="skip the cross-layer top-k overlap measurement after the timed steps")
+    ap.add_argument("--no-two-pass", action="store_true",
+                    help="skip timing the two-pass indexer beside the default")
+    ap.add_argument("--no-decode", action="store_true",
+                    help="skip the decode measurement (B = 8 over 131072 keys) after the "
+                         "prefill step")
     ap.add_argument("--tail-rows", type=int, default=0,
                     help="profiling: only the last R query rows of the prefill")
     ap.add_argument("--groups", type=int, default=0, help="profiling: only the first G groups")
@@ -847,7 +1004,7 @@ def main():
     res = run_gpu(args, rank, world)
     if rank == 0:
         if not args.no_cpu:
-            res["cpu_baseline"] = run_cpu_oracle(args.config, budget_s=20)
+            res["cpu_baseline"] = run_cpu_oracle(args.config)
         print(json.dumps(res), flush=True)
     if world > 1:
         dist.barrier()

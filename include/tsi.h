@@ -57,20 +57,26 @@ typedef enum { TSI_F32 = 0, TSI_BF16 = 1, TSI_E4M3 = 2 } tsi_dtype;
 
 /*
  * Workspace bytes needed by tsi_indexer_topk for these sizes (0 when none is needed).
- *   - Tensor-core path, T > 1: the fp32 scores of one chunk of query rows, rows of
- *     S (rounded up to 4) floats for every sequence, the chunk as many rows as fit in
- *     about 8 GiB (all T rows when they fit; at least the rows of one tensor-core unit).
- *     The rows are scored chunk by chunk, then each row's top-k is selected from its
- *     stored scores.
- *   - Tensor-core path, T = 1 (decode), and the CUDA-core path when rows are few and key
- *     ranges are split across thread blocks: candidate lists of 8-byte keys, topk per row
- *     and key split, plus a count per list (and merge staging space).
+ *   - Tensor-core path: candidate lists of 8-byte keys, topk per row (and per key split
+ *     when rows are few and long), plus a count per list.  With several query rows per
+ *     sequence and one key range per row, also the per-row admission thresholds, a list of
+ *     unit indices (4 B per 4 rows of e4m3, per 2 rows of bf16) and every 32nd key row of
+ *     the cache (B x ceil(S / 32) rows).  At B = 1, T = S = 131072, k = 2048: ~2.1 GB.
+ *   - Decode-sized requests (few rows, long caches) on either path: the per-split lists and
+ *     merge staging space.
  */
 size_t tsi_indexer_topk_workspace(int B, int T, int S, int H_I, int d_I, int topk,
                                   int qk_dtype);
 
 /*
  * Lightning-indexer score + causal top-k ("GLM-5.2 技术报告速览", §IndexShare).
+ * On the tensor-core path no score leaves the scoring kernel: each row's top k is
+ * selected in the kernel's epilogue (the pages' Ascend operator likewise fuses score,
+ * ReLU and top-k: "GLM-5: from Vibe Coding to Agentic Engineering" (Chinese translation),
+ * §5).  With several query rows per sequence the kernel first scores every 32nd key to
+ * set each row's admission threshold, then scores all keys admitting only those at or
+ * above it; rows the sample misjudged are redone from no threshold, so the result is exact
+ * for any input.
  *
  *   qI     [B, T, H_I, d_I]  qk_dtype (F32, BF16 or E4M3)   index queries
  *   kI     [B, S, d_I]       qk_dtype                        index-key cache
@@ -93,17 +99,9 @@ tsi_status tsi_indexer_topk(const void* qI, const void* kI, const void* w, int q
                             size_t workspace_bytes, void* stream);
 
 /*
- * The same results as tsi_indexer_topk, with every score kept on chip: on the tensor-core
- * path with several query rows per sequence, each 128-key tile is scored in tensor memory
- * and streamed into a shared-memory top-k selector per query row inside the scoring
- * kernel, so no score is written to HBM ("GLM-5.2 技术报告速览", §IndexShare; the Ascend
- * operator the pages describe also fuses score, ReLU and top-k).  tsi_indexer_topk instead
- * stores the scores of a chunk of rows and selects in a second kernel, which is faster on
- * a GB300 at the cost of ~8 GiB of workspace; this form needs only candidate lists
- * (8 B x topk per row, plus a count per row).  Shapes the tensor-core path does not take,
- * and one query row per sequence, run exactly as in tsi_indexer_topk.  Arguments, layouts
- * and rules as tsi_indexer_topk, with workspace_bytes >=
- * tsi_indexer_topk_onchip_workspace(...).
+ * tsi_indexer_topk under the name that states its property: every score stays on chip
+ * (same source, same passages as tsi_indexer_topk).  Arguments, layouts, rules and the
+ * workspace query are those of tsi_indexer_topk.
  */
 size_t tsi_indexer_topk_onchip_workspace(int B, int T, int S, int H_I, int d_I, int topk,
                                          int qk_dtype);
@@ -111,6 +109,25 @@ tsi_status tsi_indexer_topk_onchip(const void* qI, const void* kI, const void* w
                                    int w_dtype, int B, int T, int S, int H_I, int d_I, int topk,
                                    const int32_t* kv_len, int32_t* idx, float* score,
                                    void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * The same results as tsi_indexer_topk (same source: "GLM-5.2 技术报告速览", §IndexShare)
+ * from two passes on the tensor-core path with several query rows per sequence: the fp32
+ * scores of a chunk of query rows are written to the workspace (rows of S, rounded up to
+ * 4, floats for every sequence; the chunk as many rows as fit in about 8 GiB, all T rows
+ * when they fit), then one block per row selects and ranks its top k from them.  It costs
+ * 4 B of HBM writes and reads per causal pair.  Shapes the tensor-core path does not take,
+ * and one query row per sequence, run exactly as in tsi_indexer_topk.  Arguments, layouts
+ * and rules as tsi_indexer_topk, with workspace_bytes >=
+ * tsi_indexer_topk_two_pass_workspace(...).
+ */
+size_t tsi_indexer_topk_two_pass_workspace(int B, int T, int S, int H_I, int d_I, int topk,
+                                           int qk_dtype);
+tsi_status tsi_indexer_topk_two_pass(const void* qI, const void* kI, const void* w,
+                                     int qk_dtype, int w_dtype, int B, int T, int S, int H_I,
+                                     int d_I, int topk, const int32_t* kv_len, int32_t* idx,
+                                     float* score, void* workspace, size_t workspace_bytes,
+                                     void* stream);
 
 /*
  * tsi_indexer_topk without a workspace argument and without allocating anything.
@@ -248,10 +265,9 @@ tsi_status tsi_index_kl(int n_layers, const void* const* q, const void* const* k
  *   cand_cnt  [B*T] int32 (out): how many keys of the row the shard holds, at most topk
  *
  * Requires 0 <= key_offset, key_offset + S_shard <= S_total, and
- * workspace_bytes >= tsi_indexer_topk_shard_workspace(...): the stored scores of the
- * tensor-core path for T > 1 (as tsi_indexer_topk_workspace describes, with S_shard
- * keys), else 0 unless rows are few enough that keys are split across thread blocks.
- * Other rules as tsi_indexer_topk.
+ * workspace_bytes >= tsi_indexer_topk_shard_workspace(...): what tsi_indexer_topk_workspace
+ * describes for S_shard keys except the candidate lists, which are the caller's cand
+ * (0 when nothing else is needed).  Other rules as tsi_indexer_topk.
  */
 size_t tsi_indexer_topk_shard_workspace(int B, int T, int S_shard, int H_I, int d_I, int topk,
                                         int qk_dtype);

@@ -90,6 +90,23 @@ def _scores_bytes(B, T, S, R, budget=8 << 30):
     return B * rows * ld * 4
 
 
+def _align(x, a):
+    return (x + a - 1) // a * a
+
+
+def _lists_bytes(slots, topk=2048):
+    """One candidate list of topk 8-byte keys per slot, then a count per slot."""
+    return _align(slots * topk * 8, 16) + _align(slots * 4, 256)
+
+
+def _sampled_bytes(B, T, S, qk, R):
+    """Scratch of the sampled-threshold selection beside the lists: a threshold per row, the
+    short-unit count and list (one entry per unit of R rows), every 32nd key row."""
+    off = _align(B * T * 4, 256) + 256
+    off = _align(off + B * -(-T // R) * 4, 1024)
+    return off + _align(B * -(-S // 32) * (256 if qk == tsi.BF16 else 128), 1024)
+
+
 @pytest.mark.parametrize("B,T,S,qk,R", [
     (1, 300, 1000, tsi.E4M3, 4),        # all rows in one chunk
     (3, 5, 10, tsi.E4M3, 4),            # rows padded to 12 floats
@@ -98,20 +115,25 @@ def _scores_bytes(B, T, S, R, budget=8 << 30):
     (64, 4096, 131072, tsi.E4M3, 4),    # 256-row chunks across 64 sequences
 ])
 def test_two_pass_workspace_holds_one_chunk_of_scores(lib, B, T, S, qk, R):
-    need = lib.tsi_indexer_topk_workspace(B, T, S, 64, 128, 2048, qk)
+    need = lib.tsi_indexer_topk_two_pass_workspace(B, T, S, 64, 128, 2048, qk)
     assert need == _scores_bytes(B, T, S, R)
-    # key shards: the same scores, no candidate lists (the caller's take them)
-    assert lib.tsi_indexer_topk_shard_workspace(B, T, S, 64, 128, 2048, qk) == need
+    # key shards select on chip: the caller's lists take the candidates, the workspace
+    # holds the sampled selection's scratch only
+    assert lib.tsi_indexer_topk_shard_workspace(B, T, S, 64, 128, 2048, qk) == \
+        _sampled_bytes(B, T, S, qk, R)
 
 
-@pytest.mark.parametrize("B,T,S,qk", [(1, 131072, 131072, tsi.E4M3), (2, 3000, 3000, tsi.BF16)])
-def test_onchip_workspace_holds_candidate_lists_only(lib, B, T, S, qk):
-    # the on-chip form stores no score: one list of k 8-byte keys per row (these shapes
-    # have enough rows to keep each row's keys in one range) and a count per row
-    need = lib.tsi_indexer_topk_onchip_workspace(B, T, S, 64, 128, 2048, qk)
-    slots = B * T
-    assert need == (slots * 2048 * 8 + 15) // 16 * 16 + (slots * 4 + 255) // 256 * 256
-    assert need < lib.tsi_indexer_topk_workspace(B, T, S, 64, 128, 2048, qk) or T * S < 1 << 24
+@pytest.mark.parametrize("B,T,S,qk,R", [(1, 131072, 131072, tsi.E4M3, 4),
+                                        (2, 3000, 3000, tsi.BF16, 2)])
+def test_default_workspace_holds_candidate_lists_and_the_sample(lib, B, T, S, qk, R):
+    # the default stores no score: one list of k 8-byte keys per row (these shapes have
+    # enough rows to keep each row's keys in one range), a count per row, and the sampled
+    # selection's scratch; the on-chip name is the same call
+    need = lib.tsi_indexer_topk_workspace(B, T, S, 64, 128, 2048, qk)
+    assert need == _lists_bytes(B * T) + _sampled_bytes(B, T, S, qk, R)
+    assert lib.tsi_indexer_topk_onchip_workspace(B, T, S, 64, 128, 2048, qk) == need
+    assert need < lib.tsi_indexer_topk_two_pass_workspace(B, T, S, 64, 128, 2048, qk) or \
+        T * S < 1 << 24
 
 
 def test_decode_workspace_holds_candidate_lists(lib):

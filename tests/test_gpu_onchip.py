@@ -1,8 +1,9 @@
-"""GPU parity of tsi_indexer_topk_onchip (the scores stay in the scoring kernel, which
-selects each row's top k in its epilogue) against tsi_indexer_topk (scores stored, then
-selected by a second kernel) and the oracle.  Both compute every score the same way and
-select exactly, so their indices and scores must agree bit for bit; integer-valued inputs
-make both exact against the oracle."""
+"""GPU parity of tsi_indexer_topk (the scores stay in the scoring kernel, which selects each
+row's top k in its epilogue from a sampled threshold), its alias tsi_indexer_topk_onchip and
+tsi_indexer_topk_two_pass (scores stored, then selected by a second kernel), against each
+other and the oracle.  All compute every score the same way and select exactly, so their
+indices and scores must agree bit for bit; integer-valued inputs make them exact against
+the oracle."""
 import numpy as np
 import pytest
 import torch
@@ -33,14 +34,17 @@ CASES = [
 
 
 @pytest.mark.parametrize("B,T,S,H_I,d_I,qk,topk,kv", CASES)
-def test_onchip_equals_the_default_and_the_oracle(cuda_lib, B, T, S, H_I, d_I, qk, topk, kv):
+def test_default_onchip_and_two_pass_agree_with_the_oracle(cuda_lib, B, T, S, H_I, d_I, qk,
+                                                           topk, kv):
     qI, kI, w = _inputs(B, T, S, H_I, d_I, qk, 8100 + S + T)
     kv_t = None if kv is None else torch.tensor(kv, dtype=torch.int32, device="cuda")
-    a, sa = cuda_lib.indexer_topk(qI, kI, w, topk, kv_len=kv_t, want_score=True, onchip=True)
-    b, sb = cuda_lib.indexer_topk(qI, kI, w, topk, kv_len=kv_t, want_score=True)
+    a, sa = cuda_lib.indexer_topk(qI, kI, w, topk, kv_len=kv_t, want_score=True)
+    b, sb = cuda_lib.indexer_topk(qI, kI, w, topk, kv_len=kv_t, want_score=True, two_pass=True)
+    c, sc = cuda_lib.indexer_topk(qI, kI, w, topk, kv_len=kv_t, want_score=True, onchip=True)
     cuda_lib.device_status()
-    assert torch.equal(a, b)
+    assert torch.equal(a, b) and torch.equal(a, c)
     assert torch.equal(sa.view(torch.int32), sb.view(torch.int32))
+    assert torch.equal(sa.view(torch.int32), sc.view(torch.int32))
     rows = sorted({0, B * T - 1} | set(range(0, B * T, max(1, B * T // 9))))
     check_indexer(qI.cpu(), kI.cpu(), w.cpu(), topk, a.cpu(), sa.cpu(),
                   kv_len=None if kv is None else torch.tensor(kv), rows=np.array(rows),

@@ -1,0 +1,132 @@
+"""GPU parity of the default tensor-core indexer (tsi_indexer_topk) on inputs that defeat
+its sampled admission threshold, against the oracle.
+
+With several query rows per sequence the call first scores every 32nd key of each row and
+admits, in the full scoring pass, only keys at or above the row's ~109th largest sampled
+score (for k = 2048).  These inputs make that sample lie:
+
+- the sampled keys score low and all others high: the threshold admits every key, each
+  row's selector fills and compacts again and again;
+- the sampled keys alone score high: fewer than k keys reach the threshold, so every unit
+  is listed and done again from no threshold by the third launch;
+- half the rows of each four-row unit see the second pattern and half score every key 0
+  (all ties): units that are redone hold rows that were complete;
+- every score equal (zero gate weights).
+
+Queries and gates are positive integers and a key row holds one integer value, so every
+score is exact in fp32 and the oracle's rows must be matched bit for bit.  A full-size
+L = 131072 integer-valued prefill checks sampled rows of the common path.  (Score equation
+and k: "GLM-5.2 技术报告速览", §IndexShare; the lower-index tie rule: BASELINE's reading of
+the deterministic top-k of "GLM-5: from Vibe Coding to Agentic Engineering" (Chinese
+translation), §3.2.)
+"""
+import numpy as np
+import pytest
+import torch
+
+from parity import check_indexer
+from workloads.gen import draw
+
+pytestmark = pytest.mark.gpu
+
+H, D = 64, 128
+TORCH = {"e4m3": torch.float8_e4m3fn, "bf16": torch.bfloat16}
+# enough four-row (e4m3) or two-row (bf16) units to fill the GPU, so each row's keys stay
+# in one range and the sampled selection applies; rows are the last T of an S-key cache
+T, S, TOPK = 640, 60000, 2048
+
+
+def _check(cuda_lib, qI, kI, w, rows):
+    idx, sc = cuda_lib.indexer_topk(qI, kI, w, TOPK, want_score=True)
+    cuda_lib.device_status()
+    check_indexer(qI.cpu(), kI.cpu(), w.cpu(), TOPK, idx.cpu(), sc.cpu(), rows=np.array(rows),
+                  exact=True)
+    return idx.cpu()
+
+
+def _rows():
+    return sorted({0, 1, 2, 3, 4, 5, 6, 7, 321, 322, T - 2, T - 1})
+
+
+def _contrast(qk, sampled_value, other_value, seed, negative_rows=()):
+    """Positive integer queries (negated on `negative_rows`) and power-of-two gates; key s
+    is all `sampled_value` when the sample reads it (s % 32 == 0), else all `other_value`."""
+    qf = draw((1, T, H, D), "int8", "f32", seed, "cuda").abs()
+    qf = torch.where(qf == 0, torch.ones_like(qf), qf)
+    if len(negative_rows):
+        sign = torch.ones(T, device="cuda")
+        sign[torch.as_tensor(list(negative_rows), device="cuda")] = -1.0
+        qf = qf * sign.view(1, T, 1, 1)
+    pos = torch.arange(S, device="cuda")
+    kval = torch.where(pos % 32 == 0, sampled_value, other_value).to(torch.float32)
+    kI = kval.view(1, S, 1).expand(1, S, D).contiguous().to(TORCH[qk])
+    w = draw((1, T, H), "pow2", "bf16", seed + 1, "cuda")
+    return qf.to(TORCH[qk]), kI, w
+
+
+@pytest.mark.parametrize("qk", ["e4m3", "bf16"])
+def test_sampled_keys_low_admit_every_key(cuda_lib, qk):
+    qI, kI, w = _contrast(qk, 1.0, 4.0, 41)
+    idx = _check(cuda_lib, qI, kI, w, _rows())
+    # every row: the k lowest positions the sample does not read, in order
+    pos = torch.arange(S)
+    expect = pos[pos % 32 != 0][:TOPK].to(torch.int32)
+    assert torch.equal(idx[0], expect.expand(T, TOPK))
+
+
+@pytest.mark.parametrize("qk", ["e4m3", "bf16"])
+def test_sampled_keys_alone_high_redo_every_unit(cuda_lib, qk):
+    qI, kI, w = _contrast(qk, 4.0, 1.0, 43)
+    idx = _check(cuda_lib, qI, kI, w, _rows())
+    for t in (0, T // 2, T - 1):
+        p = S - T + t
+        n_high = p // 32 + 1
+        assert n_high < TOPK
+        row = idx[0, t]
+        assert torch.all(row[:n_high] % 32 == 0) and torch.all(row[n_high:] % 32 != 0)
+        assert torch.equal(row[:n_high], torch.arange(0, 32 * n_high, 32, dtype=torch.int32))
+
+
+def test_units_mixing_redone_and_complete_rows(cuda_lib):
+    # rows 4u + 2 and 4u + 3 score every key 0 (a negated query through the ReLU): ties,
+    # every key admitted; rows 4u and 4u + 1 come short and send their unit to the third
+    # launch, which must reproduce its complete rows exactly
+    neg = [t for t in range(T) if t % 4 >= 2]
+    qI, kI, w = _contrast("e4m3", 4.0, 1.0, 47, negative_rows=neg)
+    idx = _check(cuda_lib, qI, kI, w, _rows())
+    ties = torch.arange(TOPK, dtype=torch.int32)
+    for t in (2, 3, 322, T - 1):
+        assert torch.equal(idx[0, t], ties)
+
+
+@pytest.mark.parametrize("qk", ["e4m3", "bf16"])
+def test_all_scores_equal(cuda_lib, qk):
+    qI = draw((1, T, H, D), "int8", qk, 51, "cuda", D)
+    kI = draw((1, S, D), "int8", qk, 52, "cuda", D)
+    w = torch.zeros((1, T, H), dtype=torch.bfloat16, device="cuda")
+    idx = _check(cuda_lib, qI, kI, w, _rows())
+    assert torch.equal(idx[0], torch.arange(TOPK, dtype=torch.int32).expand(T, TOPK))
+
+
+@pytest.mark.parametrize("qk", ["e4m3", "bf16"])
+def test_random_integer_rows(cuda_lib, qk):
+    # the common path: thresholds that hold, rows of 59k to 60k keys
+    qI = draw((1, T, H, D), "int8", qk, 61, "cuda", D)
+    kI = draw((1, S, D), "int8", qk, 62, "cuda", D)
+    w = draw((1, T, H), "pow2", "bf16", 63, "cuda", D)
+    _check(cuda_lib, qI, kI, w, _rows())
+
+
+def test_full_size_prefill_integer_exact(cuda_lib):
+    # L = 131072 in one call, the benchmark's launch configuration; rows across the range,
+    # the longest last
+    L = 131072
+    qI = draw((1, L, H, D), "int8", "e4m3", 971, "cuda", D)
+    kI = draw((1, L, D), "int8", "e4m3", 972, "cuda", D)
+    w = draw((1, L, H), "pow2", "bf16", 973, "cuda", D)
+    idx, sc = cuda_lib.indexer_topk(qI, kI, w, TOPK, want_score=True)
+    cuda_lib.device_status()
+    rows = sorted({0, 1, 2047, 2048, 3839, 3840, 3841, 5000, 65535, 65536, 100001, L - 4,
+                   L - 3, L - 2, L - 1})
+    check_indexer(qI.cpu(), kI.cpu(), w.cpu(), TOPK, idx.cpu(), sc.cpu(), rows=np.array(rows),
+                  exact=True)

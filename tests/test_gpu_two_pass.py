@@ -1,5 +1,6 @@
-"""GPU parity of the two-pass tensor-core indexer (stored scores, then one block per row)
-on inputs that drive its row selection off the common path, against the oracle:
+"""GPU parity of the two-pass tensor-core indexer (tsi_indexer_topk_two_pass: stored scores,
+then one block per row) on inputs that drive its row selection off the common path, against
+the oracle:
 
 - the keys the row sample reads score low and all others high: the sampled threshold then
   admits far more keys than the row buffer holds, so the row is streamed again through
@@ -27,7 +28,7 @@ TORCH = {"e4m3": torch.float8_e4m3fn, "bf16": torch.bfloat16}
 
 
 def _check(cuda_lib, qI, kI, w, topk, rows=None):
-    idx, sc = cuda_lib.indexer_topk(qI, kI, w, topk, want_score=True)
+    idx, sc = cuda_lib.indexer_topk(qI, kI, w, topk, want_score=True, two_pass=True)
     cuda_lib.device_status()
     check_indexer(qI.cpu(), kI.cpu(), w.cpu(), topk, idx.cpu(), sc.cpu(), rows=rows, exact=True)
     return idx.cpu(), sc.cpu()
@@ -92,7 +93,7 @@ def test_ragged_sequences_sampled_rows(cuda_lib, qk):
     kI = draw((B, S, D), "int8", qk, 32, "cuda", D)
     w = draw((B, T, H), "pow2", "bf16", 33, "cuda", D)
     kv = torch.tensor([30000, 12345, 4000], dtype=torch.int32, device="cuda")
-    idx, sc = cuda_lib.indexer_topk(qI, kI, w, topk, kv_len=kv, want_score=True)
+    idx, sc = cuda_lib.indexer_topk(qI, kI, w, topk, kv_len=kv, want_score=True, two_pass=True)
     cuda_lib.device_status()
     rows = sorted({0, T - 1, T, 2 * T - 1, 2 * T, 3 * T - 1} | set(range(5, B * T, 23)))
     check_indexer(qI.cpu(), kI.cpu(), w.cpu(), topk, idx.cpu(), sc.cpu(), kv_len=kv.cpu(),

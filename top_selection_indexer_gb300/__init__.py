@@ -22,7 +22,8 @@ F32, BF16, E4M3 = 0, 1, 2
 MAX_TOPK = 2048
 
 EXPORTS = ("tsi_indexer_topk_workspace", "tsi_indexer_topk", "tsi_indexer_topk_onchip_workspace",
-           "tsi_indexer_topk_onchip", "tsi_sparse_attn_workspace",
+           "tsi_indexer_topk_onchip", "tsi_indexer_topk_two_pass_workspace",
+           "tsi_indexer_topk_two_pass", "tsi_sparse_attn_workspace",
            "tsi_sparse_attn_group", "tsi_device_status", "tsi_last_error", "tsi_version",
            "tsi_launch_count", "tsi_indexer_topk_noalloc", "tsi_indexer_topk_noalloc_limit",
            "tsi_indexer_topk_path", "tsi_sparse_attn_path", "tsi_index_share_layers",
@@ -56,6 +57,10 @@ def load():
             lib.tsi_indexer_topk_onchip_workspace.restype = sz
             lib.tsi_indexer_topk_onchip.argtypes = lib.tsi_indexer_topk.argtypes
             lib.tsi_indexer_topk_onchip.restype = i32
+            lib.tsi_indexer_topk_two_pass_workspace.argtypes = [i32] * 7
+            lib.tsi_indexer_topk_two_pass_workspace.restype = sz
+            lib.tsi_indexer_topk_two_pass.argtypes = lib.tsi_indexer_topk.argtypes
+            lib.tsi_indexer_topk_two_pass.restype = i32
             lib.tsi_sparse_attn_workspace.argtypes = [i32] * 8
             lib.tsi_sparse_attn_workspace.restype = sz
             lib.tsi_sparse_attn_group.argtypes = [i32, vp, vp, vp, i32, i32, i32, i32, i32, i32,
@@ -154,16 +159,20 @@ def _stream_handle(stream):
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
-def indexer_topk_workspace(B, T, S, H_I, d_I, topk, qk_dtype, onchip=False) -> int:
+def indexer_topk_workspace(B, T, S, H_I, d_I, topk, qk_dtype, onchip=False,
+                           two_pass=False) -> int:
     lib = load()
-    fn = lib.tsi_indexer_topk_onchip_workspace if onchip else lib.tsi_indexer_topk_workspace
+    fn = lib.tsi_indexer_topk_two_pass_workspace if two_pass else \
+        lib.tsi_indexer_topk_onchip_workspace if onchip else lib.tsi_indexer_topk_workspace
     return fn(B, T, S, H_I, d_I, topk, qk_dtype)
 
 
 def indexer_topk(qI, kI, w, topk, kv_len=None, idx=None, score=None, workspace=None,
-                 stream=None, want_score=False, onchip=False):
-    """Top-k key positions of the lightning-indexer score (``tsi_indexer_topk``, or
-    ``tsi_indexer_topk_onchip`` with ``onchip``: the same results, no score stored).
+                 stream=None, want_score=False, onchip=False, two_pass=False):
+    """Top-k key positions of the lightning-indexer score (``tsi_indexer_topk``: no score
+    leaves the scoring kernel; ``onchip`` calls ``tsi_indexer_topk_onchip``, the same;
+    ``two_pass`` calls ``tsi_indexer_topk_two_pass``: the same results from scores stored
+    for a second, selecting kernel).
 
     qI [B,T,H_I,d_I], kI [B,S,d_I] (f32/bf16/e4m3), w [B,T,H_I] (f32/bf16),
     kv_len [B] int32 or None.  Returns idx [B,T,topk] int32 (and score float32
@@ -180,12 +189,14 @@ def indexer_topk(qI, kI, w, topk, kv_len=None, idx=None, score=None, workspace=N
     code = _dtype_code(qI)
     if _dtype_code(kI) != code:
         raise TypeError("qI and kI must share a dtype")
-    need = indexer_topk_workspace(B, T, S, H_I, d_I, topk, code, onchip)
+    need = indexer_topk_workspace(B, T, S, H_I, d_I, topk, code, onchip, two_pass)
     if workspace is None and need:
         workspace = torch.empty(need, dtype=torch.uint8, device=qI.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     lib = load()
-    _check((lib.tsi_indexer_topk_onchip if onchip else lib.tsi_indexer_topk)(
+    fn = lib.tsi_indexer_topk_two_pass if two_pass else \
+        lib.tsi_indexer_topk_onchip if onchip else lib.tsi_indexer_topk
+    _check(fn(
         _dev(qI, "qI"), _dev(kI, "kI"), _dev(w, "w"), code, _dtype_code(w), B, T, S, H_I, d_I,
         topk, _dev(kv_len, "kv_len"), _dev(idx, "idx"), _dev(score, "score"),
         _dev(workspace, "workspace"), ws_bytes, _stream_handle(stream)))

@@ -25,9 +25,10 @@ struct IndexerArgs {
     // counts [B*T] instead of rank-ordered idx / score.
     uint64_t* out_cand = nullptr;
     int* out_cnt = nullptr;
-    // Tensor-core path with several query rows per sequence: select inside the scoring
-    // kernel (no score reaches HBM) instead of storing the scores for a second pass.
-    bool onchip = false;
+    // Tensor-core path with several query rows per sequence: store every score for a
+    // second, selecting pass instead of selecting inside the scoring kernel (the default,
+    // where no score reaches HBM).
+    bool two_pass = false;
 };
 
 // CUDA-core path (any supported shape).

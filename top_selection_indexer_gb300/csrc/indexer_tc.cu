@@ -2,34 +2,43 @@
 //
 // I[t,s] = sum_j w[t,j] * ReLU(qI[t,j] . kI[s]) for s <= p_t, then the top-k keys of
 // each row ("GLM-5.2 技术报告速览", §IndexShare: the score equation, k = 2048; the
-// ReLU form is chosen there for speed and FP8 friendliness).  Two variants of one kernel:
-//   - store (the default for several query rows per sequence): every causal score goes
-//     to a row-major fp32 buffer, a chunk of query rows at a time; topk_rows.cu then
-//     selects and ranks each row's k best keys from it.  The selection thus never stalls
-//     the MMA pipeline, at 4 B of HBM writes per causal pair.
-//   - select (one query row per sequence, and any launch asked to keep its scores on
-//     chip): each 128-key tile is scored in TMEM and streamed into a shared-memory top-k
-//     selector per query row, so no score reaches HBM; each row (or key chunk) leaves its
-//     k best keys unordered, for the ranking or merge kernels.
+// ReLU form is chosen there for speed and FP8 friendliness).  One kernel, two modes:
+//   - select (the default): each 128-key tile is scored in TMEM and streamed into a
+//     shared-memory top-k selector per query row, so no score reaches HBM; each row (or
+//     key chunk) leaves its k best keys unordered, for the ranking or merge kernels.  With
+//     several query rows per sequence the call runs it three times:
+//       1. on a strided sample of the keys (every 32nd, gathered into the workspace) with a
+//          small k' per row: the k'-th largest sampled score becomes the row's admission
+//          threshold, about c k keys of the row lie above it;
+//       2. on all keys, admitting only scores at or above that threshold: about c k appends
+//          per row instead of the ~k ln(L / k) of a selector that starts from nothing, so
+//          its buffer rarely fills and the epilogue almost never stops to compact;
+//       3. on the units where some row ended with fewer than k keys admitted (the sample
+//          misjudged it), from no threshold at all: the result is exact for any input.
+//   - store (the two-pass alternative): every causal score goes to a row-major fp32 buffer,
+//     a chunk of query rows at a time; topk_rows.cu then selects and ranks each row's k
+//     best keys from it, at 4 B of HBM writes and reads per causal pair.
 //
 // MMA shape: keys on M (128 rows of kI per tile, the A operand), the 64 heads of R
 // consecutive query rows on N = 64 R (the B operand), d_I = 128 on K, fp32 accumulators
 // in TMEM.  R = 4 for e4m3 (N = 256), 2 for bf16 (N = 128), 1 for decode.  The larger R,
 // the more query rows share each key tile: fewer tiles, MMA issues and barrier round
-// trips, less L2 traffic.  An epilogue warp reads its 32 TMEM lanes (keys) in the
-// 16x256b shape (see tile_score): each thread sums 16 heads of two keys, four threads
-// combine their sums with two shuffles.
+// trips, less L2 traffic.  An epilogue thread owns one key (TMEM lane, 32x32b shape) and
+// reads that key's 64 head columns of its row in four loads of 16: the gate weights of the
+// whole row stay in its registers for the unit, and the head sum needs no other thread.
 //
 // Roles of one persistent CTA (576 threads):
 //   warp 0       TMA producer: Q tile of the unit, key tiles into a ring of stages
-//   warp 1       TMEM allocator + single-thread MMA issuer (512 TMEM columns: 512 / N
-//                accumulators, so the MMA runs that many tiles ahead)
+//   warps 1, 18  MMA issuers, one thread each: warp 1 the even tiles, warp 18 the odd ones
+//                (512 TMEM columns: 512 / N accumulators, so the MMA runs that many tiles
+//                ahead; two issuers overlap each other's barrier waits).  Warp 1 also
+//                allocates TMEM.
 //   warps 2..17  R epilogue groups of 16 / R warps, one per query row of the unit; group
 //                r reads columns [64r, 64r+64) of an accumulator (and, selecting, owns a
 //                selector).  With 16 / R > 4 warps per row, the row's warp sets share out
 //                the tiles.
 // Units (R consecutive query rows x one key range) are visited longest first and spread
-// round-robin over the CTAs.
+// round-robin over the CTAs (or taken from a list of units, for the third launch).
 #include <mutex>
 
 #include <cudaTypedefs.h>
@@ -43,7 +52,8 @@ namespace {
 
 constexpr int kTileKeys = 128;  // MMA M
 constexpr int kEpiWarps = 16;
-constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr int kMmaWarp2 = 2 + kEpiWarps;  // the second MMA issuer (odd tiles)
+constexpr int kThreads = 96 + 32 * kEpiWarps;
 constexpr int kTmemCols = 512;
 constexpr int kChunkBytes = 128 * 128;  // one 128-row x 128-byte swizzled tile
 constexpr int kAllBar = 8;  // named barrier of all epilogue warps (selectors use 1..4)
@@ -53,32 +63,42 @@ struct TileCfg;
 template <>
 struct TileCfg<TSI_E4M3> {
     static constexpr int kRows = 4;    // query rows per unit
-    static constexpr int kCap = 3584;  // selector capacity per row (on-chip selection)
+    static constexpr int kCap = 4352;  // selector capacity per row (several rows per unit)
     static constexpr int kChunks = 1;  // 128-byte pieces of a d_I = 128 row
     static constexpr int kStages = 4;
+    static constexpr int kSelStages = 3;  // key stages beside R selectors
     static constexpr uint32_t kFmt = 0;
     static constexpr int kKSteps = 4;  // K = 32 per MMA
 };
 template <>
 struct TileCfg<TSI_BF16> {
     static constexpr int kRows = 2;
-    static constexpr int kCap = 4096;
+    static constexpr int kCap = 5888;
     static constexpr int kChunks = 2;
     static constexpr int kStages = 3;
+    static constexpr int kSelStages = 3;
     static constexpr uint32_t kFmt = 1;
     static constexpr int kKSteps = 4;  // per chunk, K = 16 per MMA
 };
 
+// store: scores to HBM.  select: each row's selector checks its room once per round and
+// compacts when it runs low (exact from any start).  capped: no room check at all, for
+// launches where a row's admitted keys are expected to fit (the sampled-threshold launches);
+// a row whose keys overflow the buffer is reported like a row that came short.
+enum : int { kModeStore = 0, kModeSelect = 1, kModeCapped = 2 };
+
 // R = query rows per unit: the format's default, or 1 for one query per sequence (decode),
 // where the four warp sets of the single row share out the key tiles instead of idling.
-// kStore: the epilogue stores the scores; otherwise it selects each row's top k itself.
-template <int QK, int R = TileCfg<QK>::kRows, bool kStore = false>
+// kMode: the epilogue stores the scores, or selects each row's top k itself.
+template <int QK, int R = TileCfg<QK>::kRows, int kMode = kModeSelect>
 struct Lay {
     using C = TileCfg<QK>;
+    static constexpr bool kStore = kMode == kModeStore;
     static constexpr int kR = R;
     // selector capacity: the row's warp sets offer up to 4 kGroupThreads keys between two
     // room checks (see the trigger in the epilogue), beyond the k that are kept
     static constexpr int kCap = R == 1 ? 5120 : C::kCap;
+    static constexpr int kStages = (R > 1 && !kStore) ? C::kSelStages : C::kStages;
     static constexpr int kN = 64 * kR;             // MMA N
     static constexpr int kAccBufs = kTmemCols / kN;
     static constexpr int kSubs = 4 / kR;           // warp sets per row sharing out the tiles
@@ -90,12 +110,19 @@ struct Lay {
     // the store variant keeps no selector: scores go to global memory
     static constexpr int kSelBytes = kStore ? 0 : (selector_smem_bytes<kCap>() + 15) & ~15;
     static constexpr uint32_t kIdesc = tc::instr_desc(C::kFmt, kTileKeys, kN);
-    static constexpr int kBars = 2 * C::kStages + 2 * kAccBufs + 3;
-    static constexpr int kSmem = 1024 /* alignment slack */ + C::kStages * kStageBytes +
+    static constexpr int kBars = 2 * kStages + 2 * kAccBufs + 3;
+    static constexpr int kSmem = 1024 /* alignment slack */ + kStages * kStageBytes +
                                  kQBytes + kR * kSelBytes + kBars * 8 + 16;
+    // a room check happens once per round (two tiles of each warp set); between two checks
+    // a thread's view of the count may miss the other warps' last round, and the next round
+    // adds at most 2 kGroupThreads keys
+    static constexpr int kTrigger = kCap - 4 * kGroupThreads;
     static_assert(kSmem <= 227 * 1024, "shared memory");
     static_assert(kEpiWarps == 4 * kR * kSubs, "every epilogue warp has a row");
 };
+
+// Key sample of the threshold launch: every 32nd key.
+constexpr int kSampleShift = 5;
 
 struct TcParams {
     const void* w;
@@ -113,6 +140,20 @@ struct TcParams {
     float* scores;       // store variant: row (b, t) at (b * (t_end - t_begin) + t - t_begin) * ld
     int64_t ld;
     unsigned* err;
+    // Key i of this launch sits at position i << key_shift (0: every key; kSampleShift: the
+    // threshold launch's sample, key rows gathered into a buffer of their own).
+    int key_shift;
+    // Select mode, optional: per-row admission thresholds to start from ([B * T] scores);
+    // per-row thresholds to produce instead of candidate lists (the threshold launch: the
+    // topk-th largest sampled score, -inf where every key fits the selector anyway);
+    // units whose rows came short of k keys (appended to fail_list, counted in fail_count);
+    // the units to visit (unit_list[0 .. *unit_count), instead of all n_units).
+    const float* tau_in;
+    float* tau_out;
+    int* fail_list;
+    int* fail_count;
+    const int* unit_list;
+    const int* unit_count;
 };
 
 struct Unit {
@@ -134,7 +175,7 @@ __device__ __forceinline__ Unit unit_of(const TcParams& p, int u) {
     U.t_hi = p.t_end - 1 - R * j;
     // positions relative to key 0 of this call; keys beyond the shard are not here
     const int64_t p_hi = query_position(p.kv_len, U.b, p.T, p.S_total, U.t_hi) - p.key_offset;
-    int64_t end = p_hi + 1 > 0 ? p_hi + 1 : 0;
+    int64_t end = p_hi >= 0 ? (p_hi >> p.key_shift) + 1 : 0;
     if (end > p.S) end = p.S;
     U.key_lo = static_cast<int64_t>(U.chunk) * p.chunk_keys;
     U.key_hi = U.key_lo + p.chunk_keys < end ? U.key_lo + p.chunk_keys : end;
@@ -149,83 +190,111 @@ __device__ __forceinline__ bool wait_fast(uint64_t* bar, uint32_t parity, bool p
     return probed || tc::mbar_wait(bar, parity, abort, err);
 }
 
-// 2 ReLU(x) of two accumulator words as x + |x|: exact (2x for x > 0, +0 otherwise), and an
-// add on the FMA pipe instead of a max on the half-rate ALU pipe.  The gate weights are
-// halved to match, so w/2 * (x + |x|) is exactly the product w * ReLU(x).
-__device__ __forceinline__ float2 relu2_twice(uint32_t a, uint32_t b) {
-    const float x = __uint_as_float(a), y = __uint_as_float(b);
-    return make_float2(__fadd_rn(x, fabsf(x)), __fadd_rn(y, fabsf(y)));
-}
+// Head-pair slots (of the eight in each 32-column load) whose ReLU runs on the ALU pipe as
+// a max with 0; the others run on the FMA pipe as x + |x| = 2 ReLU(x) (exact) against
+// halved gate weights.  Either way w * ReLU(x) is the same product, so the split only
+// balances the two pipes and never changes a score.
+constexpr int kAluSlots = 2;
 
 // Key lane (within the warp's 32 TMEM lanes) whose score tile_score returns to this
 // thread: lane 8 (T % 4) + T / 4 of thread T.
 __device__ __forceinline__ int scored_lane(int lane) { return 8 * (lane & 3) + (lane >> 2); }
 
-// Scores of query row r of the unit from accumulator buffer a: sum over the 64 heads of
-// w[h] * max(0, q[h].k), in packed fp32 pairs (w2 holds w / 2, see relu2_twice).
-//
-// The warp reads its 32 TMEM lanes (keys) as two 16-lane slices of the row's 64 columns
-// (16x256b shape).  Thread T then holds, for two keys, the head pairs 8m + 2c + {0, 1}
-// (c = T % 4, m = 0..7), so it needs only those 16 gate weights -- w2[m], kept in
-// registers for the whole unit instead of being re-read from shared memory for every
-// tile.  The four threads with equal T / 4 add their partial sums with two butterfly
-// shuffles (every one of them ends with the same value).  Thread T returns the score of
-// key lane scored_lane(T).  The buffer is released to the MMA once the second slice is in
-// registers.
-template <int N>
-__device__ __forceinline__ float tile_score(uint32_t tmem, int quad, int r, int a, uint64_t* tempty,
-                                            const float2 (&w2)[8]) {
-    tc::tc_fence_after();
-    const int c = threadIdx.x & 3;
-    const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + a * N + r * 64;
-    float mine = 0.f;
+// The 16 gate weights this thread needs (see tile_score), each duplicated into both halves
+// of a pair and halved where its ReLU is formed as x + |x|: slot j = 8 ch + 2 m + e holds
+// head 32 ch + 8 m + 2 (T % 4) + e.  (Halving a gate weight below 2^-125, a subnormal,
+// would drop its last bit; no gate weight is that small.)
+__device__ __forceinline__ void load_gates(float2 (&wd)[16], const void* w, int64_t row_h0,
+                                           int w_dtype, int lane) {
 #pragma unroll
-    for (int slice = 0; slice < 2; ++slice) {
-        uint32_t v[32];
-        TSI_TMEM_LD16x256_X8(taddr + (static_cast<uint32_t>(16 * slice) << 16), v);
-        tc::tmem_wait_ld();
-        if (slice == 1) {
-            tc::tc_fence_before();
-            __syncwarp();
-            if ((threadIdx.x & 31) == 0) tc::mbar_arrive(&tempty[a]);
-        }
-        // two accumulators per key for a shorter dependency chain
-        float2 a0 = make_float2(0.f, 0.f), a1 = a0, b0 = a0, b1 = a0;
-#pragma unroll
-        for (int m = 0; m < 8; m += 2) {
-            a0 = __ffma2_rn(w2[m], relu2_twice(v[4 * m + 0], v[4 * m + 1]), a0);
-            b0 = __ffma2_rn(w2[m], relu2_twice(v[4 * m + 2], v[4 * m + 3]), b0);
-            a1 = __ffma2_rn(w2[m + 1], relu2_twice(v[4 * m + 4], v[4 * m + 5]), a1);
-            b1 = __ffma2_rn(w2[m + 1], relu2_twice(v[4 * m + 6], v[4 * m + 7]), b1);
-        }
-        float sa = (a0.x + a0.y) + (a1.x + a1.y);  // key lane 16 slice + T / 4
-        float sb = (b0.x + b0.y) + (b1.x + b1.y);  // key lane 16 slice + 8 + T / 4
-        sa += __shfl_xor_sync(0xFFFFFFFFu, sa, 1);
-        sb += __shfl_xor_sync(0xFFFFFFFFu, sb, 1);
-        sa += __shfl_xor_sync(0xFFFFFFFFu, sa, 2);
-        sb += __shfl_xor_sync(0xFFFFFFFFu, sb, 2);
-        if (c == 2 * slice) mine = sa;
-        if (c == 2 * slice + 1) mine = sb;
+    for (int j = 0; j < 16; ++j) {
+        const int ch = j >> 3, m = (j >> 1) & 3, e = j & 1;
+        const float f = (j & 7) < kAluSlots ? 1.f : 0.5f;
+        const float g = f * load_elem(w, row_h0 + 32 * ch + 8 * m + 2 * (lane & 3) + e, w_dtype);
+        wd[j] = make_float2(g, g);
     }
-    return mine;
 }
 
-template <int QK, int R, bool kStore>
+// Scores of query row r of the unit from accumulator buffer a: the sum over the 64 heads of
+// w[h] * max(0, q[h].k).
+//
+// The warp reads its 32 TMEM lanes (keys) as two 16-lane slices, each in two loads of 32
+// columns (16x256b shape).  Thread T then holds, per slice, two keys (lanes L = T / 4 and
+// L + 8 of the slice) x 16 heads (8 m + 2 c + {0, 1} of each load, c = T % 4), so it needs
+// only those 16 gate weights, kept in registers for the whole unit.  Each packed FMA adds
+// one head of both keys, so a slice leaves one (key L, key L + 8) pair of partial sums.
+// The four threads with equal L then reduce-scatter their two pairs in two shuffle steps:
+// thread c ends with the whole sum of key lane 8 c + L (scored_lane), added in a fixed
+// order.  The buffer is released to the MMA once the last columns are in registers.
+template <int N>
+__device__ __forceinline__ float tile_score(uint32_t tmem, int quad, int r, int a, uint64_t* tempty,
+                                            const float2 (&wd)[16]) {
+    tc::tc_fence_after();
+    const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + a * N + r * 64;
+    float2 part[2];  // per slice: (key L, key L + 8) partial sums over this thread's heads
+#pragma unroll
+    for (int slice = 0; slice < 2; ++slice) {
+        float2 acc0 = make_float2(0.f, 0.f), acc1 = acc0;
+#pragma unroll
+        for (int ch = 0; ch < 2; ++ch) {
+            uint32_t v[16];
+            TSI_TMEM_LD16x256_X4(taddr + (static_cast<uint32_t>(16 * slice) << 16) + 32 * ch, v);
+            tc::tmem_wait_ld();
+            if (slice == 1 && ch == 1) {
+                tc::tc_fence_before();
+                __syncwarp();
+                if ((threadIdx.x & 31) == 0) tc::mbar_arrive(&tempty[a]);
+            }
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int j = 8 * ch + 2 * m + e;
+                    const float x = __uint_as_float(v[4 * m + e]);
+                    const float y = __uint_as_float(v[4 * m + 2 + e]);
+                    const float2 rx = (j & 7) < kAluSlots
+                                          ? make_float2(fmaxf(x, 0.f), fmaxf(y, 0.f))
+                                          : make_float2(__fadd_rn(x, fabsf(x)),
+                                                        __fadd_rn(y, fabsf(y)));
+                    if (e == 0)
+                        acc0 = __ffma2_rn(wd[j], rx, acc0);
+                    else
+                        acc1 = __ffma2_rn(wd[j], rx, acc1);
+                }
+            }
+        }
+        part[slice] = __fadd2_rn(acc0, acc1);
+    }
+    // reduce-scatter over the quad: first the slices (xor 2), then the two keys (xor 1)
+    const int c = threadIdx.x & 3;
+    const bool hi = (c >> 1) & 1;
+    const float2 send = hi ? part[0] : part[1];
+    const float2 keep = hi ? part[1] : part[0];
+    const float2 got = make_float2(__shfl_xor_sync(0xFFFFFFFFu, send.x, 2),
+                                   __shfl_xor_sync(0xFFFFFFFFu, send.y, 2));
+    const float2 t = __fadd2_rn(keep, got);
+    const bool odd = c & 1;
+    const float other = __shfl_xor_sync(0xFFFFFFFFu, odd ? t.x : t.y, 1);
+    return __fadd_rn(odd ? t.y : t.x, other);
+}
+
+template <int QK, int R, int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
     tsi_indexer_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                           const __grid_constant__ CUtensorMap tmap_q, const TcParams p) {
     using C = TileCfg<QK>;
-    using L = Lay<QK, R, kStore>;
+    using L = Lay<QK, R, kMode>;
+    constexpr bool kStore = L::kStore;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t* stages = base;
-    uint8_t* qbuf = stages + C::kStages * L::kStageBytes;
+    uint8_t* qbuf = stages + L::kStages * L::kStageBytes;
     uint8_t* sel_mem = qbuf + L::kQBytes;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sel_mem + R * L::kSelBytes);
     uint64_t* full = bars;
-    uint64_t* empty = full + C::kStages;
-    uint64_t* tfull = empty + C::kStages;
+    uint64_t* empty = full + L::kStages;
+    uint64_t* tfull = empty + L::kStages;
     uint64_t* tempty = tfull + L::kAccBufs;
     uint64_t* qfull = tempty + L::kAccBufs;
     uint64_t* qempty = qfull + 1;
@@ -237,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < C::kStages; ++s) {
+        for (int s = 0; s < L::kStages; ++s) {
             tc::mbar_init(&full[s], 1);
             tc::mbar_init(&empty[s], 1);
         }
@@ -246,8 +315,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::mbar_init(&tempty[a], L::kReaders);
         }
         tc::mbar_init(qfull, 1);
-        tc::mbar_init(qempty, 1);
-        tc::mbar_init(done, 1);
+        tc::mbar_init(qempty, 2);  // both MMA issuers
+        tc::mbar_init(done, 2);
         *abort = 0;
         tc::fence_barrier_init();
     }
@@ -260,6 +329,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // units of this launch: all of them, or those listed by an earlier launch
+    const int n_units = p.unit_list ? *reinterpret_cast<const volatile int*>(p.unit_count)
+                                    : p.n_units;
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
@@ -269,8 +341,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             int unit_it = 0;
             int q_last = -1;  // unit of the last query load issued
             uint32_t loaded = 0, last_ph = 0;  // per slot (bit s): loaded once, last phase
-            for (int u = blockIdx.x; u < p.n_units; u += gridDim.x, ++unit_it) {
-                const Unit U = unit_of<R>(p, u);
+            for (int j = blockIdx.x; j < n_units; j += gridDim.x, ++unit_it) {
+                const Unit U = unit_of<R>(p, p.unit_list ? p.unit_list[j] : j);
                 tc::mbar_wait(qempty, (unit_it & 1) ^ 1, abort, p.err);
                 if (!*abort) {
                     q_last = unit_it;
@@ -293,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             tc::tma_load_2d(stages + s * L::kStageBytes + c * kChunkBytes, &tmap_k,
                                             c * 64, krow, &full[s]);
                     }
-                    if (++s == C::kStages) {
+                    if (++s == L::kStages) {
                         s = 0;
                         ph ^= 1;
                     }
@@ -302,22 +374,34 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (*abort) {  // loads still in flight must land before the CTA exits (at most
                            // one per slot: a slot is reloaded only after its data was used)
                 if (q_last >= 0) tc::mbar_drain(qfull, q_last & 1);
-                for (int i = 0; i < C::kStages; ++i)
+                for (int i = 0; i < L::kStages; ++i)
                     if ((loaded >> i) & 1u) tc::mbar_drain(&full[i], (last_ph >> i) & 1u);
             }
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
+    } else if (warp == 1 || warp == kMmaWarp2) {
+        // ------------------------------------------------------------ MMA issuers
         if (lane == 0) {
-            int s = 0, a = 0;
+            const int mine = warp == 1 ? 0 : 1;  // tiles t of the CTA with t % 2 == mine
+            int s = 0, a = 0, t = 0;
             uint32_t ph = 0, aph = 0;  // phases of ring slot s and accumulator a
             int unit_it = 0;
             const uint64_t adesc = tc::smem_desc(tc::smem_addr(stages), 16, 1024);
             const uint64_t bdesc = tc::smem_desc(tc::smem_addr(qbuf), 16, 1024);
-            for (int u = blockIdx.x; u < p.n_units; u += gridDim.x, ++unit_it) {
-                const Unit U = unit_of<R>(p, u);
+            for (int j = blockIdx.x; j < n_units; j += gridDim.x, ++unit_it) {
+                const Unit U = unit_of<R>(p, p.unit_list ? p.unit_list[j] : j);
                 tc::mbar_wait(qfull, unit_it & 1, abort, p.err);
-                for (int i = 0; i < U.ntiles; ++i) {
+                for (int i = 0; i < U.ntiles; ++i, ++t) {
+                    if ((t & 1) != mine) {  // the other issuer's tile: keep the ring counters
+                        if (++s == L::kStages) {
+                            s = 0;
+                            ph ^= 1;
+                        }
+                        if (++a == L::kAccBufs) {
+                            a = 0;
+                            aph ^= 1;
+                        }
+                        continue;
+                    }
                     // probe both barriers back to back so their latencies overlap
                     const bool f_ok = tc::mbar_try_wait(&full[s], ph);
                     const bool e_ok = tc::mbar_try_wait(&tempty[a], aph ^ 1);
@@ -344,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tc::mma_commit(&empty[s]);
                     tc::mma_commit(&tfull[a]);
-                    if (++s == C::kStages) {
+                    if (++s == L::kStages) {
                         s = 0;
                         ph ^= 1;
                     }
@@ -355,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc::mma_commit(qempty);
             }
-            // every MMA issued by this thread has finished before TMEM is released
+            // every MMA issued by both threads has finished before TMEM is released
             tc::mma_commit(done);
             if (!tc::mbar_wait(done, 0, abort, p.err)) tc::mbar_drain(done, 0);
         }
@@ -369,89 +453,126 @@ __global__ void __launch_bounds__(kThreads, 1)
         TopKSelector<L::kGroupThreads, L::kCap> sel;
         if (!kStore) sel.bind(sel_mem + r * L::kSelBytes, gtid, 1 + r, p.err);
         int acc_base = 0;  // accumulator counter of the unit's first tile
-        for (int u = blockIdx.x; u < p.n_units; u += gridDim.x) {
+        for (int j = blockIdx.x; j < n_units; j += gridDim.x) {
+            const int u = p.unit_list ? p.unit_list[j] : j;
             const Unit U = unit_of<R>(p, u);
             const int t = U.t_hi - (R - 1) + r;
             const bool row_ok = t >= p.t_begin;
+            const int64_t row = static_cast<int64_t>(U.b) * p.T + t;
             int64_t limit = 0;  // keys s < limit belong to this row
-            float2 w2[8];
+            int64_t n_row = 0;  // keys of the row in the whole call (before key chunks)
+            float2 wd[16];  // this thread's 16 gate weights of the row (see load_gates)
 #pragma unroll
-            for (int m = 0; m < 8; ++m) w2[m] = make_float2(0.f, 0.f);
+            for (int m = 0; m < 16; ++m) wd[m] = make_float2(0.f, 0.f);
             if (row_ok) {
                 const int64_t pr = query_position(p.kv_len, U.b, p.T, p.S_total, t) - p.key_offset;
-                limit = pr + 1 < U.key_hi ? pr + 1 : U.key_hi;
-                const int64_t wrow = (static_cast<int64_t>(U.b) * p.T + t) * 64;
-                // this thread's 16 gate weights, halved (see tile_score, relu2_twice)
-#pragma unroll
-                for (int m = 0; m < 8; ++m) {
-                    const int64_t h = wrow + 8 * m + 2 * (lane & 3);
-                    w2[m] = make_float2(0.5f * load_elem(p.w, h, p.w_dtype),
-                                        0.5f * load_elem(p.w, h + 1, p.w_dtype));
-                }
+                n_row = pr >= 0 ? (pr >> p.key_shift) + 1 : 0;
+                if (n_row > p.S) n_row = p.S;
+                limit = n_row < U.key_hi ? n_row : U.key_hi;
+                load_gates(wd, p.w, row * 64, p.w_dtype, lane);
             }
-            // key of this thread's score in a tile: off; whole-cache position of key 0
+            // key of this thread's score in a tile
             const int off = quad * 32 + scored_lane(lane);
             if constexpr (kStore) {
                 // every tile of the row: its scores to the row's stored scores (a warp writes
                 // 32 consecutive keys, one 128-byte line); the selection runs afterwards
-                float* srow = p.scores + (static_cast<int64_t>(U.b) * (p.t_end - p.t_begin) +
-                                          (t - p.t_begin)) * p.ld;
+                float* srow_t = p.scores + (static_cast<int64_t>(U.b) * (p.t_end - p.t_begin) +
+                                            (t - p.t_begin)) * p.ld + U.key_lo + off;
+                const int64_t rest64 = limit - U.key_lo - off;
+                const int rest = rest64 < 0 ? 0 : rest64 > (1 << 30) ? (1 << 30)
+                                                                     : static_cast<int>(rest64);
                 for (int i = sub; i < U.ntiles; i += L::kSubs) {
                     const int acc = acc_base + i;
                     const int a = acc % L::kAccBufs;
-                    tc::mbar_wait(&tfull[a], (acc / L::kAccBufs) & 1, abort, p.err);
-                    const float sc = tile_score<L::kN>(tmem, quad, r, a, tempty, w2);
-                    const int64_t key = U.key_lo + static_cast<int64_t>(i) * kTileKeys + off;
-                    if (key < limit) srow[key] = sc;
+                    tc::mbar_wait_ready(&tfull[a], (acc / L::kAccBufs) & 1, abort, p.err);
+                    const float sc = tile_score<L::kN>(tmem, quad, r, a, tempty, wd);
+                    if (i * kTileKeys < rest) srow_t[i * kTileKeys] = sc;
                 }
                 acc_base += U.ntiles;
                 continue;
             }
-            // per round each warp scores two of its tiles, then one room check covers the
-            // group's offers of both
-            sel.reset();
-            const uint32_t pos0 = static_cast<uint32_t>(U.key_lo + p.key_offset);
+            // Start from the row's admission threshold (its keys with a score at or above
+            // tau), or from nothing.
+            float tau = -__int_as_float(0x7f800000);
+            if (p.tau_in && row_ok) tau = p.tau_in[row];
+            const bool has_tau = tau > -__int_as_float(0x7f800000);
+            sel.reset(has_tau ? static_cast<uint64_t>(score_order_bits(tau)) << 32 : 0ull);
+            const uint32_t pos0 = static_cast<uint32_t>(U.key_lo + p.key_offset) + off;
+            // keys of the row at or after this thread's key of tile 0 (tile i holds it at
+            // 128 i): tile i's key belongs to the row when 128 i < rest
+            int64_t rest64 = limit - U.key_lo - off;
+            const int rest = rest64 < 0 ? 0 : rest64 > (1 << 30) ? (1 << 30) : static_cast<int>(rest64);
+            // per round each warp scores two of its tiles and offers both keys at once
             for (int i0 = 0; i0 < U.ntiles; i0 += 2 * L::kSubs) {
-                float sc[2];
-                int rem[2];  // keys of tile i that belong to this row (0..128)
+                const int ia = i0 + sub, ib = i0 + L::kSubs + sub;
+                float sc[2] = {0.f, 0.f};
 #pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const int i = i0 + j * L::kSubs + sub;
-                    const int64_t left = limit - (U.key_lo + static_cast<int64_t>(i) * kTileKeys);
-                    rem[j] = left <= 0 ? 0 : left >= kTileKeys ? kTileKeys : static_cast<int>(left);
-                    sc[j] = 0.f;
+                for (int jj = 0; jj < 2; ++jj) {
+                    const int i = jj ? ib : ia;
                     if (i < U.ntiles) {
                         const int acc = acc_base + i;
                         const int a = acc % L::kAccBufs;
-                        tc::mbar_wait(&tfull[a], (acc / L::kAccBufs) & 1, abort, p.err);
-                        sc[j] = tile_score<L::kN>(tmem, quad, r, a, tempty, w2);
+                        tc::mbar_wait_ready(&tfull[a], (acc / L::kAccBufs) & 1, abort, p.err);
+                        sc[jj] = tile_score<L::kN>(tmem, quad, r, a, tempty, wd);
                     }
                 }
-                // Room for the round's offers.  All epilogue warps meet here (they wait for
-                // the same accumulators anyway): when some row is about to fill, every row
-                // past half full compacts in the same stall of the MMA pipeline instead of
-                // each stalling it on its own.
-                // One barrier: each thread's count may miss the other warps' offers of the
-                // last round (at most 2 NT keys), and this round adds at most 2 NT more, so
-                // the trigger leaves 4 NT of room.  The rows then settle their exact counts.
-                constexpr int kTrigger = L::kCap - 4 * L::kGroupThreads;
-                if (tc::bar_red_or(kAllBar, 32 * kEpiWarps, sel.count() > kTrigger)) {
-                    const int held = sel.settled_count();
-                    if (held > (p.topk + kTrigger) / 2)
-                        sel.compact(p.topk, held, false, (kTrigger - p.topk) / 4);
+                const bool ok_a = ia * kTileKeys < rest, ok_b = ib * kTileKeys < rest;
+                const uint32_t pa = pos0 + static_cast<uint32_t>(ia * kTileKeys);
+                const uint32_t pb = pos0 + static_cast<uint32_t>(ib * kTileKeys);
+                if constexpr (kMode == kModeCapped) {
+                    sel.offer2_capped(ok_a, sc[0], pa, ok_b, sc[1], pb, tau);
+                } else {
+                    // Room for the round's offers: the row's warps meet once per round.  Each
+                    // thread's count may miss the other warps' offers of the last round (at
+                    // most 2 NT keys), and this round adds at most 2 NT more, so the trigger
+                    // leaves 4 NT of room.  The row then settles its exact count and compacts.
+                    if (tc::bar_red_or(1 + r, L::kGroupThreads, sel.count() > L::kTrigger)) {
+                        const int held = sel.settled_count();
+                        if (held > L::kTrigger)
+                            sel.compact(p.topk, held, false, (L::kTrigger - p.topk) / 4);
+                    }
+                    const uint64_t thr = *reinterpret_cast<volatile uint64_t*>(sel.thr);
+                    sel.offer2_scored(ok_a, sc[0], pa, ok_b, sc[1], pb, thr, score_floor(thr));
                 }
-                const uint64_t thr = *reinterpret_cast<volatile uint64_t*>(sel.thr);
-                const uint32_t i_a = static_cast<uint32_t>((i0 + sub) * kTileKeys + off);
-                const uint32_t i_b = static_cast<uint32_t>((i0 + L::kSubs + sub) * kTileKeys + off);
-                sel.offer2_scored(off < rem[0], sc[0], pos0 + i_a, off < rem[1], sc[1], pos0 + i_b,
-                                  thr, score_floor(thr));
             }
             acc_base += U.ntiles;
+            bool short_row = false;
             if (row_ok) {
-                // the row's (chunk's) k best keys, unordered; the merge kernel ranks them
-                const int64_t row = static_cast<int64_t>(U.b) * p.T + t;
-                const int64_t slot = row * p.n_chunks + U.chunk;
-                sel.dump(p.topk, p.cand + slot * p.topk, p.cand_cnt + slot);
+                const int held = sel.settled_count();
+                const bool lost = held > L::kCap;  // capped: keys past the buffer were dropped
+                if (p.tau_out) {
+                    // Threshold launch: the topk-th largest sampled score bounds the row's
+                    // admission in the full launch (at least topk of its keys reach it).  A row
+                    // whose keys all fit the selector starts from nothing instead, and so does
+                    // one whose sample did not fit (its full launch then overflows and the
+                    // unit is redone from no threshold).
+                    float out = -__int_as_float(0x7f800000);
+                    const int64_t n_full = n_row << p.key_shift;  // upper bound of the row's keys
+                    if (!lost && held > p.topk && n_full > L::kCap) {
+                        sel.compact(p.topk, held, true, 0, false);
+                        out = score_floor(*reinterpret_cast<volatile uint64_t*>(sel.thr));
+                    }
+                    if (gtid == 0) p.tau_out[row] = out;
+                    sel.sync();
+                } else {
+                    // Admission from a threshold may leave a row with fewer than k keys (fewer
+                    // than min(k, its keys) at or above the threshold), or, capped, with more
+                    // than the buffer holds: such a unit is done again from nothing by a later
+                    // launch; its lists are not written here.
+                    int64_t n_here = limit - U.key_lo;
+                    if (n_here < 0) n_here = 0;
+                    const int need = n_here < p.topk ? static_cast<int>(n_here) : p.topk;
+                    short_row = lost || (has_tau && held < need);
+                    if (!short_row) {
+                        // the row's (chunk's) k best keys, unordered; the merge kernel ranks them
+                        const int64_t slot = row * p.n_chunks + U.chunk;
+                        sel.dump(p.topk, p.cand + slot * p.topk, p.cand_cnt + slot);
+                    }
+                }
+            }
+            if (p.fail_list) {  // one barrier per unit: record it if any row came short
+                if (tc::bar_red_or(kAllBar, 32 * kEpiWarps, short_row) && ew == 0 && lane == 0)
+                    p.fail_list[atomicAdd(p.fail_count, 1)] = u;
             }
         }
     }
@@ -561,9 +682,81 @@ size_t cand_bytes(int B, int T, int topk, int n_chunks) {
            ((slots * sizeof(int) + 255) & ~size_t(255));
 }
 
-template <int QK, int R, bool kStore>
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Selection from a sampled threshold: with several query rows per unit and one key range
+// per row (no key chunks), the three select launches (see the top of the file) apply.
+bool sampled_plan(int qk_dtype, int B, int T, int S) {
+    if (rows_per_unit(qk_dtype, T) == 1) return false;
+    int nc, ck;
+    tc_plan(qk_dtype, B, T, S, &nc, &ck);
+    return nc == 1;
+}
+
+int sample_keys(int S) { return (S + (1 << kSampleShift) - 1) >> kSampleShift; }
+
+int64_t n_units_of(int qk_dtype, int B, int T) {
+    const int R = rows_per_unit(qk_dtype, T);
+    return static_cast<int64_t>(B) * ((T + R - 1) / R);
+}
+
+// Workspace of the sampled-threshold selection after the candidate lists: per-row
+// thresholds, the short-unit count and list, the gathered key sample.
+struct SampledWs {
+    float* tau;
+    int* fail_count;
+    int* fail_list;
+    uint8_t* keys;
+    size_t bytes;
+};
+
+SampledWs sampled_ws(uint8_t* base, int qk_dtype, int B, int T, int S) {
+    SampledWs w{};
+    const size_t rows = static_cast<size_t>(B) * T;
+    size_t off = 0;
+    w.tau = reinterpret_cast<float*>(base + off);
+    off = align_up(off + rows * 4, 256);
+    w.fail_count = reinterpret_cast<int*>(base + off);
+    off += 256;
+    w.fail_list = reinterpret_cast<int*>(base + off);
+    off = align_up(off + static_cast<size_t>(n_units_of(qk_dtype, B, T)) * 4, 1024);
+    w.keys = base + off;
+    off += align_up(static_cast<size_t>(B) * sample_keys(S) * (qk_dtype == TSI_BF16 ? 256 : 128),
+                    1024);
+    w.bytes = off;
+    return w;
+}
+
+// Every 32nd key row (row bytes = 128 or 256) of each sequence into a buffer of its own,
+// [B][ceil(S / 32)] rows; thread 0 also clears the short-unit count of the call.
+__global__ void sample_keys_kernel(const uint4* __restrict__ kI, uint4* __restrict__ out, int B,
+                                   int S, int S_s, int row_vec, int* fail_count) {
+    const int64_t n = static_cast<int64_t>(B) * S_s * row_vec;
+    const int64_t i0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i0 == 0) *fail_count = 0;
+    for (int64_t i = i0; i < n; i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t v = i % row_vec;
+        const int64_t rs = i / row_vec;  // sampled row of the whole buffer
+        const int64_t b = rs / S_s;
+        const int64_t key = (rs - b * S_s) << kSampleShift;
+        out[i] = kI[(b * S + key) * row_vec + v];
+    }
+}
+
+// Target of the threshold launch: the row's ceil(c k / 32)-th largest sampled score, so that
+// about c k keys of the row reach it.  c = 1.55: with 100 sampled keys above it for k = 2048
+// the count of admitted keys varies by ~10% (the fraction of keys above the m-th of n
+// sampled is Beta(m, n - m + 1)), so fewer than k (-3.5 sigma) or more than the 4352-key
+// buffer (+3.7 sigma) happens to a few rows in 10^4; their units are redone exactly.
+int sample_topk(int topk) {
+    const int m = (155 * topk + 100 * (1 << kSampleShift) - 1) / (100 * (1 << kSampleShift));
+    return m < 1 ? 1 : m;
+}
+
+template <int QK, int R, int kMode>
 cudaError_t launch_qk(const IndexerArgs& a, void* workspace, cudaStream_t st) {
-    using L = Lay<QK, R, kStore>;
+    using L = Lay<QK, R, kMode>;
+    constexpr bool kStore = L::kStore;
     CUtensorMap tk, tq;
     // the query box is one unit's rows (64 per query row), at most 128 per copy
     if (!encode_rows128(&tk, a.kI, static_cast<int64_t>(a.B) * a.S, QK) ||
@@ -599,12 +792,70 @@ cudaError_t launch_qk(const IndexerArgs& a, void* workspace, cudaStream_t st) {
         ws += cand_bytes(a.B, a.T, a.topk, lists);
     }
     constexpr int smem = L::kSmem;
-    cudaError_t e = cudaFuncSetAttribute(tsi_indexer_tc_kernel<QK, R, kStore>,
+    cudaError_t e = cudaFuncSetAttribute(tsi_indexer_tc_kernel<QK, R, kMode>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
+    // the sampled-threshold launches run the capped form of the select kernel
+    constexpr int kCapMode = kMode == kModeSelect ? kModeCapped : kMode;
+    static_assert(Lay<QK, R, kCapMode>::kSmem == smem, "one layout for both select forms");
+    if constexpr (kMode == kModeSelect && R > 1) {
+        e = cudaFuncSetAttribute(tsi_indexer_tc_kernel<QK, R, kCapMode>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+    }
     const int chunk_rows = kStore ? score_chunk_rows(QK, a.B, a.T, a.S) : a.T;
     p.scores = kStore ? reinterpret_cast<float*>(ws) : nullptr;
     p.ld = score_ld(a.S);
+    if constexpr (!kStore && R > 1) if (lists == 1) {
+        // ---- selection from a sampled threshold: sample, threshold, full, short units
+        const SampledWs sw = sampled_ws(ws, QK, a.B, a.T, a.S);
+        const int S_s = sample_keys(a.S);
+        const int row_vec = QK == TSI_BF16 ? 16 : 8;
+        const int64_t n_vec = static_cast<int64_t>(a.B) * S_s * row_vec;
+        int blocks = static_cast<int>((n_vec + 255) / 256);
+        if (blocks > 4 * sm_count()) blocks = 4 * sm_count();
+        if (blocks < 1) blocks = 1;
+        sample_keys_kernel<<<blocks, 256, 0, st>>>(static_cast<const uint4*>(a.kI),
+                                                     reinterpret_cast<uint4*>(sw.keys), a.B, a.S,
+                                                     S_s, row_vec, sw.fail_count);
+        note_launches(1);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        CUtensorMap ts;
+        if (!encode_rows128(&ts, sw.keys, static_cast<int64_t>(a.B) * S_s, QK))
+            return cudaErrorInvalidValue;
+        p.t_begin = 0;
+        p.t_end = a.T;
+        p.n_units = static_cast<int>(n_units_of(QK, a.B, a.T));
+        const int grid = p.n_units < sm_count() ? p.n_units : sm_count();
+        // 1. thresholds from the sample
+        TcParams ps = p;
+        ps.S = S_s;
+        ps.key_shift = kSampleShift;
+        ps.topk = sample_topk(a.topk);
+        ps.tau_out = sw.tau;
+        tsi_indexer_tc_kernel<QK, R, kCapMode><<<grid, kThreads, smem, st>>>(ts, tq, ps);
+        note_launches(1);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        // 2. every key, admitted from the thresholds; short units listed
+        TcParams pf = p;
+        pf.tau_in = sw.tau;
+        pf.fail_list = sw.fail_list;
+        pf.fail_count = sw.fail_count;
+        tsi_indexer_tc_kernel<QK, R, kCapMode><<<grid, kThreads, smem, st>>>(tk, tq, pf);
+        note_launches(1);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        // 3. the listed units again, from no threshold, with room checks (a launch whose
+        // CTAs find no unit return at once)
+        TcParams pr = p;
+        pr.unit_list = sw.fail_list;
+        pr.unit_count = sw.fail_count;
+        tsi_indexer_tc_kernel<QK, R, kMode><<<grid, kThreads, smem, st>>>(tk, tq, pr);
+        note_launches(1);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        return a.out_cand ? e
+                          : launch_topk_rank(rows, a.topk, p.cand, p.cand_cnt, a.idx, a.score,
+                                             a.err, st);
+    }
     // Launch pairs over chunks of query rows, the last rows first (each chunk's rows are
     // a multiple of R except the first rows of the sequences).
     for (int t_end = a.T; t_end > 0; t_end -= chunk_rows) {
@@ -613,7 +864,7 @@ cudaError_t launch_qk(const IndexerArgs& a, void* workspace, cudaStream_t st) {
         const int n = p.t_end - p.t_begin;
         p.n_units = static_cast<int>(static_cast<int64_t>(a.B) * ((n + R - 1) / R) * p.n_chunks);
         const int grid = p.n_units < sm_count() ? p.n_units : sm_count();
-        tsi_indexer_tc_kernel<QK, R, kStore><<<grid, kThreads, smem, st>>>(tk, tq, p);
+        tsi_indexer_tc_kernel<QK, R, kMode><<<grid, kThreads, smem, st>>>(tk, tq, p);
         note_launches(1);
         e = cudaGetLastError();
         if (e != cudaSuccess || !kStore) break;
@@ -657,35 +908,37 @@ bool tc_indexer_supported(int qk_dtype, int H_I, int d_I) {
     return (qk_dtype == TSI_BF16 || qk_dtype == TSI_E4M3) && H_I == 64 && d_I == 128;
 }
 
-size_t tc_indexer_workspace_bytes(int qk_dtype, int B, int T, int S, int topk, bool onchip) {
-    if (rows_per_unit(qk_dtype, T) > 1 && !onchip)  // two passes: the stored scores
+size_t tc_indexer_workspace_bytes(int qk_dtype, int B, int T, int S, int topk, bool two_pass) {
+    if (rows_per_unit(qk_dtype, T) > 1 && two_pass)  // two passes: the stored scores
         return score_scratch_bytes(qk_dtype, B, T, S);
     int nc, ck;
     tc_plan(qk_dtype, B, T, S, &nc, &ck);
-    return cand_bytes(B, T, topk, nc) +
-           (nc > 1 ? topk_merge_stage_bytes(B * T, topk, nc) : 0);
+    size_t n = cand_bytes(B, T, topk, nc) + (nc > 1 ? topk_merge_stage_bytes(B * T, topk, nc) : 0);
+    if (sampled_plan(qk_dtype, B, T, S)) n += sampled_ws(nullptr, qk_dtype, B, T, S).bytes;
+    return n;
 }
 
 size_t tc_indexer_split_workspace_bytes(int qk_dtype, int B, int T, int S, int topk) {
-    // the caller's lists take the candidates of a one-list-per-row launch
-    if (rows_per_unit(qk_dtype, T) > 1) return score_scratch_bytes(qk_dtype, B, T, S);
+    // the caller's lists take the candidates of a one-list-per-row launch; what remains is
+    // the sampled selection's scratch, or the chunk lists and their merge stage
     int nc, ck;
     tc_plan(qk_dtype, B, T, S, &nc, &ck);
+    if (sampled_plan(qk_dtype, B, T, S)) return sampled_ws(nullptr, qk_dtype, B, T, S).bytes;
     return nc <= 1 ? 0 : tc_indexer_workspace_bytes(qk_dtype, B, T, S, topk, false);
 }
 
 cudaError_t launch_indexer_tc(const IndexerArgs& a, void* workspace, cudaStream_t st) {
     if (a.B * a.T == 0) return cudaSuccess;
     if (rows_per_unit(a.qk_dtype, a.T) == 1)
-        return a.qk_dtype == TSI_E4M3 ? launch_qk<TSI_E4M3, 1, false>(a, workspace, st)
-                                      : launch_qk<TSI_BF16, 1, false>(a, workspace, st);
-    if (a.onchip)
+        return a.qk_dtype == TSI_E4M3 ? launch_qk<TSI_E4M3, 1, kModeSelect>(a, workspace, st)
+                                      : launch_qk<TSI_BF16, 1, kModeSelect>(a, workspace, st);
+    if (a.two_pass)
         return a.qk_dtype == TSI_E4M3
-                   ? launch_qk<TSI_E4M3, TileCfg<TSI_E4M3>::kRows, false>(a, workspace, st)
-                   : launch_qk<TSI_BF16, TileCfg<TSI_BF16>::kRows, false>(a, workspace, st);
+                   ? launch_qk<TSI_E4M3, TileCfg<TSI_E4M3>::kRows, kModeStore>(a, workspace, st)
+                   : launch_qk<TSI_BF16, TileCfg<TSI_BF16>::kRows, kModeStore>(a, workspace, st);
     return a.qk_dtype == TSI_E4M3
-               ? launch_qk<TSI_E4M3, TileCfg<TSI_E4M3>::kRows, true>(a, workspace, st)
-               : launch_qk<TSI_BF16, TileCfg<TSI_BF16>::kRows, true>(a, workspace, st);
+               ? launch_qk<TSI_E4M3, TileCfg<TSI_E4M3>::kRows, kModeSelect>(a, workspace, st)
+               : launch_qk<TSI_BF16, TileCfg<TSI_BF16>::kRows, kModeSelect>(a, workspace, st);
 }
 
 }  // namespace tsi

@@ -12,7 +12,7 @@ namespace tsi {
 // Indexer + top-k with tcgen05 MMAs (BF16 or E4M3 inputs, H_I = 64, d_I = 128).
 bool tc_indexer_supported(int qk_dtype, int H_I, int d_I);
 size_t tc_indexer_workspace_bytes(int qk_dtype, int B, int T, int S, int topk,
-                                  bool onchip = false);
+                                  bool two_pass = false);
 // Only the split (decode) candidate lists, for callers that take unordered candidates.
 size_t tc_indexer_split_workspace_bytes(int qk_dtype, int B, int T, int S, int topk);
 cudaError_t launch_indexer_tc(const IndexerArgs& a, void* workspace, cudaStream_t st);

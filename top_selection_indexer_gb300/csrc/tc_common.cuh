@@ -70,6 +70,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     return true;
 }
 
+// The same bounded wait for a phase that is usually complete already: one probe before
+// the abort flag is read (a completed phase is taken even after an abort).
+__device__ __forceinline__ bool mbar_wait_ready(uint64_t* bar, uint32_t parity,
+                                                volatile int* abort, unsigned* err) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return mbar_wait(bar, parity, abort, err);
+}
+
 // Bounded wait that ignores the abort flag: after an abort, for the asynchronous work this
 // thread has already started (MMAs, TMA loads) to finish before shared memory or TMEM is
 // given up.  Returns false if the bound runs out.
@@ -151,6 +159,19 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
           "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),        \
           "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),        \
           "=r"(r[31])                                                                           \
+        : "r"(taddr))
+
+// 16 lanes x 32 consecutive TMEM columns -> 16 registers per thread.  Thread T gets lanes
+// L = T/4 and L + 8 (of the 16 starting at the address's lane); for m = 0..3 registers
+// 4m, 4m+1 hold lane L, columns 8m + 2(T%4) + {0, 1} and registers 4m+2, 4m+3 the same
+// columns of lane L + 8.
+#define TSI_TMEM_LD16x256_X4(taddr, r)                                                           \
+    asm volatile(                                                                                \
+        "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13," \
+        "%14,%15}, [%16];"                                                                       \
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),  \
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),           \
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])                                                 \
         : "r"(taddr))
 
 // 16 lanes x 64 consecutive TMEM columns -> 32 registers per thread.  Thread T gets lanes

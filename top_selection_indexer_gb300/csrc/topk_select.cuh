@@ -91,12 +91,13 @@ struct TopKSelector {
         return *reinterpret_cast<volatile int*>(&ctl[0]);
     }
 
-    __device__ void reset() {
+    // Collective: empty the selector; keys below `threshold` are never admitted.
+    __device__ void reset(uint64_t threshold = 0ull) {
         sync();
         if (tid == 0) {
             ctl[0] = 0;
             ctl[4] = 0;
-            *thr = 0ull;
+            *thr = threshold;
             *rng = 0ull;
         }
         for (int i = tid; i < 256; i += NT) hist[i] = 0u;
@@ -220,6 +221,30 @@ struct TopKSelector {
         const bool c1 = ok1 && s1 >= floor;
         if (!__any_sync(kFull, c0 || c1)) return;
         offer2_thr(c0, make_key(s0, pos0), c1, make_key(s1, pos1), threshold);
+    }
+
+    // Warp-collective: append the keys of two scored positions per thread whose score
+    // reaches `floor` (every key of such a score is at least the threshold the selector was
+    // reset to), with no room check: slots past CAP are not written and the count runs on
+    // beyond CAP, so a caller that finds settled_count() > CAP knows keys were lost.  One
+    // shared-memory reservation per warp.
+    __device__ __forceinline__ void offer2_capped(bool ok0, float s0, uint32_t pos0, bool ok1,
+                                                  float s1, uint32_t pos1, float floor) {
+        const bool t0 = ok0 && s0 >= floor;
+        const bool t1 = ok1 && s1 >= floor;
+        const unsigned m0 = __ballot_sync(kFull, t0);
+        const unsigned m1 = __ballot_sync(kFull, t1);
+        if ((m0 | m1) == 0u) return;
+        const int lane = threadIdx.x & 31;
+        const int n0 = __popc(m0);
+        int base = 0;
+        if (lane == 0) base = atomicAdd(&ctl[0], n0 + __popc(m1));
+        base = __shfl_sync(kFull, base, 0);
+        const unsigned below = (1u << lane) - 1u;
+        const int p0 = base + __popc(m0 & below);
+        const int p1 = base + n0 + __popc(m1 & below);
+        if (t0 && p0 < CAP) buf[p0] = make_key(s0, pos0);
+        if (t1 && p1 < CAP) buf[p1] = make_key(s1, pos1);
     }
 
     // Collective: drop held keys that cannot be among the k largest (no-op when n <= k).

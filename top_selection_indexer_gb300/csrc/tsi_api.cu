@@ -75,19 +75,19 @@ bool use_tc_attn(int H, int Hkv, int Dqk, int Dv, bool v_from_k) {
 namespace {
 
 size_t indexer_workspace(int B, int T, int S, int H_I, int d_I, int topk, int qk_dtype,
-                         bool onchip) {
+                         bool two_pass) {
     if (B <= 0 || T <= 0 || S < 0 || topk < 1) return 0;
     if (use_tc_indexer(qk_dtype, H_I, d_I))
-        return tsi::tc_indexer_workspace_bytes(qk_dtype, B, T, S, topk, onchip);
+        return tsi::tc_indexer_workspace_bytes(qk_dtype, B, T, S, topk, two_pass);
     return tsi::generic_workspace_bytes(B, T, S, topk);
 }
 
-// tsi_indexer_topk and its on-chip form: onchip keeps the tensor-core path's scores in
-// the scoring kernel (selection in its epilogue) instead of storing them for a second pass.
+// tsi_indexer_topk and its two-pass form: two_pass stores the tensor-core path's scores for
+// a second, selecting kernel instead of selecting in the scoring kernel's epilogue.
 tsi_status indexer_topk(const void* qI, const void* kI, const void* w, int qk_dtype, int w_dtype,
                         int B, int T, int S, int H_I, int d_I, int topk, const int32_t* kv_len,
                         int32_t* idx, float* score, void* workspace, size_t workspace_bytes,
-                        void* stream, bool onchip) {
+                        void* stream, bool two_pass) {
     if (!qk_dtype_ok(qk_dtype)) return fail(TSI_ERR_INVALID_ARG, "qk_dtype %d unknown", qk_dtype);
     if (!w_dtype_ok(w_dtype)) return fail(TSI_ERR_INVALID_ARG, "w_dtype %d unknown", w_dtype);
     if (B < 0 || T < 0 || S < 0)
@@ -107,7 +107,7 @@ tsi_status indexer_topk(const void* qI, const void* kI, const void* w, int qk_dt
     if (!aligned16(qI) || !aligned16(kI) || !aligned16(w) || !aligned16(idx) ||
         !aligned16(score) || !aligned16(kv_len))
         return fail(TSI_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
-    const size_t need = indexer_workspace(B, T, S, H_I, d_I, topk, qk_dtype, onchip);
+    const size_t need = indexer_workspace(B, T, S, H_I, d_I, topk, qk_dtype, two_pass);
     if (workspace_bytes < need || (need > 0 && !workspace))
         return fail(TSI_ERR_WORKSPACE, "workspace %zu bytes, need %zu", workspace_bytes, need);
     if (need > 0 && !aligned16(workspace))
@@ -117,7 +117,7 @@ tsi_status indexer_topk(const void* qI, const void* kI, const void* w, int qk_dt
     if (st != TSI_OK) return st;
     tsi::IndexerArgs a{qI, kI, w, qk_dtype, w_dtype, B, T, S, H_I, d_I, topk, kv_len,
                        idx, score, err};
-    a.onchip = onchip;
+    a.two_pass = two_pass;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = tc ? tsi::launch_indexer_tc(a, workspace, s)
                        : tsi::launch_indexer_generic(a, workspace, s);
@@ -153,6 +153,11 @@ size_t tsi_indexer_topk_workspace(int B, int T, int S, int H_I, int d_I, int top
 
 size_t tsi_indexer_topk_onchip_workspace(int B, int T, int S, int H_I, int d_I, int topk,
                                          int qk_dtype) {
+    return indexer_workspace(B, T, S, H_I, d_I, topk, qk_dtype, false);
+}
+
+size_t tsi_indexer_topk_two_pass_workspace(int B, int T, int S, int H_I, int d_I, int topk,
+                                           int qk_dtype) {
     return indexer_workspace(B, T, S, H_I, d_I, topk, qk_dtype, true);
 }
 
@@ -168,6 +173,14 @@ tsi_status tsi_indexer_topk_onchip(const void* qI, const void* kI, const void* w
                                    int w_dtype, int B, int T, int S, int H_I, int d_I, int topk,
                                    const int32_t* kv_len, int32_t* idx, float* score,
                                    void* workspace, size_t workspace_bytes, void* stream) {
+    return indexer_topk(qI, kI, w, qk_dtype, w_dtype, B, T, S, H_I, d_I, topk, kv_len, idx, score,
+                        workspace, workspace_bytes, stream, false);
+}
+
+tsi_status tsi_indexer_topk_two_pass(const void* qI, const void* kI, const void* w, int qk_dtype,
+                                     int w_dtype, int B, int T, int S, int H_I, int d_I, int topk,
+                                     const int32_t* kv_len, int32_t* idx, float* score,
+                                     void* workspace, size_t workspace_bytes, void* stream) {
     return indexer_topk(qI, kI, w, qk_dtype, w_dtype, B, T, S, H_I, d_I, topk, kv_len, idx, score,
                         workspace, workspace_bytes, stream, true);
 }
