@@ -155,23 +155,156 @@ namespace {
 
 // One block per row: the row's n <= topk distinct keys (unordered) become idx / score in
 // rank order.
+//
+// Bucket rank.  The keys of a row lie in [kmin, kmax], so they share every bit above the
+// highest bit in which those two differ; the next kRankBucketBits bits (down from that
+// bit) split them into 2048 buckets whose order is the key order.  A histogram and an
+// exclusive scan (largest bucket first) give each bucket its range of ranks; the keys are
+// scattered into their buckets, and each key's rank is its bucket's first rank plus the
+// number of larger keys in its bucket.  Rank keys are distinct, so the ranks are a
+// permutation.  A row with more than kRankBucketMax keys in one bucket (many equal scores)
+// is ranked by the bitonic sorts and merges of rank_merge_write instead, so the work per
+// key stays bounded.
+constexpr int kRankBucketBits = 11;
+constexpr int kRankBuckets = 1 << kRankBucketBits;
+constexpr int kRankBucketMax = 32;
+
 __global__ void __launch_bounds__(kRankThreads) topk_rank_kernel(int topk, const uint64_t* cand,
                                                                   const int* cand_cnt,
                                                                   int32_t* idx, float* score,
                                                                   unsigned* err) {
-    __shared__ __align__(16) uint64_t xs[2 * kRankN];  // keys, then ranking scratch
+    __shared__ __align__(16) uint64_t xs[2 * kRankN];  // bucketed keys; ranking scratch
+    __shared__ unsigned cnt[kRankBuckets];   // keys per bucket, then the bucket's first rank
+    __shared__ unsigned fill[kRankBuckets];  // scatter cursors
+    __shared__ unsigned long long rng[2];
+    __shared__ unsigned wsum[kRankThreads / 32];
+    __shared__ unsigned big;
     const int row = blockIdx.x;
     const int t = threadIdx.x;
+    const int lane = t & 31, wid = t >> 5;
     int n = cand_cnt[row];
     if (n < 0 || n > topk) {
         if (t == 0) atomicOr(err, kErrAssert);
         n = n < 0 ? 0 : topk;
     }
     const uint64_t* c = cand + static_cast<int64_t>(row) * topk;
-    for (int i = t; i < kRankN; i += kRankThreads) xs[i] = i < n ? c[i] : 0ull;
+    int32_t* io = idx + static_cast<int64_t>(row) * topk;
+    float* so = score ? score + static_cast<int64_t>(row) * topk : nullptr;
+    // this thread's keys: slots t + 256 j
+    uint64_t x[kRankPer];
+    uint64_t hi = 0ull, lo = ~0ull;
+#pragma unroll
+    for (int j = 0; j < kRankPer; ++j) {
+        const int i = t + kRankThreads * j;
+        x[j] = i < n ? c[i] : 0ull;
+        if (i < n) {
+            hi = x[j] > hi ? x[j] : hi;
+            lo = x[j] < lo ? x[j] : lo;
+        }
+    }
+    for (int i = t; i < kRankBuckets; i += kRankThreads) {
+        cnt[i] = 0u;
+        fill[i] = 0u;
+    }
+    if (t == 0) {
+        rng[0] = 0ull;
+        rng[1] = ~0ull;
+        big = 0u;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const uint64_t h2 = __shfl_xor_sync(kFull, hi, o);
+        const uint64_t l2 = __shfl_xor_sync(kFull, lo, o);
+        hi = h2 > hi ? h2 : hi;
+        lo = l2 < lo ? l2 : lo;
+    }
     __syncthreads();
-    rank_merge_write(xs, xs + kRankN, n, topk, idx + static_cast<int64_t>(row) * topk,
-                    score ? score + static_cast<int64_t>(row) * topk : nullptr, t, 1);
+    if (lane == 0 && n > 0) {
+        atomicMax(&rng[0], static_cast<unsigned long long>(hi));
+        atomicMin(&rng[1], static_cast<unsigned long long>(lo));
+    }
+    __syncthreads();
+    hi = rng[0];
+    lo = rng[1];
+    // bucket b of key v: the kRankBucketBits bits below the common prefix, largest first
+    const int top = n > 1 ? 63 - __clzll(static_cast<long long>(hi ^ lo)) : 0;
+    const int shift = top + 1 > kRankBucketBits ? top + 1 - kRankBucketBits : 0;
+    auto bucket = [&](uint64_t v) {
+        return static_cast<unsigned>(kRankBuckets - 1) -
+               (static_cast<unsigned>(v >> shift) & static_cast<unsigned>(kRankBuckets - 1));
+    };
+#pragma unroll
+    for (int j = 0; j < kRankPer; ++j)
+        if (t + kRankThreads * j < n) atomicAdd(&cnt[bucket(x[j])], 1u);
+    __syncthreads();
+    // exclusive scan of the 2048 counts: thread t owns buckets 8 t .. 8 t + 7
+    unsigned v[kRankPer];
+    unsigned own = 0u, mx = 0u;
+#pragma unroll
+    for (int j = 0; j < kRankPer; ++j) {
+        v[j] = cnt[kRankPer * t + j];
+        own += v[j];
+        mx = v[j] > mx ? v[j] : mx;
+    }
+    unsigned incl = own;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned y = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) wsum[wid] = incl;
+    if (mx > static_cast<unsigned>(kRankBucketMax)) atomicMax(&big, mx);
+    __syncthreads();
+    unsigned base = 0u;
+    for (int w = 0; w < wid; ++w) base += wsum[w];
+    const bool bucketed = big == 0u;
+    if (bucketed) {
+        unsigned run = base + incl - own;
+#pragma unroll
+        for (int j = 0; j < kRankPer; ++j) {
+            cnt[kRankPer * t + j] = run;  // first rank of the bucket
+            run += v[j];
+        }
+    }
+    __syncthreads();
+    if (!bucketed) {  // a bucket too full for counting: sort and merge
+        for (int i = t; i < kRankN; i += kRankThreads) xs[i] = i < n ? c[i] : 0ull;
+        __syncthreads();
+        rank_merge_write(xs, xs + kRankN, n, topk, io, so, t, 1);
+        return;
+    }
+    // scatter into bucket order
+    unsigned slot[kRankPer];
+#pragma unroll
+    for (int j = 0; j < kRankPer; ++j) {
+        slot[j] = 0u;
+        if (t + kRankThreads * j < n) {
+            const unsigned b = bucket(x[j]);
+            slot[j] = cnt[b] + atomicAdd(&fill[b], 1u);
+            xs[slot[j]] = x[j];
+        }
+    }
+    __syncthreads();
+    // rank = first rank of the bucket + larger keys in the bucket; the ranked keys go to the
+    // second half of xs, then out in rank order with consecutive threads on consecutive ranks
+    uint64_t* ranked = xs + kRankN;
+#pragma unroll
+    for (int j = 0; j < kRankPer; ++j) {
+        if (t + kRankThreads * j < n) {
+            const unsigned b = bucket(x[j]);
+            const unsigned first = cnt[b], m = fill[b];
+            unsigned r = first;
+            for (unsigned q = first; q < first + m; ++q) r += xs[q] > x[j] ? 1u : 0u;
+            ranked[r] = x[j];
+        }
+    }
+    __syncthreads();
+    for (int r = t; r < topk; r += kRankThreads) {
+        const bool real = r < n;
+        const uint64_t v = real ? ranked[r] : 0ull;
+        io[r] = real ? key_position(v) : -1;
+        if (so) so[r] = real ? key_score(v) : -__int_as_float(0x7f800000);
+    }
 }
 
 // ------------------------------------------------------------------- split merge

@@ -154,6 +154,10 @@ struct TcParams {
     int* fail_count;
     const int* unit_list;
     const int* unit_count;
+    // raw query rows and their size (the next unit's rows and gate weights are prefetched
+    // into L2 while the current unit runs)
+    const uint8_t* q_raw;
+    int q_row_bytes, w_bytes;
 };
 
 struct Unit {
@@ -352,6 +356,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int h = 0; h < L::kN; h += 128)
                             tc::tma_load_2d(qbuf + c * L::kQChunkBytes + h * 128, &tmap_q, c * 64,
                                             qrow + h, qfull);
+                    // the next unit's query rows and gate weights into L2, so that its Q load
+                    // and the epilogue's gate loads do not wait on HBM
+                    const int jn = j + gridDim.x;
+                    if (jn < n_units) {
+                        const Unit Un = unit_of<R>(p, p.unit_list ? p.unit_list[jn] : jn);
+                        int64_t r0 = static_cast<int64_t>(Un.b) * p.T + Un.t_hi - (R - 1);
+                        const int64_t r1 = static_cast<int64_t>(Un.b) * p.T + Un.t_hi + 1;
+                        if (r0 < static_cast<int64_t>(Un.b) * p.T) r0 = static_cast<int64_t>(Un.b) * p.T;
+                        if (r1 > r0) {
+                            tc::prefetch_l2(p.q_raw + r0 * 64 * p.q_row_bytes,
+                                            static_cast<uint32_t>((r1 - r0) * 64 * p.q_row_bytes));
+                            tc::prefetch_l2(static_cast<const uint8_t*>(p.w) + r0 * 64 * p.w_bytes,
+                                            static_cast<uint32_t>((r1 - r0) * 64 * p.w_bytes));
+                        }
+                    }
                 }
                 for (int i = 0; i < U.ntiles; ++i) {
                     const bool ready = tc::mbar_try_wait(&empty[s], ph ^ 1);
@@ -776,6 +795,9 @@ cudaError_t launch_qk(const IndexerArgs& a, void* workspace, cudaStream_t st) {
     p.idx = a.idx;
     p.score = a.score;
     p.err = a.err;
+    p.q_raw = static_cast<const uint8_t*>(a.qI);
+    p.q_row_bytes = QK == TSI_BF16 ? 256 : 128;
+    p.w_bytes = a.w_dtype == TSI_BF16 ? 2 : 4;
     tc_plan(QK, a.B, a.T, a.S, &p.n_chunks, &p.chunk_keys);
     const int rows = a.B * a.T;
     // Candidate lists: the caller's (one list per row), else the workspace's (the fused

@@ -67,7 +67,7 @@ struct TopKSelector {
     unsigned* hist;  // [256]
     int* ctl;        // [8]: 0 count, 1 digit, 2 above, 3 in-bin, 4 write cursor
     uint64_t* thr;   // admission threshold
-    uint64_t* rng;   // largest held key, during a compaction
+    uint64_t* rng;   // [2]: largest and smallest held key, during a compaction
     int tid;         // 0..NT-1 within the group
     int bar_id;      // named barrier of the group
     unsigned* err;   // device error word: consistency checks record kErrAssert here
@@ -98,7 +98,8 @@ struct TopKSelector {
             ctl[0] = 0;
             ctl[4] = 0;
             *thr = threshold;
-            *rng = 0ull;
+            rng[0] = 0ull;
+            rng[1] = ~0ull;
         }
         for (int i = tid; i < 256; i += NT) hist[i] = 0u;
         sync();
@@ -150,7 +151,8 @@ struct TopKSelector {
             ctl[0] = 0;
             ctl[4] = 0;
             *thr = threshold;
-            *rng = 0ull;
+            rng[0] = 0ull;
+            rng[1] = ~0ull;
         }
         sync();
     }
@@ -258,11 +260,14 @@ struct TopKSelector {
     // k + slack keys: every key dropped is below the k-th largest, so nothing of the
     // final top k is lost.  The admission threshold rises to the kept bin's lower edge.
     // move = false only sets that threshold and leaves the buffer as it is (for a caller
-    // that empties it next).  Between compactions hist[] is all zero and rng[0] is 0.
+    // that empties it next).  Between compactions hist[] is all zero, rng[0] is 0 and
+    // rng[1] all ones.
     __device__ void compact(int k, int n, bool exact = true, int slack = 0, bool move = true) {
         if (n <= k) return;
         constexpr int U = 4;  // keys in flight per thread
-        uint64_t hi = 0ull;
+        // the range of the held keys: bits above the highest bit in which the smallest and
+        // the largest differ are common to all of them
+        uint64_t hi = 0ull, mn = ~0ull;
         for (int b = 0; b < n; b += U * NT) {
             uint64_t x[U];
 #pragma unroll
@@ -271,19 +276,27 @@ struct TopKSelector {
                 x[j] = i < n ? buf[i] : 0ull;
             }
 #pragma unroll
-            for (int j = 0; j < U; ++j) hi = x[j] > hi ? x[j] : hi;
+            for (int j = 0; j < U; ++j) {
+                hi = x[j] > hi ? x[j] : hi;
+                if (b + j * NT + tid < n) mn = x[j] < mn ? x[j] : mn;
+            }
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
             const uint64_t h2 = __shfl_xor_sync(kFull, hi, o);
+            const uint64_t m2 = __shfl_xor_sync(kFull, mn, o);
             hi = h2 > hi ? h2 : hi;
+            mn = m2 < mn ? m2 : mn;
         }
-        if ((threadIdx.x & 31) == 0)
+        if ((threadIdx.x & 31) == 0) {
             atomicMax(reinterpret_cast<unsigned long long*>(rng), static_cast<unsigned long long>(hi));
+            atomicMin(reinterpret_cast<unsigned long long*>(rng + 1),
+                      static_cast<unsigned long long>(mn));
+        }
         sync();
-        hi = *rng;
-        const uint64_t lo = *thr;
-        if (hi <= lo) {  // n >= 2 distinct keys, all >= lo: the largest is above lo
+        hi = rng[0];
+        const uint64_t lo = rng[1];
+        if (hi <= lo || lo < *thr) {  // n >= 2 distinct keys, all >= the threshold
             if (tid == 0) atomicOr(err, kErrAssert);
             return;
         }
@@ -324,7 +337,8 @@ struct TopKSelector {
                 for (int j = 0; j < 8; ++j) hist[255 - (tid * 8 + j)] = 0u;
                 if (tid == 0) {
                     ctl[1] = -1;
-                    *rng = 0ull;  // every thread read it before the barrier above
+                    rng[0] = 0ull;  // every thread read them before the barrier above
+                    rng[1] = ~0ull;
                 }
                 __syncwarp();
                 unsigned incl = sum;
