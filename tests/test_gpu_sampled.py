@@ -2,7 +2,7 @@
 its sampled admission threshold, against the oracle.
 
 With several query rows per sequence the call first scores every 32nd key of each row and
-admits, in the full scoring pass, only keys at or above the row's ~109th largest sampled
+admits, in the full scoring pass, only keys at or above the row's 100th largest sampled
 score (for k = 2048).  These inputs make that sample lie:
 
 - the sampled keys score low and all others high: the threshold admits every key, each
