@@ -74,8 +74,10 @@ def _kernel_files(kernel):
     return {
         "tsi_attn_tc_kernel": ["attn_tc.cu", "latent_gather.cuh", "tc_common.cuh"],
         "attn_generic_kernel": ["attn_generic.cu"],
-        "tsi_indexer_tc_kernel": ["indexer_tc.cu", "topk_rows.cu", "topk_select.cuh",
-                                  "rank_sort.cuh", "tc_common.cuh"],
+        # the default call: sample gather, threshold and full scoring passes, short units,
+        # then the ranking kernel (indexer_generic.cu)
+        "tsi_indexer_tc_kernel": ["indexer_tc.cu", "indexer_generic.cu", "topk_select.cuh",
+                                  "rank_sort.cuh", "tc_common.cuh", "kernels_tc.cuh"],
         "indexer_generic_kernel": ["indexer_generic.cu", "topk_select.cuh"],
         "tsi_index_kl_tc_kernel": ["index_kl_tc.cu", "latent_gather.cuh", "tc_common.cuh"],
     }[kernel]

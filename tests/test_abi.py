@@ -126,11 +126,13 @@ def test_two_pass_workspace_holds_one_chunk_of_scores(lib, B, T, S, qk, R):
 @pytest.mark.parametrize("B,T,S,qk,R", [(1, 131072, 131072, tsi.E4M3, 4),
                                         (2, 3000, 3000, tsi.BF16, 2)])
 def test_default_workspace_holds_candidate_lists_and_the_sample(lib, B, T, S, qk, R):
-    # the default stores no score: one list of k 8-byte keys per row (these shapes have
+    # the default stores no score: one list per row of every key its selector held (8 B a
+    # key, the selector's capacity: 4352 keys for e4m3, 5888 for bf16; these shapes have
     # enough rows to keep each row's keys in one range), a count per row, and the sampled
     # selection's scratch; the on-chip name is the same call
     need = lib.tsi_indexer_topk_workspace(B, T, S, 64, 128, 2048, qk)
-    assert need == _lists_bytes(B * T) + _sampled_bytes(B, T, S, qk, R)
+    cap = 5888 if qk == tsi.BF16 else 4352
+    assert need == _lists_bytes(B * T, cap) + _sampled_bytes(B, T, S, qk, R)
     assert lib.tsi_indexer_topk_onchip_workspace(B, T, S, 64, 128, 2048, qk) == need
     assert need < lib.tsi_indexer_topk_two_pass_workspace(B, T, S, 64, 128, 2048, qk) or \
         T * S < 1 << 24

@@ -153,48 +153,60 @@ namespace {
 
 // ------------------------------------------------------------------------- ranking
 
-// One block per row: the row's n <= topk distinct keys (unordered) become idx / score in
-// rank order.
+// One block per row: the row's n distinct keys (unordered, n <= the list's stride) become
+// its min(n, topk) best as idx / score in rank order.
 //
-// Bucket rank.  The keys of a row lie in [kmin, kmax], so they share every bit above the
-// highest bit in which those two differ; the next kRankBucketBits bits (down from that
-// bit) split them into 2048 buckets whose order is the key order.  A histogram and an
-// exclusive scan (largest bucket first) give each bucket its range of ranks; the keys are
-// scattered into their buckets, and each key's rank is its bucket's first rank plus the
-// number of larger keys in its bucket.  Rank keys are distinct, so the ranks are a
-// permutation.  A row with more than kRankBucketMax keys in one bucket (many equal scores)
-// is ranked by the bitonic sorts and merges of rank_merge_write instead, so the work per
-// key stays bounded.
+// Bucket rank.  The keys of a row lie in [kmin, kmax]; (key - kmin) >> shift, with the
+// shift that maps kmax - kmin below 2^kRankBucketBits, splits them into 2048 buckets of
+// equal width whose order is the key order (buckets aligned to the key range, not to bit
+// boundaries: a range that crosses a power of two in score is not coarsened).  A histogram
+// and an exclusive scan (largest bucket first) give each bucket its first rank.  A bucket whose
+// first rank is k or more holds no key of the result and is skipped; the keys of the
+// others are scattered into their buckets, and each key's rank is its bucket's first rank
+// plus the number of larger keys in its bucket.  Rank keys are distinct, so the ranks are
+// a permutation.  A row with more than kRankBucketMax keys in one of the buckets it keeps
+// (many equal scores, or keys crowded below an outlier) takes the general path instead: an
+// exact MSD radix select of its k best (when it holds more than k), then the bitonic sorts
+// and merges of rank_merge_write, so the work per key stays bounded.
 constexpr int kRankBucketBits = 11;
 constexpr int kRankBuckets = 1 << kRankBucketBits;
 constexpr int kRankBucketMax = 32;
+constexpr int kRankScanPer = kRankBuckets / kRankThreads;  // buckets per thread in the scan
+constexpr int kRankListIn = 24;  // list slots per thread of the wide form: 6144 keys a row
+static_assert(kRankScanPer * kRankThreads == kRankBuckets, "scan layout");
 
-__global__ void __launch_bounds__(kRankThreads) topk_rank_kernel(int topk, const uint64_t* cand,
-                                                                  const int* cand_cnt,
-                                                                  int32_t* idx, float* score,
-                                                                  unsigned* err) {
-    __shared__ __align__(16) uint64_t xs[2 * kRankN];  // bucketed keys; ranking scratch
-    __shared__ unsigned cnt[kRankBuckets];   // keys per bucket, then the bucket's first rank
-    __shared__ unsigned fill[kRankBuckets];  // scatter cursors
+template <int IN>  // list slots per thread: a list holds at most IN * kRankThreads keys
+__global__ void __launch_bounds__(kRankThreads, IN <= 17 ? 4 : 3)
+    topk_rank_kernel(int topk, int stride, const uint64_t* cand, const int* cand_cnt,
+                     int32_t* idx, float* score, unsigned* err) {
+    // xs: the kept buckets' keys (at most k - 1 + kRankBucketMax), then the ranked keys; the
+    // general path uses the first 2 kRankN as keys and ranking scratch.  cnt: keys per
+    // bucket, then the bucket's first rank.  fill: scatter cursors; the radix select's
+    // histogram.  (kRankSmemBytes of dynamic shared memory.)
+    extern __shared__ __align__(16) uint64_t rank_smem[];
+    uint64_t* xs = rank_smem;
+    unsigned* cnt = reinterpret_cast<unsigned*>(rank_smem + 2 * kRankN + kRankBucketMax);
+    unsigned* fill = cnt + kRankBuckets;
     __shared__ unsigned long long rng[2];
     __shared__ unsigned wsum[kRankThreads / 32];
-    __shared__ unsigned big;
+    __shared__ int ctl[4];  // big bucket; radix select: bin, keys above it, keys in it
     const int row = blockIdx.x;
     const int t = threadIdx.x;
     const int lane = t & 31, wid = t >> 5;
     int n = cand_cnt[row];
-    if (n < 0 || n > topk) {
+    if (n < 0 || n > stride || n > IN * kRankThreads) {
         if (t == 0) atomicOr(err, kErrAssert);
-        n = n < 0 ? 0 : topk;
+        n = n < 0 ? 0 : (stride < IN * kRankThreads ? stride : IN * kRankThreads);
     }
-    const uint64_t* c = cand + static_cast<int64_t>(row) * topk;
+    const int n_out = n < topk ? n : topk;
+    const uint64_t* c = cand + static_cast<int64_t>(row) * stride;
     int32_t* io = idx + static_cast<int64_t>(row) * topk;
     float* so = score ? score + static_cast<int64_t>(row) * topk : nullptr;
-    // this thread's keys: slots t + 256 j
-    uint64_t x[kRankPer];
+    // this thread's keys: slots t + 256 j (0 past the n-th: below every real key)
+    uint64_t x[IN];
     uint64_t hi = 0ull, lo = ~0ull;
 #pragma unroll
-    for (int j = 0; j < kRankPer; ++j) {
+    for (int j = 0; j < IN; ++j) {
         const int i = t + kRankThreads * j;
         x[j] = i < n ? c[i] : 0ull;
         if (i < n) {
@@ -209,7 +221,7 @@ __global__ void __launch_bounds__(kRankThreads) topk_rank_kernel(int topk, const
     if (t == 0) {
         rng[0] = 0ull;
         rng[1] = ~0ull;
-        big = 0u;
+        ctl[0] = 0;
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -225,26 +237,25 @@ __global__ void __launch_bounds__(kRankThreads) topk_rank_kernel(int topk, const
     }
     __syncthreads();
     hi = rng[0];
-    lo = rng[1];
-    // bucket b of key v: the kRankBucketBits bits below the common prefix, largest first
-    const int top = n > 1 ? 63 - __clzll(static_cast<long long>(hi ^ lo)) : 0;
-    const int shift = top + 1 > kRankBucketBits ? top + 1 - kRankBucketBits : 0;
+    lo = n > 0 ? rng[1] : hi;
+    // bucket b of key v: (v - kmin) >> shift, largest first
+    const uint64_t width = hi - lo;
+    const int wbits = width ? 64 - __clzll(static_cast<long long>(width)) : 0;
+    const int shift = wbits > kRankBucketBits ? wbits - kRankBucketBits : 0;
     auto bucket = [&](uint64_t v) {
-        return static_cast<unsigned>(kRankBuckets - 1) -
-               (static_cast<unsigned>(v >> shift) & static_cast<unsigned>(kRankBuckets - 1));
+        return static_cast<unsigned>(kRankBuckets - 1) - static_cast<unsigned>((v - lo) >> shift);
     };
 #pragma unroll
-    for (int j = 0; j < kRankPer; ++j)
+    for (int j = 0; j < IN; ++j)
         if (t + kRankThreads * j < n) atomicAdd(&cnt[bucket(x[j])], 1u);
     __syncthreads();
-    // exclusive scan of the 2048 counts: thread t owns buckets 8 t .. 8 t + 7
-    unsigned v[kRankPer];
-    unsigned own = 0u, mx = 0u;
+    // exclusive scan of the counts: thread t owns buckets kRankScanPer t .. + kRankScanPer - 1
+    unsigned v[kRankScanPer];
+    unsigned own = 0u;
 #pragma unroll
-    for (int j = 0; j < kRankPer; ++j) {
-        v[j] = cnt[kRankPer * t + j];
+    for (int j = 0; j < kRankScanPer; ++j) {
+        v[j] = cnt[kRankScanPer * t + j];
         own += v[j];
-        mx = v[j] > mx ? v[j] : mx;
     }
     unsigned incl = own;
 #pragma unroll
@@ -253,58 +264,149 @@ __global__ void __launch_bounds__(kRankThreads) topk_rank_kernel(int topk, const
         if (lane >= o) incl += y;
     }
     if (lane == 31) wsum[wid] = incl;
-    if (mx > static_cast<unsigned>(kRankBucketMax)) atomicMax(&big, mx);
     __syncthreads();
     unsigned base = 0u;
     for (int w = 0; w < wid; ++w) base += wsum[w];
-    const bool bucketed = big == 0u;
-    if (bucketed) {
+    {
         unsigned run = base + incl - own;
+        bool big = false;
 #pragma unroll
-        for (int j = 0; j < kRankPer; ++j) {
-            cnt[kRankPer * t + j] = run;  // first rank of the bucket
+        for (int j = 0; j < kRankScanPer; ++j) {
+            cnt[kRankScanPer * t + j] = run;  // first rank of the bucket
+            // a kept bucket (first rank below k) must be small enough to count in
+            big |= run < static_cast<unsigned>(topk) && v[j] > static_cast<unsigned>(kRankBucketMax);
             run += v[j];
         }
+        if (big) ctl[0] = 1;
     }
     __syncthreads();
-    if (!bucketed) {  // a bucket too full for counting: sort and merge
-        for (int i = t; i < kRankN; i += kRankThreads) xs[i] = i < n ? c[i] : 0ull;
+    if (ctl[0] == 0) {
+        // scatter the kept buckets' keys into bucket order
+#pragma unroll
+        for (int j = 0; j < IN; ++j) {
+            if (t + kRankThreads * j < n) {
+                const unsigned b = bucket(x[j]);
+                const unsigned first = cnt[b];
+                if (first < static_cast<unsigned>(topk)) xs[first + atomicAdd(&fill[b], 1u)] = x[j];
+            }
+        }
         __syncthreads();
-        rank_merge_write(xs, xs + kRankN, n, topk, io, so, t, 1);
+        // rank = first rank of the bucket + larger keys in the bucket; the result goes to
+        // the second part of xs, then out in rank order (consecutive threads, consecutive
+        // ranks)
+        uint64_t* ranked = xs + kRankN + kRankBucketMax;
+#pragma unroll
+        for (int j = 0; j < IN; ++j) {
+            if (t + kRankThreads * j < n) {
+                const unsigned b = bucket(x[j]);
+                const unsigned first = cnt[b];
+                if (first < static_cast<unsigned>(topk)) {
+                    const unsigned m = fill[b];
+                    unsigned r = first;
+                    for (unsigned q = first; q < first + m; ++q) r += xs[q] > x[j] ? 1u : 0u;
+                    if (r < static_cast<unsigned>(topk)) ranked[r] = x[j];
+                }
+            }
+        }
+        __syncthreads();
+        for (int r = t; r < topk; r += kRankThreads) {
+            const bool real = r < n_out;
+            const uint64_t y = real ? ranked[r] : 0ull;
+            io[r] = real ? key_position(y) : -1;
+            if (so) so[r] = real ? key_score(y) : -__int_as_float(0x7f800000);
+        }
         return;
     }
-    // scatter into bucket order
-    unsigned slot[kRankPer];
+    // General path.  More than k keys: an exact MSD radix select finds the k-th largest
+    // key (the bits above the highest bit in which the smallest and largest keys differ are
+    // common to all; then one digit of up to 8 bits per pass narrows down the bin of the
+    // k-th key until that bin holds exactly the keys still needed); keys at or above the
+    // resulting prefix are exactly the k best.
+    uint64_t prefix = 0ull;
+    if (n > topk) {
+        unsigned* hist = fill;  // 256 bins, zero from the start of the kernel
+        const int top = 63 - __clzll(static_cast<long long>(hi ^ lo));  // n > 1: keys differ
+        prefix = top == 63 ? 0ull : (hi & ~((2ull << top) - 1ull));
+        int width = top + 1 < 8 ? top + 1 : 8;
+        int sh = top + 1 - width;
+        int need = topk;
+        while (true) {
+            const int end = sh + width;
+            const uint64_t hmask = end >= 64 ? 0ull : ~((1ull << end) - 1ull);
+            const unsigned dmask = (1u << width) - 1u;
 #pragma unroll
-    for (int j = 0; j < kRankPer; ++j) {
-        slot[j] = 0u;
-        if (t + kRankThreads * j < n) {
-            const unsigned b = bucket(x[j]);
-            slot[j] = cnt[b] + atomicAdd(&fill[b], 1u);
-            xs[slot[j]] = x[j];
+            for (int j = 0; j < IN; ++j)
+                if (t + kRankThreads * j < n && (x[j] & hmask) == prefix)
+                    atomicAdd(&hist[static_cast<unsigned>(x[j] >> sh) & dmask], 1u);
+            __syncthreads();
+            if (t < 32) {
+                // lane l scans bins 255-8l .. 248-8l (descending key order), then clears them
+                unsigned cb[8];
+                unsigned sum = 0;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    cb[j] = hist[255 - (t * 8 + j)];
+                    sum += cb[j];
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) hist[255 - (t * 8 + j)] = 0u;
+                if (t == 0) ctl[1] = -1;
+                __syncwarp();
+                unsigned inc = sum;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const unsigned y = __shfl_up_sync(kFull, inc, o);
+                    if (t >= o) inc += y;
+                }
+                const unsigned exc = inc - sum;
+                if (exc < static_cast<unsigned>(need) && static_cast<unsigned>(need) <= inc) {
+                    unsigned above = exc;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        if (above + cb[j] >= static_cast<unsigned>(need)) {
+                            ctl[1] = 255 - (t * 8 + j);
+                            ctl[2] = static_cast<int>(above);
+                            ctl[3] = static_cast<int>(cb[j]);
+                            break;
+                        }
+                        above += cb[j];
+                    }
+                }
+            }
+            __syncthreads();
+            const int d = ctl[1];
+            if (d < 0) {  // no bin holds the k-th key: counts are inconsistent
+                if (t == 0) atomicOr(err, kErrAssert);
+                break;
+            }
+            prefix |= static_cast<uint64_t>(d) << sh;
+            need -= ctl[2];
+            const bool done = ctl[3] == need || sh == 0;
+            __syncthreads();  // every thread has read ctl before the next scan writes it
+            if (done) break;
+            width = sh < 8 ? sh : 8;
+            sh -= width;
+        }
+    }
+    // the (at most k) kept keys into xs[0 .. n_out), the rest of the first kRankN slots 0
+    for (int i = t; i < kRankN; i += kRankThreads) xs[i] = 0ull;
+    if (t == 0) ctl[2] = 0;
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < IN; ++j) {
+        const bool keep = t + kRankThreads * j < n && x[j] >= prefix;
+        const unsigned m = __ballot_sync(kFull, keep);
+        if (m) {
+            int at = 0;
+            if (lane == 0) at = atomicAdd(&ctl[2], __popc(m));
+            at = __shfl_sync(kFull, at, 0);
+            const int pos = at + __popc(m & ((1u << lane) - 1u));
+            if (keep && pos < kRankN) xs[pos] = x[j];
         }
     }
     __syncthreads();
-    // rank = first rank of the bucket + larger keys in the bucket; the ranked keys go to the
-    // second half of xs, then out in rank order with consecutive threads on consecutive ranks
-    uint64_t* ranked = xs + kRankN;
-#pragma unroll
-    for (int j = 0; j < kRankPer; ++j) {
-        if (t + kRankThreads * j < n) {
-            const unsigned b = bucket(x[j]);
-            const unsigned first = cnt[b], m = fill[b];
-            unsigned r = first;
-            for (unsigned q = first; q < first + m; ++q) r += xs[q] > x[j] ? 1u : 0u;
-            ranked[r] = x[j];
-        }
-    }
-    __syncthreads();
-    for (int r = t; r < topk; r += kRankThreads) {
-        const bool real = r < n;
-        const uint64_t v = real ? ranked[r] : 0ull;
-        io[r] = real ? key_position(v) : -1;
-        if (so) so[r] = real ? key_score(v) : -__int_as_float(0x7f800000);
-    }
+    if (t == 0 && ctl[2] != n_out) atomicOr(err, kErrAssert);
+    rank_merge_write(xs, xs + kRankN, n_out, topk, io, so, t, 1);
 }
 
 // ------------------------------------------------------------------- split merge
@@ -518,10 +620,34 @@ __global__ void __launch_bounds__(kMergeThreads) topk_split_merge_kernel(
 
 }  // namespace
 
-cudaError_t launch_topk_rank(int rows, int topk, const uint64_t* cand, const int* cand_cnt,
-                             int32_t* idx, float* score, unsigned* err, cudaStream_t st) {
+int topk_rank_max_stride() { return kRankListIn * kRankThreads; }
+
+constexpr int kRankSmemBytes = (2 * kRankN + kRankBucketMax) * 8 + 2 * kRankBuckets * 4;
+
+template <int IN>
+cudaError_t rank_launch(int rows, int topk, int stride, const uint64_t* cand, const int* cand_cnt,
+                        int32_t* idx, float* score, unsigned* err, cudaStream_t st) {
+    static cudaError_t attr = cudaFuncSetAttribute(
+        topk_rank_kernel<IN>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRankSmemBytes);
+    if (attr != cudaSuccess) return attr;
+    topk_rank_kernel<IN><<<rows, kRankThreads, kRankSmemBytes, st>>>(topk, stride, cand,
+                                                                     cand_cnt, idx, score, err);
+    return cudaSuccess;
+}
+
+cudaError_t launch_topk_rank(int rows, int topk, int stride, const uint64_t* cand,
+                             const int* cand_cnt, int32_t* idx, float* score, unsigned* err,
+                             cudaStream_t st) {
     if (rows == 0) return cudaSuccess;
-    topk_rank_kernel<<<rows, kRankThreads, 0, st>>>(topk, cand, cand_cnt, idx, score, err);
+    if (stride < topk || stride > topk_rank_max_stride()) return cudaErrorInvalidValue;
+    // the fewest list slots per thread that hold the stride (registers: blocks per SM)
+    const cudaError_t e =
+        stride <= kRankN ? rank_launch<kRankPer>(rows, topk, stride, cand, cand_cnt, idx, score,
+                                                 err, st)
+        : stride <= 17 * kRankThreads
+            ? rank_launch<17>(rows, topk, stride, cand, cand_cnt, idx, score, err, st)
+            : rank_launch<kRankListIn>(rows, topk, stride, cand, cand_cnt, idx, score, err, st);
+    if (e != cudaSuccess) return e;
     note_launches(1);
     return cudaGetLastError();
 }

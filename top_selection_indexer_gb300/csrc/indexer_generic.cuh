@@ -99,9 +99,12 @@ struct ScoreRows {
 size_t topk_rows_smem_bytes();
 cudaError_t launch_topk_rows(const ScoreRows& r, cudaStream_t st);
 
-// Rank one unordered list of at most topk distinct keys per row ([rows][topk] keys +
-// counts) into rank-ordered idx / score rows.
-cudaError_t launch_topk_rank(int rows, int topk, const uint64_t* cand, const int* cand_cnt,
-                             int32_t* idx, float* score, unsigned* err, cudaStream_t st);
+// One unordered list of distinct keys per row ([rows][stride] keys + counts [rows], at most
+// stride keys a list) into each row's min(count, topk) best as rank-ordered idx / score
+// rows.  topk <= stride <= topk_rank_max_stride().
+int topk_rank_max_stride();
+cudaError_t launch_topk_rank(int rows, int topk, int stride, const uint64_t* cand,
+                             const int* cand_cnt, int32_t* idx, float* score, unsigned* err,
+                             cudaStream_t st);
 
 }  // namespace tsi

@@ -135,6 +135,10 @@ struct TcParams {
     float* score;
     uint64_t* cand;
     int* cand_cnt;
+    // Keys per candidate list: 0, lists of topk keys, each row's (chunk's) exact k best; or
+    // the selector's capacity, every key the row held (the ranking kernel keeps the k best,
+    // so no exact selection stalls this kernel at the end of a unit).
+    int cand_stride;
     int n_chunks, chunk_keys, n_units;
     int t_begin, t_end;  // query rows [t_begin, t_end) of every sequence in this launch
     float* scores;       // store variant: row (b, t) at (b * (t_end - t_begin) + t - t_begin) * ld
@@ -583,9 +587,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int need = n_here < p.topk ? static_cast<int>(n_here) : p.topk;
                     short_row = lost || (has_tau && held < need);
                     if (!short_row) {
-                        // the row's (chunk's) k best keys, unordered; the merge kernel ranks them
+                        // the row's (chunk's) held keys, or its k best, unordered; the
+                        // ranking or merge kernel takes them from there
                         const int64_t slot = row * p.n_chunks + U.chunk;
-                        sel.dump(p.topk, p.cand + slot * p.topk, p.cand_cnt + slot);
+                        if (p.cand_stride)
+                            sel.dump_all(p.cand + slot * p.cand_stride, p.cand_cnt + slot);
+                        else
+                            sel.dump(p.topk, p.cand + slot * p.topk, p.cand_cnt + slot);
                     }
                 }
             }
@@ -714,6 +722,12 @@ bool sampled_plan(int qk_dtype, int B, int T, int S) {
 
 int sample_keys(int S) { return (S + (1 << kSampleShift) - 1) >> kSampleShift; }
 
+// Keys per candidate list of the sampled-threshold launches: the row selector's capacity.
+int sampled_list_stride(int qk_dtype) {
+    return qk_dtype == TSI_BF16 ? Lay<TSI_BF16, TileCfg<TSI_BF16>::kRows, kModeSelect>::kCap
+                                : Lay<TSI_E4M3, TileCfg<TSI_E4M3>::kRows, kModeSelect>::kCap;
+}
+
 int64_t n_units_of(int qk_dtype, int B, int T) {
     const int R = rows_per_unit(qk_dtype, T);
     return static_cast<int64_t>(B) * ((T + R - 1) / R);
@@ -802,16 +816,21 @@ cudaError_t launch_qk(const IndexerArgs& a, void* workspace, cudaStream_t st) {
     const int rows = a.B * a.T;
     // Candidate lists: the caller's (one list per row), else the workspace's (the fused
     // variant: one per key chunk).  The store variant ranks each row itself, or leaves it
-    // unordered in the caller's lists, so its workspace holds the stored scores only.
+    // unordered in the caller's lists, so its workspace holds the stored scores only.  The
+    // sampled-threshold launches write each row's held keys to lists of the selector's
+    // capacity, and the ranking kernel selects from them.
     const int lists = p.n_chunks;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const bool wide = !kStore && R > 1 && lists == 1 && !a.out_cand;
+    const int stride = wide ? L::kCap : a.topk;
     if ((kStore || lists == 1) && a.out_cand) {
         p.cand = a.out_cand;
         p.cand_cnt = a.out_cnt;
     } else if (!kStore) {
         p.cand = reinterpret_cast<uint64_t*>(ws);
-        p.cand_cnt = reinterpret_cast<int*>(p.cand + static_cast<size_t>(rows) * lists * a.topk);
-        ws += cand_bytes(a.B, a.T, a.topk, lists);
+        p.cand_cnt = reinterpret_cast<int*>(p.cand + static_cast<size_t>(rows) * lists * stride);
+        p.cand_stride = wide ? stride : 0;
+        ws += cand_bytes(a.B, a.T, stride, lists);
     }
     constexpr int smem = L::kSmem;
     cudaError_t e = cudaFuncSetAttribute(tsi_indexer_tc_kernel<QK, R, kMode>,
@@ -875,8 +894,8 @@ cudaError_t launch_qk(const IndexerArgs& a, void* workspace, cudaStream_t st) {
         note_launches(1);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         return a.out_cand ? e
-                          : launch_topk_rank(rows, a.topk, p.cand, p.cand_cnt, a.idx, a.score,
-                                             a.err, st);
+                          : launch_topk_rank(rows, a.topk, stride, p.cand, p.cand_cnt, a.idx,
+                                             a.score, a.err, st);
     }
     // Launch pairs over chunks of query rows, the last rows first (each chunk's rows are
     // a multiple of R except the first rows of the sequences).
@@ -913,8 +932,8 @@ cudaError_t launch_qk(const IndexerArgs& a, void* workspace, cudaStream_t st) {
     if (e != cudaSuccess || kStore) return e;
     if (lists == 1)
         return a.out_cand ? e
-                          : launch_topk_rank(rows, a.topk, p.cand, p.cand_cnt, a.idx, a.score,
-                                             a.err, st);
+                          : launch_topk_rank(rows, a.topk, stride, p.cand, p.cand_cnt, a.idx,
+                                             a.score, a.err, st);
     // decode: the chunk lists of few rows are merged in two stages (stage space after them)
     void* stage = reinterpret_cast<uint8_t*>(p.cand_cnt) +
                   ((static_cast<size_t>(rows) * p.n_chunks * sizeof(int) + 255) & ~size_t(255));
@@ -935,8 +954,13 @@ size_t tc_indexer_workspace_bytes(int qk_dtype, int B, int T, int S, int topk, b
         return score_scratch_bytes(qk_dtype, B, T, S);
     int nc, ck;
     tc_plan(qk_dtype, B, T, S, &nc, &ck);
-    size_t n = cand_bytes(B, T, topk, nc) + (nc > 1 ? topk_merge_stage_bytes(B * T, topk, nc) : 0);
-    if (sampled_plan(qk_dtype, B, T, S)) n += sampled_ws(nullptr, qk_dtype, B, T, S).bytes;
+    // the sampled-threshold launches keep each row's held keys (lists of the selector's
+    // capacity); the others each row's or chunk's k best
+    const bool sampled = sampled_plan(qk_dtype, B, T, S);
+    const int stride = sampled ? sampled_list_stride(qk_dtype) : topk;
+    size_t n = cand_bytes(B, T, stride, nc) +
+               (nc > 1 ? topk_merge_stage_bytes(B * T, topk, nc) : 0);
+    if (sampled) n += sampled_ws(nullptr, qk_dtype, B, T, S).bytes;
     return n;
 }
 
