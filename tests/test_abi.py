@@ -138,6 +138,16 @@ def test_default_workspace_holds_candidate_lists_and_the_sample(lib, B, T, S, qk
         T * S < 1 << 24
 
 
+def test_bf16_decode_takes_the_cuda_core_path(lib):
+    # bf16 with one query per sequence: the CUDA-core path's workspace (as for fp32 inputs)
+    for S in (4000, 131072):
+        assert lib.tsi_indexer_topk_workspace(8, 1, S, 64, 128, 2048, tsi.BF16) == \
+            lib.tsi_indexer_topk_workspace(8, 1, S, 64, 128, 2048, tsi.F32)
+    # several queries per sequence stay on the tensor cores
+    assert lib.tsi_indexer_topk_workspace(1, 4096, 4096, 64, 128, 2048, tsi.BF16) != \
+        lib.tsi_indexer_topk_workspace(1, 4096, 4096, 64, 128, 2048, tsi.F32)
+
+
 def test_decode_workspace_holds_candidate_lists(lib):
     # one query per sequence: key-range candidate lists (8 B a key) and counts, no scores
     need = lib.tsi_indexer_topk_workspace(8, 1, 131072, 64, 128, 2048, tsi.E4M3)

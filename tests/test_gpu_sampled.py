@@ -14,7 +14,9 @@ score (for k = 2048).  These inputs make that sample lie:
 - every score equal (zero gate weights).
 
 Queries and gates are positive integers and a key row holds one integer value, so every
-score is exact in fp32 and the oracle's rows must be matched bit for bit.  A full-size
+score is exact in fp32 and the oracle's rows must be matched bit for bit.  The same kinds of
+input then go through the one-query-per-sequence (decode) path in e4m3, which has no sampled
+threshold: key chunks selected in the scoring kernel, merged per row.  A full-size
 L = 131072 integer-valued prefill checks sampled rows of the common path.  (Score equation
 and k: "GLM-5.2 技术报告速览", §IndexShare; the lower-index tie rule: BASELINE's reading of
 the deterministic top-k of "GLM-5: from Vibe Coding to Agentic Engineering" (Chinese
@@ -129,4 +131,97 @@ def test_full_size_prefill_integer_exact(cuda_lib):
     rows = sorted({0, 1, 2047, 2048, 3839, 3840, 3841, 5000, 65535, 65536, 100001, L - 4,
                    L - 3, L - 2, L - 1})
     check_indexer(qI.cpu(), kI.cpu(), w.cpu(), TOPK, idx.cpu(), sc.cpu(), rows=np.array(rows),
+                  exact=True)
+
+
+# ---- one query per sequence (decode, e4m3): no sampled threshold; each row's keys are split
+# into 19 chunks of 3200 keys that select in the scoring kernel's epilogue (their selectors
+# compact when every key is admitted), then the chunk lists are merged in two stages.
+# Adversarial inputs like the ones above, exact against the oracle.  (bf16 requests of one
+# query per sequence take the CUDA-core path.)
+
+BD, SD = 8, 60000
+
+
+def _decode_contrast(qk, sampled_value, other_value, seed, negative_rows=(), kv=None):
+    qf = draw((BD, 1, H, D), "int8", "f32", seed, "cuda").abs()
+    qf = torch.where(qf == 0, torch.ones_like(qf), qf)
+    if len(negative_rows):
+        sign = torch.ones(BD, device="cuda")
+        sign[torch.as_tensor(list(negative_rows), device="cuda")] = -1.0
+        qf = qf * sign.view(BD, 1, 1, 1)
+    pos = torch.arange(SD, device="cuda")
+    kval = torch.where(pos % 32 == 0, sampled_value, other_value).to(torch.float32)
+    kI = kval.view(1, SD, 1).expand(BD, SD, D).contiguous().to(TORCH[qk])
+    w = draw((BD, 1, H), "pow2", "bf16", seed + 1, "cuda")
+    return qf.to(TORCH[qk]), kI, w
+
+
+def _check_decode(cuda_lib, qI, kI, w, kv=None):
+    kvt = None if kv is None else torch.tensor(kv, dtype=torch.int32, device="cuda")
+    idx, sc = cuda_lib.indexer_topk(qI, kI, w, TOPK, kv_len=kvt, want_score=True)
+    cuda_lib.device_status()
+    check_indexer(qI.cpu(), kI.cpu(), w.cpu(), TOPK, idx.cpu(), sc.cpu(), rows=np.arange(BD),
+                  exact=True, kv_len=None if kv is None else torch.tensor(kv))
+    return idx.cpu()
+
+
+@pytest.mark.parametrize("qk", ["e4m3"])
+def test_decode_sample_low_others_high(cuda_lib, qk):
+    # two score values, every other key above the every-32nd ones: full chunk lists, ties
+    # inside each score
+    qI, kI, w = _decode_contrast(qk, 1.0, 4.0, 141)
+    idx = _check_decode(cuda_lib, qI, kI, w)
+    pos = torch.arange(SD)
+    expect = pos[pos % 32 != 0][:TOPK].to(torch.int32)
+    assert torch.equal(idx[:, 0], expect.expand(BD, TOPK))
+
+
+@pytest.mark.parametrize("qk", ["e4m3"])
+def test_decode_sample_high_others_low(cuda_lib, qk):
+    # fewer than k keys of the higher score: each row ends in keys of the lower score
+    qI, kI, w = _decode_contrast(qk, 4.0, 1.0, 143)
+    idx = _check_decode(cuda_lib, qI, kI, w)
+    n_high = (SD - 1) // 32 + 1
+    assert n_high < TOPK
+    row = idx[0, 0]
+    assert torch.equal(row[:n_high], torch.arange(0, 32 * n_high, 32, dtype=torch.int32))
+
+
+def test_decode_rows_mixing_ties_and_short_rows(cuda_lib):
+    # rows 1, 4, 6 score every key 0 (ties); ragged caches, one of a single chunk, one tiny
+    neg = [1, 4, 6]
+    kv = [60000, 41000, 60000, 30001, 2049, 60000, 17, 59999]
+    qI, kI, w = _decode_contrast("e4m3", 4.0, 1.0, 147, negative_rows=neg)
+    idx = _check_decode(cuda_lib, qI, kI, w, kv=kv)
+    assert torch.equal(idx[1, 0], torch.arange(TOPK, dtype=torch.int32))
+
+
+@pytest.mark.parametrize("qk", ["e4m3"])
+def test_decode_all_scores_equal(cuda_lib, qk):
+    qI = draw((BD, 1, H, D), "int8", qk, 151, "cuda", D)
+    kI = draw((BD, SD, D), "int8", qk, 152, "cuda", D)
+    w = torch.zeros((BD, 1, H), dtype=torch.bfloat16, device="cuda")
+    idx = _check_decode(cuda_lib, qI, kI, w)
+    assert torch.equal(idx[:, 0], torch.arange(TOPK, dtype=torch.int32).expand(BD, TOPK))
+
+
+@pytest.mark.parametrize("qk", ["e4m3"])
+def test_decode_random_integer_rows(cuda_lib, qk):
+    # random integer scores over ragged caches
+    qI = draw((BD, 1, H, D), "int8", qk, 161, "cuda", D)
+    kI = draw((BD, SD, D), "int8", qk, 162, "cuda", D)
+    w = draw((BD, 1, H), "pow2", "bf16", 163, "cuda", D)
+    _check_decode(cuda_lib, qI, kI, w, kv=[60000, 16384, 16385, 59001, 30000, 1, 2048, 45000])
+
+
+def test_decode_full_size_integer_exact(cuda_lib):
+    # the benchmark's decode shape: B = 8 over L = 131072
+    L = 131072
+    qI = draw((BD, 1, H, D), "int8", "e4m3", 171, "cuda", D)
+    kI = draw((BD, L, D), "int8", "e4m3", 172, "cuda", D)
+    w = draw((BD, 1, H), "pow2", "bf16", 173, "cuda", D)
+    idx, sc = cuda_lib.indexer_topk(qI, kI, w, TOPK, want_score=True)
+    cuda_lib.device_status()
+    check_indexer(qI.cpu(), kI.cpu(), w.cpu(), TOPK, idx.cpu(), sc.cpu(), rows=np.arange(BD),
                   exact=True)

@@ -66,6 +66,13 @@ bool use_tc_indexer(int qk_dtype, int H_I, int d_I) {
     return tsi::tc_indexer_supported(qk_dtype, H_I, d_I);
 }
 
+// The tensor-core path for a request.  bf16 requests of one query per sequence go to the
+// CUDA-core path: the tensor-core pass with one bf16 query row per unit faulted on key
+// caches of repeated rows, cause not found, so it does not run.
+bool use_tc_indexer(int qk_dtype, int H_I, int d_I, int T) {
+    return use_tc_indexer(qk_dtype, H_I, d_I) && !(qk_dtype == TSI_BF16 && T == 1);
+}
+
 bool use_tc_attn(int H, int Hkv, int Dqk, int Dv, bool v_from_k) {
     return tsi::tc_attn_supported(H, Hkv, Dqk, Dv, v_from_k);
 }
@@ -77,7 +84,7 @@ namespace {
 size_t indexer_workspace(int B, int T, int S, int H_I, int d_I, int topk, int qk_dtype,
                          bool two_pass) {
     if (B <= 0 || T <= 0 || S < 0 || topk < 1) return 0;
-    if (use_tc_indexer(qk_dtype, H_I, d_I))
+    if (use_tc_indexer(qk_dtype, H_I, d_I, T))
         return tsi::tc_indexer_workspace_bytes(qk_dtype, B, T, S, topk, two_pass);
     return tsi::generic_workspace_bytes(B, T, S, topk);
 }
@@ -95,7 +102,7 @@ tsi_status indexer_topk(const void* qI, const void* kI, const void* w, int qk_dt
     if (topk < 1 || topk > TSI_MAX_TOPK)
         return fail(TSI_ERR_UNSUPPORTED, "topk=%d outside [1, %d]", topk, TSI_MAX_TOPK);
     if (H_I < 1 || d_I < 1) return fail(TSI_ERR_INVALID_ARG, "H_I=%d d_I=%d", H_I, d_I);
-    const bool tc = use_tc_indexer(qk_dtype, H_I, d_I);
+    const bool tc = use_tc_indexer(qk_dtype, H_I, d_I, T);
     if (!tc && !tsi::generic_supported(H_I, d_I))
         return fail(TSI_ERR_UNSUPPORTED, "H_I=%d d_I=%d unsupported (d_I<=256, H_I<=128, "
                     "H_I*d_I<=8192)", H_I, d_I);
@@ -188,7 +195,7 @@ tsi_status tsi_indexer_topk_two_pass(const void* qI, const void* kI, const void*
 size_t tsi_indexer_topk_shard_workspace(int B, int T, int S_shard, int H_I, int d_I, int topk,
                                         int qk_dtype) {
     if (B <= 0 || T <= 0 || S_shard < 0 || topk < 1) return 0;
-    if (use_tc_indexer(qk_dtype, H_I, d_I))
+    if (use_tc_indexer(qk_dtype, H_I, d_I, T))
         return tsi::tc_indexer_split_workspace_bytes(qk_dtype, B, T, S_shard, topk);
     return tsi::generic_workspace_bytes(B, T, S_shard, topk);
 }
@@ -210,7 +217,7 @@ tsi_status tsi_indexer_topk_shard(const void* qI, const void* kI, const void* w,
     if (topk < 1 || topk > TSI_MAX_TOPK)
         return fail(TSI_ERR_UNSUPPORTED, "topk=%d outside [1, %d]", topk, TSI_MAX_TOPK);
     if (H_I < 1 || d_I < 1) return fail(TSI_ERR_INVALID_ARG, "H_I=%d d_I=%d", H_I, d_I);
-    const bool tc = use_tc_indexer(qk_dtype, H_I, d_I);
+    const bool tc = use_tc_indexer(qk_dtype, H_I, d_I, T);
     if (!tc && !tsi::generic_supported(H_I, d_I))
         return fail(TSI_ERR_UNSUPPORTED, "H_I=%d d_I=%d unsupported (d_I<=256, H_I<=128, "
                     "H_I*d_I<=8192)", H_I, d_I);
