@@ -13,6 +13,7 @@ the host cores on a bounded row sample of the same workload.
 """
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -45,12 +46,19 @@ def _peaks():
             "source": "fallback"}
 
 
+def _code_only(text):
+    """Source text without comments and blank lines (a comment edit keeps the key)."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    lines = (re.sub(r"//.*$", "", ln).rstrip() for ln in text.splitlines())
+    return "\n".join(ln for ln in lines if ln)
+
+
 def _kernel_sources_sha(names):
     h = hashlib.sha256()
     for n in names:
         p = os.path.join(ROOT, "top_selection_indexer_gb300", "csrc", n)
         if os.path.exists(p):
-            h.update(open(p, "rb").read())
+            h.update(_code_only(open(p, encoding="utf-8").read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -2,19 +2,23 @@
 //
 // I[t,s] = sum_j w[t,j] * ReLU(qI[t,j] . kI[s]) for s <= p_t, then the top-k keys of
 // each row ("GLM-5.2 技术报告速览", §IndexShare: the score equation, k = 2048; the
-// ReLU form is chosen there for speed and FP8 friendliness).  One kernel, two modes:
-//   - select (the default): each 128-key tile is scored in TMEM and streamed into a
-//     shared-memory top-k selector per query row, so no score reaches HBM; each row (or
-//     key chunk) leaves its k best keys unordered, for the ranking or merge kernels.  With
-//     several query rows per sequence the call runs it three times:
-//       1. on a strided sample of the keys (every 32nd, gathered into the workspace) with a
-//          small k' per row: the k'-th largest sampled score becomes the row's admission
-//          threshold, about c k keys of the row lie above it;
-//       2. on all keys, admitting only scores at or above that threshold: about c k appends
-//          per row instead of the ~k ln(L / k) of a selector that starts from nothing, so
-//          its buffer rarely fills and the epilogue almost never stops to compact;
-//       3. on the units where some row ended with fewer than k keys admitted (the sample
-//          misjudged it), from no threshold at all: the result is exact for any input.
+// ReLU form is chosen there for speed and FP8 friendliness).  One kernel, three modes:
+//   - capped and select (the default): each 128-key tile is scored in TMEM and streamed
+//     into a shared-memory top-k selector per query row, so no score reaches HBM.  With
+//     several query rows per sequence the call runs the kernel three times:
+//       1. (capped) on a strided sample of the keys (every 32nd, gathered into the
+//          workspace) with a small k' per row: the k'-th largest sampled score becomes the
+//          row's admission threshold, about c k keys of the row lie above it;
+//       2. (capped) on all keys, admitting only scores at or above that threshold: about
+//          c k appends per row instead of the ~k ln(L / k) of a selector that starts from
+//          nothing; the buffer is sized so that it never needs a room check, and each row
+//          leaves every key it holds, unordered, for the ranking kernel (which keeps the
+//          k best);
+//       3. (select: room checks, compactions) on the units where some row ended with
+//          fewer than k keys admitted or overflowed its buffer (the sample misjudged it),
+//          from no threshold at all: the result is exact for any input.
+//     With one query per sequence (decode) the select mode runs once over key chunks, each
+//     chunk leaving its exact k best for the merge kernels.
 //   - store (the two-pass alternative): every causal score goes to a row-major fp32 buffer,
 //     a chunk of query rows at a time; topk_rows.cu then selects and ranks each row's k
 //     best keys from it, at 4 B of HBM writes and reads per causal pair.
@@ -23,12 +27,13 @@
 // consecutive query rows on N = 64 R (the B operand), d_I = 128 on K, fp32 accumulators
 // in TMEM.  R = 4 for e4m3 (N = 256), 2 for bf16 (N = 128), 1 for decode.  The larger R,
 // the more query rows share each key tile: fewer tiles, MMA issues and barrier round
-// trips, less L2 traffic.  An epilogue thread owns one key (TMEM lane, 32x32b shape) and
-// reads that key's 64 head columns of its row in four loads of 16: the gate weights of the
-// whole row stay in its registers for the unit, and the head sum needs no other thread.
+// trips, less L2 traffic.  An epilogue warp reads its 32 TMEM lanes (keys) of its row's 64
+// columns as two 16-lane slices in the 16x256b shape (see tile_score): each thread holds
+// two keys x 16 heads per slice, so its 16 gate weights stay in registers for the unit.
 //
-// Roles of one persistent CTA (576 threads):
-//   warp 0       TMA producer: Q tile of the unit, key tiles into a ring of stages
+// Roles of one persistent CTA (608 threads):
+//   warp 0       TMA producer: Q tile of the unit, key tiles into a ring of stages, the
+//                next unit's query rows and gate weights prefetched into L2
 //   warps 1, 18  MMA issuers, one thread each: warp 1 the even tiles, warp 18 the odd ones
 //                (512 TMEM columns: 512 / N accumulators, so the MMA runs that many tiles
 //                ahead; two issuers overlap each other's barrier waits).  Warp 1 also

@@ -472,9 +472,8 @@ struct TopKSelector {
         sync();
     }
 
-    // Collective: reduce to at most k keys and copy them (unordered) to global memory.
-    // Collective: every held key (no selection) and the count; the caller's list has room
-    // for CAP keys.
+    // Collective: every held key (no selection), unordered, and the count; the caller's list
+    // has room for CAP keys.
     __device__ void dump_all(uint64_t* out, int* out_count) {
         const int n = settled_count();
         for (int i = tid; i < n; i += NT) out[i] = buf[i];
@@ -482,7 +481,8 @@ struct TopKSelector {
         sync();
     }
 
-    // Collective: the k largest held keys (an exact compaction first) and their count.
+    // Collective: the k largest held keys (an exact compaction first), unordered, and their
+    // count.
     __device__ void dump(int k, uint64_t* out, int* out_count) {
         compact(k, settled_count());
         const int n = settled_count();
