@@ -426,10 +426,12 @@ template <int kMergeThreads>
 __global__ void __launch_bounds__(kMergeThreads) topk_split_merge_kernel(
     int topk, int n_splits, int lists_per_group, const uint64_t* cand, int64_t row_stride,
     int64_t list_stride, const int* cand_cnt, int64_t cnt_row, int64_t cnt_list, int32_t* idx,
-    float* score, uint64_t* out_keys, int* out_cnt, int staged, unsigned* err) {
+    float* score, uint64_t* out_keys, int* out_cnt, int staged, int append_cap, unsigned* err) {
     // staged: the block's candidate slots are copied once into dynamic shared memory and
     // every pass reads them there (empty slots hold 0, which no rank key equals: its low
-    // word is 0xFFFFFFFF - position)
+    // word is 0xFFFFFFFF - position).  append_cap > 0 (with out_keys): the block appends its
+    // survivors to input row `row`'s list, out_keys[row * append_cap ...], at a cursor
+    // out_cnt[row] (zero before the launch), instead of writing list v of its own.
     extern __shared__ uint64_t stg[];
     __shared__ __align__(16) uint64_t xs[2 * kRankN];  // keys, then ranking scratch
     __shared__ unsigned hist[256];
@@ -607,6 +609,18 @@ __global__ void __launch_bounds__(kMergeThreads) topk_split_merge_kernel(
     });
     __syncthreads();
     if (tid == 0 && ctl[3] != n) atomicOr(err, kErrAssert);
+    if (out_keys && append_cap > 0) {  // the survivors appended to the row's list
+        if (tid == 0) ctl[0] = atomicAdd(&out_cnt[row], n);
+        __syncthreads();
+        const int at = ctl[0];
+        if (at + n > append_cap) {
+            if (tid == 0) atomicOr(err, kErrAssert);
+            return;
+        }
+        for (int i = tid; i < n; i += kMergeThreads)
+            out_keys[static_cast<int64_t>(row) * append_cap + at + i] = xs[i];
+        return;
+    }
     if (out_keys) {  // the survivors themselves, unordered
         for (int i = tid; i < n; i += kMergeThreads)
             out_keys[static_cast<int64_t>(v) * topk + i] = xs[i];
@@ -667,7 +681,7 @@ cudaError_t launch_topk_merge_strided(int rows, int topk, int n_lists, const uin
                                       int* out_cnt, unsigned* err, cudaStream_t st) {
     return launch_topk_merge_grouped(rows, topk, n_lists, n_lists, cand, row_stride, list_stride,
                                      cand_cnt, cnt_row, cnt_list, idx, score, out_keys, out_cnt,
-                                     err, st);
+                                     err, st, 0);
 }
 
 cudaError_t launch_topk_merge_grouped(int rows, int topk, int n_lists, int lists_per_group,
@@ -675,7 +689,7 @@ cudaError_t launch_topk_merge_grouped(int rows, int topk, int n_lists, int lists
                                       int64_t list_stride, const int* cand_cnt, int64_t cnt_row,
                                       int64_t cnt_list, int32_t* idx, float* score,
                                       uint64_t* out_keys, int* out_cnt, unsigned* err,
-                                      cudaStream_t st) {
+                                      cudaStream_t st, int append_cap) {
     if (rows == 0) return cudaSuccess;
     if (n_lists < 1 || n_lists > kMaxSplits || lists_per_group < 1) return cudaErrorInvalidValue;
     const int groups = (n_lists + lists_per_group - 1) / lists_per_group;
@@ -696,11 +710,11 @@ cudaError_t launch_topk_merge_grouped(int rows, int topk, int n_lists, int lists
         }
         topk_split_merge_kernel<1024><<<static_cast<int>(blocks), 1024, staged ? stage : 0, st>>>(
             topk, n_lists, lists_per_group, cand, row_stride, list_stride, cand_cnt, cnt_row,
-            cnt_list, idx, score, out_keys, out_cnt, staged, err);
+            cnt_list, idx, score, out_keys, out_cnt, staged, append_cap, err);
     } else {
         topk_split_merge_kernel<kRankThreads><<<static_cast<int>(blocks), kRankThreads, 0, st>>>(
             topk, n_lists, lists_per_group, cand, row_stride, list_stride, cand_cnt, cnt_row,
-            cnt_list, idx, score, out_keys, out_cnt, 0, err);
+            cnt_list, idx, score, out_keys, out_cnt, 0, append_cap, err);
     }
     note_launches(1);
     return cudaGetLastError();
@@ -731,6 +745,28 @@ cudaError_t launch_topk_merge_two_stage(int rows, int topk, int n_lists, const u
         return launch_topk_merge_strided(rows, topk, n_lists, cand, row_stride, list_stride,
                                          cand_cnt, cnt_row, cnt_list, idx, score, out_keys,
                                          out_cnt, err, st);
+    // Rank-ordered output: groups of lists merged by separate blocks, each appending its
+    // top k to one list per row, which the select-and-rank kernel finishes (it takes up to
+    // topk_rank_max_stride() keys a row) -- when at most that many group results per row
+    // fit, and each group's lists fit one block's staging.
+    const int groups_r = topk_rank_max_stride() / topk < 3 ? topk_rank_max_stride() / topk : 3;
+    const int g_r = groups_r > 0 ? (n_lists + groups_r - 1) / groups_r : n_lists + 1;
+    const size_t row_keys = static_cast<size_t>(groups_r) * topk;
+    const size_t need = rows * row_keys * sizeof(uint64_t) + rows * sizeof(int);
+    if (!out_keys && groups_r > 1 && g_r < n_lists &&
+        static_cast<size_t>(g_r) * topk * sizeof(uint64_t) <= kMaxStageBytes &&
+        need <= topk_merge_stage_bytes(rows, topk, n_lists)) {
+        uint64_t* rkeys = static_cast<uint64_t*>(stage);
+        int* rcnt = reinterpret_cast<int*>(rkeys + rows * row_keys);
+        cudaError_t e = cudaMemsetAsync(rcnt, 0, rows * sizeof(int), st);
+        if (e != cudaSuccess) return e;
+        e = launch_topk_merge_grouped(rows, topk, n_lists, g_r, cand, row_stride, list_stride,
+                                      cand_cnt, cnt_row, cnt_list, nullptr, nullptr, rkeys, rcnt,
+                                      err, st, static_cast<int>(row_keys));
+        if (e != cudaSuccess) return e;
+        return launch_topk_rank(rows, topk, static_cast<int>(row_keys), rkeys, rcnt, idx, score,
+                                err, st);
+    }
     const int groups = (n_lists + g - 1) / g;
     uint64_t* skeys = static_cast<uint64_t*>(stage);
     int* scnt = reinterpret_cast<int*>(skeys + static_cast<size_t>(rows) * groups * topk);

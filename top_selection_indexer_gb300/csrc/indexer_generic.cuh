@@ -54,19 +54,23 @@ cudaError_t launch_topk_merge_strided(int rows, int topk, int n_lists, const uin
 
 // The same with each row's lists split into groups of lists_per_group, one block per
 // (row, group): output row r * groups + g holds group g's top-k of row r as unordered keys
-// (out_keys required when there is more than one group).
+// (out_keys required when there is more than one group).  append_cap > 0: each group's
+// top-k is appended instead to row r's list out_keys[r * append_cap ...] at the cursor
+// out_cnt[r], which the caller zeroes first.
 cudaError_t launch_topk_merge_grouped(int rows, int topk, int n_lists, int lists_per_group,
                                       const uint64_t* cand, int64_t row_stride,
                                       int64_t list_stride, const int* cand_cnt, int64_t cnt_row,
                                       int64_t cnt_list, int32_t* idx, float* score,
                                       uint64_t* out_keys, int* out_cnt, unsigned* err,
-                                      cudaStream_t st);
+                                      cudaStream_t st, int append_cap = 0);
 
-// Merge in two stages when rows are few and lists many (decode): groups of about
-// sqrt(n_lists) lists are merged by separate blocks into `stage` (topk_merge_stage_bytes),
-// then each row's group results by one block; the top k of a union is the top k of the
-// union of its parts' top k, so the result equals the one-stage merge.  Falls back to one
-// stage when grouping does not pay or stage is null.
+// Merge in two stages when rows are few and lists many (decode): groups of lists are merged
+// by separate blocks into `stage` (topk_merge_stage_bytes), then each row's group results;
+// the top k of a union is the top k of the union of its parts' top k, so the result equals
+// the one-stage merge.  For rank-ordered output the groups (at most three, when each fits
+// one block's staging) append to one list per row and the select-and-rank kernel finishes;
+// otherwise about sqrt(n_lists) groups of about sqrt(n_lists) lists, then one merge block
+// per row.  Falls back to one stage when grouping does not pay or stage is null.
 int topk_merge_group_size(int rows, int n_lists);
 size_t topk_merge_stage_bytes(int rows, int topk, int n_lists);
 cudaError_t launch_topk_merge_two_stage(int rows, int topk, int n_lists, const uint64_t* cand,
