@@ -171,12 +171,12 @@ namespace {
 constexpr int kRankBucketBits = 11;
 constexpr int kRankBuckets = 1 << kRankBucketBits;
 constexpr int kRankBucketMax = 32;
-constexpr int kRankScanPer = kRankBuckets / kRankThreads;  // buckets per thread in the scan
 constexpr int kRankListIn = 24;  // list slots per thread of the wide form: 6144 keys a row
-static_assert(kRankScanPer * kRankThreads == kRankBuckets, "scan layout");
 
-template <int IN>  // list slots per thread: a list holds at most IN * kRankThreads keys
-__global__ void __launch_bounds__(kRankThreads, IN <= 17 ? 4 : 3)
+// NT threads a block (256, or 1024 for few rows: shorter latency per row); IN list slots per
+// thread: a list holds at most IN * NT keys.
+template <int NT, int IN>
+__global__ void __launch_bounds__(NT, NT > NT ? 1 : IN <= 17 ? 4 : 3)
     topk_rank_kernel(int topk, int stride, const uint64_t* cand, const int* cand_cnt,
                      int32_t* idx, float* score, unsigned* err) {
     // xs: the kept buckets' keys (at most k - 1 + kRankBucketMax), then the ranked keys; the
@@ -188,15 +188,17 @@ __global__ void __launch_bounds__(kRankThreads, IN <= 17 ? 4 : 3)
     unsigned* cnt = reinterpret_cast<unsigned*>(rank_smem + 2 * kRankN + kRankBucketMax);
     unsigned* fill = cnt + kRankBuckets;
     __shared__ unsigned long long rng[2];
-    __shared__ unsigned wsum[kRankThreads / 32];
+    constexpr int kScanPer = kRankBuckets / NT;  // buckets per thread in the scan
+    static_assert(kScanPer * NT == kRankBuckets, "scan layout");
+    __shared__ unsigned wsum[NT / 32];
     __shared__ int ctl[4];  // big bucket; radix select: bin, keys above it, keys in it
     const int row = blockIdx.x;
     const int t = threadIdx.x;
     const int lane = t & 31, wid = t >> 5;
     int n = cand_cnt[row];
-    if (n < 0 || n > stride || n > IN * kRankThreads) {
+    if (n < 0 || n > stride || n > IN * NT) {
         if (t == 0) atomicOr(err, kErrAssert);
-        n = n < 0 ? 0 : (stride < IN * kRankThreads ? stride : IN * kRankThreads);
+        n = n < 0 ? 0 : (stride < IN * NT ? stride : IN * NT);
     }
     const int n_out = n < topk ? n : topk;
     const uint64_t* c = cand + static_cast<int64_t>(row) * stride;
@@ -207,14 +209,14 @@ __global__ void __launch_bounds__(kRankThreads, IN <= 17 ? 4 : 3)
     uint64_t hi = 0ull, lo = ~0ull;
 #pragma unroll
     for (int j = 0; j < IN; ++j) {
-        const int i = t + kRankThreads * j;
+        const int i = t + NT * j;
         x[j] = i < n ? c[i] : 0ull;
         if (i < n) {
             hi = x[j] > hi ? x[j] : hi;
             lo = x[j] < lo ? x[j] : lo;
         }
     }
-    for (int i = t; i < kRankBuckets; i += kRankThreads) {
+    for (int i = t; i < kRankBuckets; i += NT) {
         cnt[i] = 0u;
         fill[i] = 0u;
     }
@@ -247,14 +249,14 @@ __global__ void __launch_bounds__(kRankThreads, IN <= 17 ? 4 : 3)
     };
 #pragma unroll
     for (int j = 0; j < IN; ++j)
-        if (t + kRankThreads * j < n) atomicAdd(&cnt[bucket(x[j])], 1u);
+        if (t + NT * j < n) atomicAdd(&cnt[bucket(x[j])], 1u);
     __syncthreads();
-    // exclusive scan of the counts: thread t owns buckets kRankScanPer t .. + kRankScanPer - 1
-    unsigned v[kRankScanPer];
+    // exclusive scan of the counts: thread t owns buckets kScanPer t .. + kScanPer - 1
+    unsigned v[kScanPer];
     unsigned own = 0u;
 #pragma unroll
-    for (int j = 0; j < kRankScanPer; ++j) {
-        v[j] = cnt[kRankScanPer * t + j];
+    for (int j = 0; j < kScanPer; ++j) {
+        v[j] = cnt[kScanPer * t + j];
         own += v[j];
     }
     unsigned incl = own;
@@ -271,8 +273,8 @@ __global__ void __launch_bounds__(kRankThreads, IN <= 17 ? 4 : 3)
         unsigned run = base + incl - own;
         bool big = false;
 #pragma unroll
-        for (int j = 0; j < kRankScanPer; ++j) {
-            cnt[kRankScanPer * t + j] = run;  // first rank of the bucket
+        for (int j = 0; j < kScanPer; ++j) {
+            cnt[kScanPer * t + j] = run;  // first rank of the bucket
             // a kept bucket (first rank below k) must be small enough to count in
             big |= run < static_cast<unsigned>(topk) && v[j] > static_cast<unsigned>(kRankBucketMax);
             run += v[j];
@@ -284,7 +286,7 @@ __global__ void __launch_bounds__(kRankThreads, IN <= 17 ? 4 : 3)
         // scatter the kept buckets' keys into bucket order
 #pragma unroll
         for (int j = 0; j < IN; ++j) {
-            if (t + kRankThreads * j < n) {
+            if (t + NT * j < n) {
                 const unsigned b = bucket(x[j]);
                 const unsigned first = cnt[b];
                 if (first < static_cast<unsigned>(topk)) xs[first + atomicAdd(&fill[b], 1u)] = x[j];
@@ -297,7 +299,7 @@ __global__ void __launch_bounds__(kRankThreads, IN <= 17 ? 4 : 3)
         uint64_t* ranked = xs + kRankN + kRankBucketMax;
 #pragma unroll
         for (int j = 0; j < IN; ++j) {
-            if (t + kRankThreads * j < n) {
+            if (t + NT * j < n) {
                 const unsigned b = bucket(x[j]);
                 const unsigned first = cnt[b];
                 if (first < static_cast<unsigned>(topk)) {
@@ -309,7 +311,7 @@ __global__ void __launch_bounds__(kRankThreads, IN <= 17 ? 4 : 3)
             }
         }
         __syncthreads();
-        for (int r = t; r < topk; r += kRankThreads) {
+        for (int r = t; r < topk; r += NT) {
             const bool real = r < n_out;
             const uint64_t y = real ? ranked[r] : 0ull;
             io[r] = real ? key_position(y) : -1;
@@ -336,7 +338,7 @@ __global__ void __launch_bounds__(kRankThreads, IN <= 17 ? 4 : 3)
             const unsigned dmask = (1u << width) - 1u;
 #pragma unroll
             for (int j = 0; j < IN; ++j)
-                if (t + kRankThreads * j < n && (x[j] & hmask) == prefix)
+                if (t + NT * j < n && (x[j] & hmask) == prefix)
                     atomicAdd(&hist[static_cast<unsigned>(x[j] >> sh) & dmask], 1u);
             __syncthreads();
             if (t < 32) {
@@ -389,12 +391,12 @@ __global__ void __launch_bounds__(kRankThreads, IN <= 17 ? 4 : 3)
         }
     }
     // the (at most k) kept keys into xs[0 .. n_out), the rest of the first kRankN slots 0
-    for (int i = t; i < kRankN; i += kRankThreads) xs[i] = 0ull;
+    for (int i = t; i < kRankN; i += NT) xs[i] = 0ull;
     if (t == 0) ctl[2] = 0;
     __syncthreads();
 #pragma unroll
     for (int j = 0; j < IN; ++j) {
-        const bool keep = t + kRankThreads * j < n && x[j] >= prefix;
+        const bool keep = t + NT * j < n && x[j] >= prefix;
         const unsigned m = __ballot_sync(kFull, keep);
         if (m) {
             int at = 0;
@@ -406,7 +408,7 @@ __global__ void __launch_bounds__(kRankThreads, IN <= 17 ? 4 : 3)
     }
     __syncthreads();
     if (t == 0 && ctl[2] != n_out) atomicOr(err, kErrAssert);
-    rank_merge_write(xs, xs + kRankN, n_out, topk, io, so, t, 1);
+    if (t < kRankThreads) rank_merge_write(xs, xs + kRankN, n_out, topk, io, so, t, 1);
 }
 
 // ------------------------------------------------------------------- split merge
@@ -638,14 +640,14 @@ int topk_rank_max_stride() { return kRankListIn * kRankThreads; }
 
 constexpr int kRankSmemBytes = (2 * kRankN + kRankBucketMax) * 8 + 2 * kRankBuckets * 4;
 
-template <int IN>
+template <int NT, int IN>
 cudaError_t rank_launch(int rows, int topk, int stride, const uint64_t* cand, const int* cand_cnt,
                         int32_t* idx, float* score, unsigned* err, cudaStream_t st) {
     static cudaError_t attr = cudaFuncSetAttribute(
-        topk_rank_kernel<IN>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRankSmemBytes);
+        topk_rank_kernel<NT, IN>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRankSmemBytes);
     if (attr != cudaSuccess) return attr;
-    topk_rank_kernel<IN><<<rows, kRankThreads, kRankSmemBytes, st>>>(topk, stride, cand,
-                                                                     cand_cnt, idx, score, err);
+    topk_rank_kernel<NT, IN><<<rows, NT, kRankSmemBytes, st>>>(topk, stride, cand, cand_cnt, idx,
+                                                              score, err);
     return cudaSuccess;
 }
 
@@ -654,13 +656,23 @@ cudaError_t launch_topk_rank(int rows, int topk, int stride, const uint64_t* can
                              cudaStream_t st) {
     if (rows == 0) return cudaSuccess;
     if (stride < topk || stride > topk_rank_max_stride()) return cudaErrorInvalidValue;
-    // the fewest list slots per thread that hold the stride (registers: blocks per SM)
+    // Few rows (decode): one wide block per row, the row's latency is the call's.  Else
+    // 256 threads and the fewest list slots per thread that hold the stride (registers:
+    // blocks per SM).
+    constexpr int kWide = 1024;
     const cudaError_t e =
-        stride <= kRankN ? rank_launch<kRankPer>(rows, topk, stride, cand, cand_cnt, idx, score,
-                                                 err, st)
+        rows < 152 ? (stride <= 2 * kWide
+                          ? rank_launch<kWide, 2>(rows, topk, stride, cand, cand_cnt, idx, score,
+                                                  err, st)
+                          : rank_launch<kWide, kRankListIn * kRankThreads / kWide>(
+                                rows, topk, stride, cand, cand_cnt, idx, score, err, st))
+        : stride <= kRankN ? rank_launch<kRankThreads, kRankPer>(rows, topk, stride, cand,
+                                                                 cand_cnt, idx, score, err, st)
         : stride <= 17 * kRankThreads
-            ? rank_launch<17>(rows, topk, stride, cand, cand_cnt, idx, score, err, st)
-            : rank_launch<kRankListIn>(rows, topk, stride, cand, cand_cnt, idx, score, err, st);
+            ? rank_launch<kRankThreads, 17>(rows, topk, stride, cand, cand_cnt, idx, score, err,
+                                            st)
+            : rank_launch<kRankThreads, kRankListIn>(rows, topk, stride, cand, cand_cnt, idx,
+                                                     score, err, st);
     if (e != cudaSuccess) return e;
     note_launches(1);
     return cudaGetLastError();
