@@ -24,9 +24,9 @@
 // Roles of one persistent CTA (512 threads):
 //   warps 0..3    softmax (heads 16 w .. 16 w + 15, four threads per head, 16 keys each)
 //                 and the row epilogue (O^T's value dims); thread 0 also loads Q by TMA
-//   warp 4        TMEM allocator + issuer of the S products (one thread)
-//   warp 5        issuer of the P.V products (one thread): the two streams of tcgen05 work
-//                 wait on different inputs, so neither holds up the other
+//   warp 4        TMEM allocator + issuer of the S products (lane 0 issues)
+//   warp 5        issuer of the P.V products (lane 0 issues): the two streams of tcgen05
+//                 work wait on different inputs, so neither holds up the other
 //   warps 6..15   gather: 16-byte cp.async of the selected latent rows into the 128-byte-
 //                 swizzled chunks of a half-tile buffer, one mbarrier per buffer
 // Few rows (decode): a row's half-tiles are split over CTAs and the unnormalised partials
@@ -180,10 +180,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == kMmaWarp || warp == kPvWarp) {
         // ------------------------------------------------------------ MMA issuers
-        // Two threads issue tcgen05 work: warp 4 the S products as key half-tiles land,
-        // warp 5 the P.V products as the softmax finishes them, so neither waits on the
-        // other's inputs (each commits only its own barriers).
-        if (lane == 0 && warp == kMmaWarp) {
+        // Two warps issue tcgen05 work: warp 4 the S products as key half-tiles land, warp 5
+        // the P.V products as the softmax finishes them, so neither waits on the other's
+        // inputs (each commits only its own barriers).  The whole warp runs the loop (its
+        // descriptors stay warp-uniform); lane 0 issues every MMA and commit.
+        const bool leader = lane == 0;
+        if (warp == kMmaWarp) {
             int it = 0, un = 0;
             for (int u = blockIdx.x; u < p.n_units; u += gridDim.x, ++un) {
                 const Work W = work_of(p, u);
@@ -203,19 +205,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int c = 0; c < kChunks; ++c) {
 #pragma unroll
                             for (int kk = 0; kk < 4; ++kk)
-                                tc::mma_bf16(tmem + kColS + 64 * b,
-                                             da0 + ((c * kQChunkBytes + kk * 32) >> 4),
-                                             db0 + ((c * kChunkBytes + kk * 32) >> 4), kIdescS,
-                                             (c | kk) ? 1u : 0u);
+                                if (leader)
+                                    tc::mma_bf16(tmem + kColS + 64 * b,
+                                                 da0 + ((c * kQChunkBytes + kk * 32) >> 4),
+                                                 db0 + ((c * kChunkBytes + kk * 32) >> 4),
+                                                 kIdescS, (c | kk) ? 1u : 0u);
                         }
                     }
-                    tc::mma_commit(&sm.s_full[b]);
+                    if (leader) tc::mma_commit(&sm.s_full[b]);
                 }
             }
-            tc::mma_commit(&sm.done[0]);
+            if (leader) tc::mma_commit(&sm.done[0]);
             if (!tc::mbar_wait(&sm.done[0], 0, abort, p.err))
                 tc::mbar_drain(&sm.done[0], 0);  // issued MMAs finish before TMEM is freed
-        } else if (lane == 0) {
+        } else {
             int it = 0, un = 0;
             for (int u = blockIdx.x; u < p.n_units; u += gridDim.x, ++un) {
                 const Work W = work_of(p, u);
@@ -234,18 +237,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int m = 0; m < 4; ++m) {
 #pragma unroll
                             for (int kk = 0; kk < 4; ++kk)
-                                tc::mma_bf16(tmem + kColO + 64 * m,
-                                             da0 + ((2 * m * kChunkBytes + kk * 2048) >> 4),
-                                             db0 + ((kk * 32) >> 4), kIdescO,
-                                             kk == 0 ? first : 1u);
+                                if (leader)
+                                    tc::mma_bf16(tmem + kColO + 64 * m,
+                                                 da0 + ((2 * m * kChunkBytes + kk * 2048) >> 4),
+                                                 db0 + ((kk * 32) >> 4), kIdescO,
+                                                 kk == 0 ? first : 1u);
                         }
                     }
-                    tc::mma_commit(&sm.empty[b]);
-                    tc::mma_commit(&sm.pv_done);
+                    if (leader) tc::mma_commit(&sm.empty[b]);
+                    if (leader) tc::mma_commit(&sm.pv_done);
                 }
-                tc::mma_commit(&sm.o_full);
+                if (leader) tc::mma_commit(&sm.o_full);
             }
-            tc::mma_commit(&sm.done[1]);
+            if (leader) tc::mma_commit(&sm.done[1]);
             if (!tc::mbar_wait(&sm.done[1], 0, abort, p.err))
                 tc::mbar_drain(&sm.done[1], 0);  // issued MMAs finish before TMEM is freed
         }

@@ -34,7 +34,7 @@
 // Roles of one persistent CTA (608 threads):
 //   warp 0       TMA producer: Q tile of the unit, key tiles into a ring of stages, the
 //                next unit's query rows and gate weights prefetched into L2
-//   warps 1, 18  MMA issuers, one thread each: warp 1 the even tiles, warp 18 the odd ones
+//   warps 1, 18  MMA issuers (lane 0 issues): warp 1 the even tiles, warp 18 the odd ones
 //                (512 TMEM columns: 512 / N accumulators, so the MMA runs that many tiles
 //                ahead; two issuers overlap each other's barrier waits).  Warp 1 also
 //                allocates TMEM.
@@ -408,7 +408,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1 || warp == kMmaWarp2) {
         // ------------------------------------------------------------ MMA issuers
-        if (lane == 0) {
+        // The whole warp runs the loop (its descriptors stay warp-uniform); lane 0 issues
+        // every MMA and commit.
+        const bool leader = lane == 0;
+        {
             const int mine = warp == 1 ? 0 : 1;  // tiles t of the CTA with t % 2 == mine
             int s = 0, a = 0, t = 0;
             uint32_t ph = 0, aph = 0;  // phases of ring slot s and accumulator a
@@ -447,15 +450,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 const uint64_t da = a0 + ((c * kChunkBytes + k * 32) >> 4);
                                 const uint64_t db = bdesc + ((c * L::kQChunkBytes + k * 32) >> 4);
                                 const uint32_t accum = (c | k) ? 1u : 0u;
-                                if (QK == TSI_E4M3)
-                                    tc::mma_f8(d, da, db, L::kIdesc, accum);
-                                else
-                                    tc::mma_bf16(d, da, db, L::kIdesc, accum);
+                                if (leader) {
+                                    if (QK == TSI_E4M3)
+                                        tc::mma_f8(d, da, db, L::kIdesc, accum);
+                                    else
+                                        tc::mma_bf16(d, da, db, L::kIdesc, accum);
+                                }
                             }
                         }
                     }
-                    tc::mma_commit(&empty[s]);
-                    tc::mma_commit(&tfull[a]);
+                    if (leader) tc::mma_commit(&empty[s]);
+                    if (leader) tc::mma_commit(&tfull[a]);
                     if (++s == L::kStages) {
                         s = 0;
                         ph ^= 1;
@@ -465,10 +470,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         aph ^= 1;
                     }
                 }
-                tc::mma_commit(qempty);
+                if (leader) tc::mma_commit(qempty);
             }
             // every MMA issued by both threads has finished before TMEM is released
-            tc::mma_commit(done);
+            if (leader) tc::mma_commit(done);
             if (!tc::mbar_wait(done, 0, abort, p.err)) tc::mbar_drain(done, 0);
         }
     } else {
