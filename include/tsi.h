@@ -57,11 +57,13 @@ typedef enum { TSI_F32 = 0, TSI_BF16 = 1, TSI_E4M3 = 2 } tsi_dtype;
 
 /*
  * Workspace bytes needed by tsi_indexer_topk for these sizes (0 when none is needed).
- *   - Tensor-core path: candidate lists of 8-byte keys, topk per row (and per key split
- *     when rows are few and long), plus a count per list.  With several query rows per
- *     sequence and one key range per row, also the per-row admission thresholds, a list of
- *     unit indices (4 B per 4 rows of e4m3, per 2 rows of bf16) and every 32nd key row of
- *     the cache (B x ceil(S / 32) rows).  At B = 1, T = S = 131072, k = 2048: ~2.1 GB.
+ *   - Tensor-core path: candidate lists of 8-byte keys plus a count per list.  With
+ *     several query rows per sequence and one key range per row: one list per row of the
+ *     row selector's capacity (4352 keys for e4m3, 5888 for bf16: the keys at or above the
+ *     row's threshold, which the ranking kernel selects from), the per-row admission
+ *     thresholds, a list of unit indices (4 B per 4 rows of e4m3, per 2 rows of bf16) and
+ *     every 32nd key row of the cache (B x ceil(S / 32) rows); at B = 1, T = S = 131072:
+ *     ~4.6 GB.  Otherwise topk keys per row and key split.
  *   - Decode-sized requests (few rows, long caches) on either path: the per-split lists and
  *     merge staging space.
  */
@@ -88,10 +90,10 @@ size_t tsi_indexer_topk_workspace(int B, int T, int S, int H_I, int d_I, int top
  *   score  [B, T, topk] float (out, may be NULL)  the fp32 score of each idx entry,
  *          -inf for padding.
  *
- * Scores are accumulated in fp32 (tensor cores for BF16/E4M3 with H_I = 64,
- * d_I = 128; CUDA cores otherwise).  1 <= topk <= TSI_MAX_TOPK, d_I <= 256,
- * H_I <= 128.  Pointers must be 16-byte aligned.  Requires
- * workspace_bytes >= tsi_indexer_topk_workspace(...).
+ * Scores are accumulated in fp32 (tensor cores for BF16/E4M3 with H_I = 64, d_I = 128,
+ * except BF16 with one query per sequence, T = 1; CUDA cores otherwise).
+ * 1 <= topk <= TSI_MAX_TOPK, d_I <= 256, H_I <= 128.  Pointers must be 16-byte aligned.
+ * Requires workspace_bytes >= tsi_indexer_topk_workspace(...).
  */
 tsi_status tsi_indexer_topk(const void* qI, const void* kI, const void* w, int qk_dtype,
                             int w_dtype, int B, int T, int S, int H_I, int d_I, int topk,
@@ -354,7 +356,9 @@ tsi_status tsi_device_status(void* stream);
 const char* tsi_last_error(void);
 
 /* Which kernels serve a shape: 1 = tensor-core (tcgen05) path, 0 = CUDA-core path,
- * -1 = unsupported.  v_from_k != 0 means the value is the first Dv dims of the key. */
+ * -1 = unsupported.  For the indexer this is the path of requests with several queries
+ * per sequence (T > 1); BF16 requests with T = 1 take the CUDA-core path.  v_from_k != 0
+ * means the value is the first Dv dims of the key. */
 int tsi_indexer_topk_path(int qk_dtype, int H_I, int d_I);
 int tsi_sparse_attn_path(int H, int Hkv, int Dqk, int Dv, int v_from_k);
 
