@@ -163,8 +163,9 @@ namespace {
 // and an exclusive scan (largest bucket first) give each bucket its first rank.  A bucket whose
 // first rank is k or more holds no key of the result and is skipped; the keys of the
 // others are scattered into their buckets, and each key's rank is its bucket's first rank
-// plus the number of larger keys in its bucket.  Rank keys are distinct, so the ranks are
-// a permutation.  A row with more than kRankBucketMax keys in one of the buckets it keeps
+// plus the number of larger keys in its bucket.  The ranking walks the scattered keys in
+// bucket order, so the threads of a warp mostly count within one bucket: equal loop lengths,
+// broadcast reads.  Rank keys are distinct, so the ranks are a permutation.  A row with more than kRankBucketMax keys in one of the buckets it keeps
 // (many equal scores, or keys crowded below an outlier) takes the general path instead: an
 // exact MSD radix select of its k best (when it holds more than k), then the bitonic sorts
 // and merges of rank_merge_write, so the work per key stays bounded.
@@ -191,7 +192,8 @@ __global__ void __launch_bounds__(NT, NT > NT ? 1 : IN <= 17 ? 4 : 3)
     constexpr int kScanPer = kRankBuckets / NT;  // buckets per thread in the scan
     static_assert(kScanPer * NT == kRankBuckets, "scan layout");
     __shared__ unsigned wsum[NT / 32];
-    __shared__ int ctl[4];  // big bucket; radix select: bin, keys above it, keys in it
+    // big bucket, keys in the kept buckets; radix select: bin, keys above it, keys in it
+    __shared__ int ctl[4];
     const int row = blockIdx.x;
     const int t = threadIdx.x;
     const int lane = t & 31, wid = t >> 5;
@@ -224,6 +226,7 @@ __global__ void __launch_bounds__(NT, NT > NT ? 1 : IN <= 17 ? 4 : 3)
         rng[0] = 0ull;
         rng[1] = ~0ull;
         ctl[0] = 0;
+        ctl[1] = n;  // every bucket is kept when the row holds at most k keys
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -277,6 +280,9 @@ __global__ void __launch_bounds__(NT, NT > NT ? 1 : IN <= 17 ? 4 : 3)
             cnt[kScanPer * t + j] = run;  // first rank of the bucket
             // a kept bucket (first rank below k) must be small enough to count in
             big |= run < static_cast<unsigned>(topk) && v[j] > static_cast<unsigned>(kRankBucketMax);
+            // the bucket holding rank k - 1 ends the kept buckets' keys
+            if (run < static_cast<unsigned>(topk) && run + v[j] >= static_cast<unsigned>(topk))
+                ctl[1] = static_cast<int>(run + v[j]);
             run += v[j];
         }
         if (big) ctl[0] = 1;
@@ -293,22 +299,19 @@ __global__ void __launch_bounds__(NT, NT > NT ? 1 : IN <= 17 ? 4 : 3)
             }
         }
         __syncthreads();
-        // rank = first rank of the bucket + larger keys in the bucket; the result goes to
-        // the second part of xs, then out in rank order (consecutive threads, consecutive
-        // ranks)
+        // rank = first rank of the bucket + larger keys in the bucket, for the kept buckets'
+        // keys xs[0, kept) in bucket order; the result goes to the second part of xs, then
+        // out in rank order (consecutive threads, consecutive ranks)
         uint64_t* ranked = xs + kRankN + kRankBucketMax;
-#pragma unroll
-        for (int j = 0; j < IN; ++j) {
-            if (t + NT * j < n) {
-                const unsigned b = bucket(x[j]);
-                const unsigned first = cnt[b];
-                if (first < static_cast<unsigned>(topk)) {
-                    const unsigned m = fill[b];
-                    unsigned r = first;
-                    for (unsigned q = first; q < first + m; ++q) r += xs[q] > x[j] ? 1u : 0u;
-                    if (r < static_cast<unsigned>(topk)) ranked[r] = x[j];
-                }
-            }
+        const int kept = ctl[1];
+        for (int i = t; i < kept; i += NT) {
+            const uint64_t y = xs[i];
+            const unsigned b = bucket(y);
+            const unsigned first = cnt[b];
+            const unsigned m = fill[b];
+            unsigned r = first;
+            for (unsigned q = first; q < first + m; ++q) r += xs[q] > y ? 1u : 0u;
+            if (r < static_cast<unsigned>(topk)) ranked[r] = y;
         }
         __syncthreads();
         for (int r = t; r < topk; r += NT) {
