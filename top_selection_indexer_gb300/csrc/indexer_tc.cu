@@ -582,6 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float out = -__int_as_float(0x7f800000);
                     const int64_t n_full = n_row << p.key_shift;  // upper bound of the row's keys
                     if (!lost && held > p.topk && n_full > L::kCap) {
+                        if constexpr (kMode == kModeCapped) sel.keys_from_raw(held);
                         sel.compact(p.topk, held, true, 0, false);
                         out = score_floor(*reinterpret_cast<volatile uint64_t*>(sel.thr));
                     }
@@ -600,10 +601,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // the row's (chunk's) held keys, or its k best, unordered; the
                         // ranking or merge kernel takes them from there
                         const int64_t slot = row * p.n_chunks + U.chunk;
-                        if (p.cand_stride)
+                        if constexpr (kMode == kModeCapped) {  // the buffer holds raw pairs
+                            if (p.cand_stride) {
+                                sel.dump_all_raw(p.cand + slot * p.cand_stride, p.cand_cnt + slot);
+                            } else {
+                                sel.keys_from_raw(held);
+                                sel.dump(p.topk, p.cand + slot * p.topk, p.cand_cnt + slot);
+                            }
+                        } else if (p.cand_stride) {
                             sel.dump_all(p.cand + slot * p.cand_stride, p.cand_cnt + slot);
-                        else
+                        } else {
                             sel.dump(p.topk, p.cand + slot * p.topk, p.cand_cnt + slot);
+                        }
                     }
                 }
             }

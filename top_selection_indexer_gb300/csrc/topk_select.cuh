@@ -34,6 +34,17 @@ __device__ __forceinline__ uint64_t make_key(float score, uint32_t s) {
            static_cast<uint64_t>(0xFFFFFFFFu - s);
 }
 
+// A candidate before it becomes a key: the score's bits above the position.  The capped
+// offers store these (one move, no arithmetic on the scoring path) and the buffer is turned
+// into keys once, when the unit ends.
+__device__ __forceinline__ uint64_t raw_pair(float score, uint32_t s) {
+    return (static_cast<uint64_t>(__float_as_uint(score)) << 32) | static_cast<uint64_t>(s);
+}
+
+__device__ __forceinline__ uint64_t key_of_raw(uint64_t r) {
+    return make_key(__uint_as_float(static_cast<uint32_t>(r >> 32)), static_cast<uint32_t>(r));
+}
+
 // The smallest fp32 score whose keys can reach `threshold`: a finite score x has
 // make_key(x, s) >= threshold for some s exactly when x >= score_floor(threshold) (the
 // order is monotone in the score, -0.0 and +0.0 alike).  Thresholds whose score word lies
@@ -225,11 +236,12 @@ struct TopKSelector {
         offer2_thr(c0, make_key(s0, pos0), c1, make_key(s1, pos1), threshold);
     }
 
-    // Warp-collective: append the keys of two scored positions per thread whose score
-    // reaches `floor` (every key of such a score is at least the threshold the selector was
-    // reset to), with no room check: slots past CAP are not written and the count runs on
-    // beyond CAP, so a caller that finds settled_count() > CAP knows keys were lost.  One
-    // shared-memory reservation per warp.
+    // Warp-collective: append two scored positions per thread whose score reaches `floor`
+    // (every key of such a score is at least the threshold the selector was reset to), with
+    // no room check: slots past CAP are not written and the count runs on beyond CAP, so a
+    // caller that finds settled_count() > CAP knows keys were lost.  One shared-memory
+    // reservation per warp.  The buffer receives raw_pair()s, not keys: keys_from_raw() or
+    // dump_all_raw() converts them before anything compares them.
     __device__ __forceinline__ void offer2_capped(bool ok0, float s0, uint32_t pos0, bool ok1,
                                                   float s1, uint32_t pos1, float floor) {
         const bool t0 = ok0 && s0 >= floor;
@@ -245,8 +257,15 @@ struct TopKSelector {
         const unsigned below = (1u << lane) - 1u;
         const int p0 = base + __popc(m0 & below);
         const int p1 = base + n0 + __popc(m1 & below);
-        if (t0 && p0 < CAP) buf[p0] = make_key(s0, pos0);
-        if (t1 && p1 < CAP) buf[p1] = make_key(s1, pos1);
+        if (t0 && p0 < CAP) buf[p0] = raw_pair(s0, pos0);
+        if (t1 && p1 < CAP) buf[p1] = raw_pair(s1, pos1);
+    }
+
+    // Collective: turn the first n (at most CAP) held raw_pair()s into keys in place.
+    __device__ void keys_from_raw(int n) {
+        if (n > CAP) n = CAP;
+        for (int i = tid; i < n; i += NT) buf[i] = key_of_raw(buf[i]);
+        sync();
     }
 
     // Collective: drop held keys that cannot be among the k largest (no-op when n <= k).
@@ -477,6 +496,14 @@ struct TopKSelector {
     __device__ void dump_all(uint64_t* out, int* out_count) {
         const int n = settled_count();
         for (int i = tid; i < n; i += NT) out[i] = buf[i];
+        if (tid == 0) *out_count = n;
+        sync();
+    }
+
+    // Collective: dump_all of a buffer of raw_pair()s, each turned into its key on the way.
+    __device__ void dump_all_raw(uint64_t* out, int* out_count) {
+        const int n = settled_count();
+        for (int i = tid; i < n; i += NT) out[i] = key_of_raw(buf[i]);
         if (tid == 0) *out_count = n;
         sync();
     }
