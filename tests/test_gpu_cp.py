@@ -72,3 +72,24 @@ def test_merge_of_one_list_ranks_it(cuda_lib):
     ref = cuda_lib.indexer_topk(qI, kI, w, 64)
     cuda_lib.device_status()
     assert torch.equal(idx, ref.view(-1, 64))
+
+
+def test_signed_gates_shards_merge_to_the_whole_cache(cuda_lib):
+    # gate weights of both signs (powers of two): negative scores through the shards' capped
+    # passes, whose raw (score, position) pairs become rank keys before each unit's exact
+    # selection; rows of up to 7000 keys per shard take sampled thresholds
+    B, T, S, topk = 1, 2000, 12000, 2048
+    qI = draw((B, T, 64, 128), "int8", "e4m3", 7101, "cuda", 128)
+    kI = draw((B, S, 128), "int8", "e4m3", 7102, "cuda", 128)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(7103)
+    sign = torch.randint(0, 2, (B, T, 64), generator=g, device="cuda").to(torch.float32) * 2 - 1
+    w = (draw((B, T, 64), "pow2", "f32", 7104, "cuda") * sign).to(torch.bfloat16)
+    idx_m, sc_m = _sharded(cuda_lib, qI, kI, w, topk, (5000,))
+    idx_w, sc_w = cuda_lib.indexer_topk(qI, kI, w, topk, want_score=True)
+    cuda_lib.device_status()
+    assert torch.equal(idx_m.view(-1, topk), idx_w.view(-1, topk))
+    assert torch.equal(sc_m.view(-1, topk).view(torch.int32), sc_w.view(-1, topk).view(torch.int32))
+    rows = [0, 1, 777, 1500, T - 2, T - 1]
+    ref_idx, _ = oracle.indexer_topk(qI.cpu(), kI.cpu(), w.cpu(), topk, rows=rows)
+    assert np.array_equal(idx_m.view(-1, topk).cpu().numpy()[rows], np.asarray(ref_idx))

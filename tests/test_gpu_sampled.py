@@ -11,15 +11,17 @@ score (for k = 2048).  These inputs make that sample lie:
   is listed and done again from no threshold by the third launch;
 - half the rows of each four-row unit see the second pattern and half score every key 0
   (all ties): units that are redone hold rows that were complete;
-- every score equal (zero gate weights).
+- every score equal (zero gate weights);
+- gate weights of both signs, so that many scores (and some thresholds) are negative.
 
-Queries and gates are positive integers and a key row holds one integer value, so every
+In the first three, queries and gates are positive integers and a key row holds one
+integer value; the signed gates are powers of two over integer queries and keys.  Every
 score is exact in fp32 and the oracle's rows must be matched bit for bit.  The same kinds of
 input then go through the one-query-per-sequence (decode) path in e4m3, which has no sampled
 threshold: key chunks selected in the scoring kernel, merged per row.  A full-size
 L = 131072 integer-valued prefill checks sampled rows of the common path.  (Score equation
-and k: "GLM-5.2 技术报告速览", §IndexShare; the lower-index tie rule: BASELINE's reading of
-the deterministic top-k of "GLM-5: from Vibe Coding to Agentic Engineering" (Chinese
+and k: "GLM-5.2 技术报告速览", §IndexShare; the lower-index tie rule: the reading taken here
+of the deterministic top-k of "GLM-5: from Vibe Coding to Agentic Engineering" (Chinese
 translation), §3.2.)
 """
 import numpy as np
@@ -137,6 +139,29 @@ def test_full_size_prefill_integer_exact(cuda_lib):
 # ---- one query per sequence (decode, e4m3): no sampled threshold; each row's keys are split
 # into 19 chunks of 3200 keys that select in the scoring kernel's epilogue (their selectors
 # compact when every key is admitted), then the chunk lists are merged in two stages.
+def _signed_gates(shape, seed):
+    """Powers of two 2^-4 .. 1 with a random sign each: the score equation puts no sign on
+    the gate weights, and with signed ones many scores are negative."""
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    sign = torch.randint(0, 2, shape, generator=g, device="cuda").to(torch.float32) * 2 - 1
+    return (draw(shape, "pow2", "f32", seed + 1, "cuda") * sign).to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("qk", ["e4m3", "bf16"])
+def test_signed_gate_weights_integer_exact(cuda_lib, qk):
+    # negative scores through the sampled threshold, the raw (score, position) pairs the
+    # capped pass appends and their rank keys; every score is a multiple of 2^-4 below 2^20
+    # in magnitude, so fp32 holds it exactly in any order of summation
+    qI = draw((1, T, H, D), "int8", qk, 181, "cuda", D)
+    kI = draw((1, S, D), "int8", qk, 182, "cuda", D)
+    w = _signed_gates((1, T, H), 183)
+    idx = _check(cuda_lib, qI, kI, w, _rows())
+    idx2 = cuda_lib.indexer_topk(qI, kI, w, TOPK, two_pass=True)
+    cuda_lib.device_status()
+    assert torch.equal(idx, idx2.cpu())
+
+
 # Adversarial inputs like the ones above, exact against the oracle.  (bf16 requests of one
 # query per sequence take the CUDA-core path.)
 
@@ -212,6 +237,13 @@ def test_decode_random_integer_rows(cuda_lib, qk):
     qI = draw((BD, 1, H, D), "int8", qk, 161, "cuda", D)
     kI = draw((BD, SD, D), "int8", qk, 162, "cuda", D)
     w = draw((BD, 1, H), "pow2", "bf16", 163, "cuda", D)
+    _check_decode(cuda_lib, qI, kI, w, kv=[60000, 16384, 16385, 59001, 30000, 1, 2048, 45000])
+
+
+def test_decode_signed_gate_weights_integer_exact(cuda_lib):
+    qI = draw((BD, 1, H, D), "int8", "e4m3", 191, "cuda", D)
+    kI = draw((BD, SD, D), "int8", "e4m3", 192, "cuda", D)
+    w = _signed_gates((BD, 1, H), 193)
     _check_decode(cuda_lib, qI, kI, w, kv=[60000, 16384, 16385, 59001, 30000, 1, 2048, 45000])
 
 
