@@ -535,8 +535,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             // 128 i): tile i's key belongs to the row when 128 i < rest
             int64_t rest64 = limit - U.key_lo - off;
             const int rest = rest64 < 0 ? 0 : rest64 > (1 << 30) ? (1 << 30) : static_cast<int>(rest64);
-            // per round each warp scores two of its tiles and offers both keys at once
-            for (int i0 = 0; i0 < U.ntiles; i0 += 2 * L::kSubs) {
+            int i0 = 0;
+            if constexpr (kMode == kModeCapped && L::kSubs == 1) {
+                // Rounds whose two tiles hold only keys of the row, for every thread: no bounds
+                // checks (tile i is whole when (i + 1) * 128 <= limit - key_lo).
+                int64_t nf64 = (limit - U.key_lo) / kTileKeys;
+                const int n_full = nf64 < 0 ? 0 : nf64 > U.ntiles ? U.ntiles : static_cast<int>(nf64);
+                for (; i0 + 2 <= n_full; i0 += 2) {
+                    const unsigned acc_a = static_cast<unsigned>(acc_base + i0);
+                    const unsigned acc_b = acc_a + 1u;
+                    const int a_a = static_cast<int>(acc_a % L::kAccBufs);
+                    const int a_b = static_cast<int>(acc_b % L::kAccBufs);
+                    tc::mbar_wait_ready(&tfull[a_a], (acc_a / L::kAccBufs) & 1u, abort, p.err);
+                    const float s_a = tile_score<L::kN>(tmem, quad, r, a_a, tempty, wd);
+                    tc::mbar_wait_ready(&tfull[a_b], (acc_b / L::kAccBufs) & 1u, abort, p.err);
+                    const float s_b = tile_score<L::kN>(tmem, quad, r, a_b, tempty, wd);
+                    sel.offer2_capped(true, s_a, pos0 + static_cast<uint32_t>(i0 * kTileKeys),
+                                      true, s_b, pos0 + static_cast<uint32_t>((i0 + 1) * kTileKeys),
+                                      tau);
+                }
+            }
+            // per round each warp scores two of its tiles and offers both keys at once (the
+            // rest of the unit's tiles: bounds checked)
+            for (; i0 < U.ntiles; i0 += 2 * L::kSubs) {
                 const int ia = i0 + sub, ib = i0 + L::kSubs + sub;
                 float sc[2] = {0.f, 0.f};
 #pragma unroll
