@@ -206,8 +206,12 @@ __device__ __forceinline__ bool wait_fast(uint64_t* bar, uint32_t parity, bool p
 // Head-pair slots (of the eight in each 32-column load) whose ReLU runs on the ALU pipe as
 // a max with 0; the others run on the FMA pipe as x + |x| = 2 ReLU(x) (exact) against
 // halved gate weights.  Either way w * ReLU(x) is the same product, so the split only
-// balances the two pipes and never changes a score.
-constexpr int kAluSlots = 2;
+// balances the two pipes and never changes a score.  Two of eight for the four-row e4m3
+// units, one for the two-row bf16 units (N = 128), whose MMAs leave the epilogue more time.
+template <int N>
+constexpr int alu_slots() {
+    return N == 128 ? 1 : 2;
+}
 
 // Key lane (within the warp's 32 TMEM lanes) whose score tile_score returns to this
 // thread: lane 8 (T % 4) + T / 4 of thread T.
@@ -217,12 +221,13 @@ __device__ __forceinline__ int scored_lane(int lane) { return 8 * (lane & 3) + (
 // of a pair and halved where its ReLU is formed as x + |x|: slot j = 8 ch + 2 m + e holds
 // head 32 ch + 8 m + 2 (T % 4) + e.  (Halving a gate weight below 2^-125, a subnormal,
 // would drop its last bit; no gate weight is that small.)
+template <int N>
 __device__ __forceinline__ void load_gates(float2 (&wd)[16], const void* w, int64_t row_h0,
                                            int w_dtype, int lane) {
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
         const int ch = j >> 3, m = (j >> 1) & 3, e = j & 1;
-        const float f = (j & 7) < kAluSlots ? 1.f : 0.5f;
+        const float f = (j & 7) < alu_slots<N>() ? 1.f : 0.5f;
         const float g = f * load_elem(w, row_h0 + 32 * ch + 8 * m + 2 * (lane & 3) + e, w_dtype);
         wd[j] = make_float2(g, g);
     }
@@ -265,7 +270,7 @@ __device__ __forceinline__ float tile_score(uint32_t tmem, int quad, int r, int 
                     const int j = 8 * ch + 2 * m + e;
                     const float x = __uint_as_float(v[4 * m + e]);
                     const float y = __uint_as_float(v[4 * m + 2 + e]);
-                    const float2 rx = (j & 7) < kAluSlots
+                    const float2 rx = (j & 7) < alu_slots<N>()
                                           ? make_float2(fmaxf(x, 0.f), fmaxf(y, 0.f))
                                           : make_float2(__fadd_rn(x, fabsf(x)),
                                                         __fadd_rn(y, fabsf(y)));
@@ -502,7 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 n_row = pr >= 0 ? (pr >> p.key_shift) + 1 : 0;
                 if (n_row > p.S) n_row = p.S;
                 limit = n_row < U.key_hi ? n_row : U.key_hi;
-                load_gates(wd, p.w, row * 64, p.w_dtype, lane);
+                load_gates<L::kN>(wd, p.w, row * 64, p.w_dtype, lane);
             }
             // key of this thread's score in a tile
             const int off = quad * 32 + scored_lane(lane);
