@@ -80,7 +80,7 @@ struct Smem {
     uint64_t o_empty;
     uint64_t done[2];  // each MMA issuer's work complete
     float alpha[kHeads];  // rescale factors of a running-max refresh
-    float linv[kHeads];  // 1 / row sum, for the epilogue
+    alignas(16) float linv[kHeads];  // 1 / row sum, for the epilogue (read as float4)
     uint32_t tmem_slot;
     int abort;
 };
@@ -467,12 +467,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int i = 0; i < 32; ++i)
                             po[static_cast<int64_t>(i) * kDv] = __uint_as_float(o[i]);
                     } else {
+                        // the 32 factors first: read between the stores, each would wait for
+                        // its shared-memory load (the stores may alias it for the compiler)
+                        float li[32];
+#pragma unroll
+                        for (int i = 0; i < 32; i += 4) {
+                            const float4 v = *reinterpret_cast<const float4*>(&sm.linv[32 * half + i]);
+                            li[i] = v.x;
+                            li[i + 1] = v.y;
+                            li[i + 2] = v.z;
+                            li[i + 3] = v.w;
+                        }
                         __nv_bfloat16* out =
                             p.out + (static_cast<int64_t>(W.row) * kHeads + 32 * half) * kDv + d;
 #pragma unroll
                         for (int i = 0; i < 32; ++i)
-                            out[static_cast<int64_t>(i) * kDv] = __float2bfloat16_rn(
-                                __uint_as_float(o[i]) * sm.linv[32 * half + i]);
+                            out[static_cast<int64_t>(i) * kDv] =
+                                __float2bfloat16_rn(__uint_as_float(o[i]) * li[i]);
                     }
                 }
             }
