@@ -314,11 +314,23 @@ __global__ void __launch_bounds__(NT, NT > NT ? 1 : IN <= 17 ? 4 : 3)
             if (r < static_cast<unsigned>(topk)) ranked[r] = y;
         }
         __syncthreads();
-        for (int r = t; r < topk; r += NT) {
-            const bool real = r < n_out;
-            const uint64_t y = real ? ranked[r] : 0ull;
-            io[r] = real ? key_position(y) : -1;
-            if (so) so[r] = real ? key_score(y) : -__int_as_float(0x7f800000);
+        constexpr int kW = 4;  // ranks read ahead of the stores
+        for (int r0 = t; r0 < topk; r0 += kW * NT) {
+            uint64_t y[kW];
+#pragma unroll
+            for (int j = 0; j < kW; ++j) {
+                const int r = r0 + j * NT;
+                y[j] = r < n_out ? ranked[r] : 0ull;
+            }
+#pragma unroll
+            for (int j = 0; j < kW; ++j) {
+                const int r = r0 + j * NT;
+                if (r < topk) {
+                    const bool real = r < n_out;
+                    io[r] = real ? key_position(y[j]) : -1;
+                    if (so) so[r] = real ? key_score(y[j]) : -__int_as_float(0x7f800000);
+                }
+            }
         }
         return;
     }

@@ -501,9 +501,18 @@ struct TopKSelector {
     }
 
     // Collective: dump_all of a buffer of raw_pair()s, each turned into its key on the way.
+    // Four reads ahead of the stores: a read between them would wait on its own latency.
     __device__ void dump_all_raw(uint64_t* out, int* out_count) {
         const int n = settled_count();
-        for (int i = tid; i < n; i += NT) out[i] = key_of_raw(buf[i]);
+        constexpr int U = 4;
+        for (int b = tid; b < n; b += U * NT) {
+            uint64_t v[U];
+#pragma unroll
+            for (int j = 0; j < U; ++j) v[j] = b + j * NT < n ? buf[b + j * NT] : 0ull;
+#pragma unroll
+            for (int j = 0; j < U; ++j)
+                if (b + j * NT < n) out[b + j * NT] = key_of_raw(v[j]);
+        }
         if (tid == 0) *out_count = n;
         sync();
     }
