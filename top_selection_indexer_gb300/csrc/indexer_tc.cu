@@ -11,9 +11,11 @@
 //          row's admission threshold, about c k keys of the row lie above it;
 //       2. (capped) on all keys, admitting only scores at or above that threshold: about
 //          c k appends per row instead of the ~k ln(L / k) of a selector that starts from
-//          nothing; the buffer is sized so that it never needs a room check, and each row
-//          leaves every key it holds, unordered, for the ranking kernel (which keeps the
-//          k best);
+//          nothing; the buffer is sized so that it never needs a room check, an append is
+//          the raw (score bits, position) pair (the rank key is built once, when the unit
+//          ends), the rounds over tiles wholly inside the row skip the bounds tests, and
+//          each row leaves every key it holds, unordered, for the ranking kernel (which
+//          keeps the k best);
 //       3. (select: room checks, compactions) on the units where some row ended with
 //          fewer than k keys admitted or overflowed its buffer (the sample misjudged it),
 //          from no threshold at all: the result is exact for any input.

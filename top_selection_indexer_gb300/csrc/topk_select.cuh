@@ -8,7 +8,8 @@
 // Engineering" (Chinese translation) §3.2 asks for, with the lower-index tie rule).
 //
 // A group of NT threads owns one selector: a buffer of CAP keys, an admission
-// threshold `thr` and a 256-bin histogram.  Keys >= thr are appended; when the buffer
+// threshold `thr` and a 256-bin histogram.  (The capped offers append raw (score bits,
+// position) pairs instead, turned into keys in one pass before anything compares them.)  Keys >= thr are appended; when the buffer
 // is nearly full a radix select over the key bits finds the bound T with exactly k
 // keys >= T, drops the rest and raises thr to T.  Invariant: every dropped key is
 // smaller than k kept keys, so the buffer always holds the top k of all offered keys.
