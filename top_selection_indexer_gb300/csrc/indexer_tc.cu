@@ -532,9 +532,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 continue;
             }
             // Start from the row's admission threshold (its keys with a score at or above
-            // tau), or from nothing.
+            // tau), or from nothing: always for a row whose keys all fit the buffer (the
+            // threshold launch may skip such rows).
             float tau = -__int_as_float(0x7f800000);
-            if (p.tau_in && row_ok) tau = p.tau_in[row];
+            if (p.tau_in && row_ok && n_row > L::kCap) tau = p.tau_in[row];
             const bool has_tau = tau > -__int_as_float(0x7f800000);
             sel.reset(has_tau ? static_cast<uint64_t>(score_order_bits(tau)) << 32 : 0ull);
             const uint32_t pos0 = static_cast<uint32_t>(U.key_lo + p.key_offset) + off;
@@ -915,15 +916,35 @@ cudaError_t launch_qk(const IndexerArgs& a, void* workspace, cudaStream_t st) {
         p.t_end = a.T;
         p.n_units = static_cast<int>(n_units_of(QK, a.B, a.T));
         const int grid = p.n_units < sm_count() ? p.n_units : sm_count();
-        // 1. thresholds from the sample
+        // 1. thresholds from the sample, for the units (longest first) that hold a row with
+        // more keys than the buffer: without per-sequence lengths they are the first B J
+        // units, row group j having t_hi = T - 1 - R j; the full launch gives rows that fit
+        // the buffer no threshold
+        int64_t thr_units = p.n_units;
+        if (!a.kv_len) {
+            int64_t J = 0;
+            for (;; ++J) {
+                const int64_t t_hi = static_cast<int64_t>(a.T) - 1 - static_cast<int64_t>(R) * J;
+                if (t_hi < 0) break;
+                const int64_t pos = static_cast<int64_t>(p.S_total) - a.T + t_hi - a.key_offset;
+                int64_t n = pos >= 0 ? (pos >> kSampleShift) + 1 : 0;
+                if (n > S_s) n = S_s;
+                if ((n << kSampleShift) <= L::kCap) break;
+            }
+            thr_units = static_cast<int64_t>(a.B) * J;
+        }
         TcParams ps = p;
         ps.S = S_s;
         ps.key_shift = kSampleShift;
         ps.topk = sample_topk(a.topk);
         ps.tau_out = sw.tau;
-        tsi_indexer_tc_kernel<QK, R, kCapMode><<<grid, kThreads, smem, st>>>(ts, tq, ps);
-        note_launches(1);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        ps.n_units = static_cast<int>(thr_units);
+        if (thr_units > 0) {
+            const int grid_thr = thr_units < sm_count() ? static_cast<int>(thr_units) : sm_count();
+            tsi_indexer_tc_kernel<QK, R, kCapMode><<<grid_thr, kThreads, smem, st>>>(ts, tq, ps);
+            note_launches(1);
+            if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        }
         // 2. every key, admitted from the thresholds; short units listed
         TcParams pf = p;
         pf.tau_in = sw.tau;
